@@ -1,0 +1,187 @@
+/*
+ * ref_scan.c -- fp64 CPU oracle for the fused selective-scan forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * definition that the CUDA path is checked against.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg load it.  It shares no code,
+ * header, helper or constant with the CUDA library, and it includes none of it.
+ *
+ * Sources (page, then section):
+ *   [P1] the article at pwwt.cn/news/6372990 on Mamba's hardware-aware
+ *        algorithm and parallel associative scan:
+ *        s1.1 the discretised recurrence h_t = Abar_t h_{t-1} + Bbar_t x_t,
+ *        y_t = C_t h_t + D x_t;  s2.1 an update step as the affine map (a, b)
+ *        and the composition rule;  s2.3 padded steps as the identity (1, 0);
+ *        s2.4 Abar = exp(delta * A) with A < 0 and delta > 0, fp32 (here fp64)
+ *        accumulation;  s3.3 the fused quantities (discretise, b = Bbar x,
+ *        scan, C contraction, D residual);  s3.4 per-chunk boundary states;
+ *        s4.1 the naive serial loop with a zero initial state.
+ *   [P2] "Mamba并行扫描与硬件感知优化：从SSM递推到GPU高效实现"
+ *        (bjdmk.com.cn/news/5218626):
+ *        s2.2 the operator pair (A_t, b_t) and its merge rule;  s4.2 the
+ *        element-wise (diagonal) state transition, states of shape (..., N).
+ *
+ * Readings where the pages leave a step open (each is also listed in the
+ * design notes of the repository):
+ *   - The transition is diagonal: one scalar decay per (channel d, state n).
+ *   - Bbar x is taken as delta * B * x (the pages name zero-order hold but
+ *     write no formula for Bbar; delta * B is its first-order form).
+ *   - delta arrives already positive (after softplus); it is not transformed.
+ *   - The optional gate multiplies the whole output by silu(z) = z / (1+e^-z),
+ *     after the D residual is added.
+ *   - h_0 = 0.  Steps t >= valid_len[b] are the identity map (a=1, b=0): the
+ *     state is frozen and the output there is exactly 0.
+ *   - The chunk boundary state of chunk c is the global state h at step
+ *     min((c+1)*chunk_len, L) - 1.
+ *
+ * Inputs are read as the exact stored values (fp32, or bf16 widened exactly)
+ * and widened to double; everything after that is double arithmetic with the
+ * C library's exp().
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef REF_PLANT
+#define REF_PLANT 0 /* >0 only in the mutation tests: plants one known mistake */
+#endif
+
+enum { REF_F32 = 0, REF_BF16 = 1 };
+
+/* Exact widening of one stored element to double.  A bf16 value is the upper
+ * 16 bits of the fp32 with the same sign, exponent and leading mantissa bits. */
+static double ref_load(const void* p, int dtype, int64_t i) {
+  if (dtype == REF_F32) return (double)((const float*)p)[i];
+  uint32_t u = (uint32_t)((const uint16_t*)p)[i] << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* [P1 s2.1], [P2 s2.2]: applying (a1, b1) and then (a2, b2) to h gives
+ * a2 (a1 h + b1) + b2, i.e. the pair (a1 a2, a2 b1 + b2).  The b part is
+ * order sensitive. */
+void ref_combine(double a1, double b1, double a2, double b2, double* a_out, double* b_out) {
+#if REF_PLANT == 1
+  /* planted mistake: operands of the b part swapped */
+  *a_out = a1 * a2;
+  *b_out = a1 * b2 + b1;
+#else
+  *a_out = a1 * a2;
+  *b_out = a2 * b1 + b2;
+#endif
+}
+
+/* [P1 s4.1]: the serial first-order recurrence h_t = a_t h_{t-1} + b_t,
+ * starting from h_{-1} = h0.  h[t] receives the state after step t. */
+void ref_linear_recurrence(const double* a, const double* b, int64_t L, double h0, double* h) {
+  double s = h0;
+  for (int64_t t = 0; t < L; ++t) {
+    s = a[t] * s + b[t];
+    h[t] = s;
+  }
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double ref_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/*
+ * The selective-scan forward over all (b, d) channels.
+ *
+ * Layouts (row-major, contiguous): x, delta, z, y are [batch, seqlen, dim];
+ * B, C are [batch, seqlen, dstate] (shared by every channel d); A is
+ * [dim, dstate] fp32; D is [dim] fp32 (NULL = no residual); z NULL = no gate;
+ * valid_len is [batch] int32 (NULL = every step valid).  y_out receives
+ * [batch, seqlen, dim] doubles.  states_out (NULL = not wanted, also when
+ * chunk_len <= 0) receives [batch, ceil(seqlen/chunk_len), dim, dstate] doubles.
+ * nthreads <= 0 lets OpenMP choose.  The (b, d) loop is parallel only for
+ * speed: each channel is computed by exactly one thread, in program order.
+ * Returns 0, or -1 on bad sizes or a failed allocation.
+ */
+int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const int32_t* valid_len, double* y_out,
+                 double* states_out, int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                 int64_t chunk_len, int dtype, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate < 1) return -1;
+  if (dtype != REF_F32 && dtype != REF_BF16) return -1;
+  const int want_states = (states_out != NULL && chunk_len > 0);
+  const int64_t n_chunks = want_states ? (seqlen + chunk_len - 1) / chunk_len : 0;
+  const int64_t channels = batch * dim;
+  int failed = 0;
+
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : failed)
+#endif
+  for (int64_t bd = 0; bd < channels; ++bd) {
+    const int64_t b = bd / dim, d = bd % dim;
+    double* h = (double*)malloc((size_t)dstate * sizeof(double));
+    if (!h) { failed = 1; continue; }
+    for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0; /* [P1 s4.1] h_0 = 0 */
+
+    int64_t Lv = seqlen; /* [P1 s2.3] steps from valid_len on are the identity */
+    if (valid_len) {
+      Lv = valid_len[b];
+      if (Lv < 0) Lv = 0;
+      if (Lv > seqlen) Lv = seqlen;
+    }
+
+    for (int64_t t = 0; t < seqlen; ++t) {
+      const int64_t e = (b * seqlen + t) * dim + d; /* element (b, t, d) */
+      const int64_t r = (b * seqlen + t) * dstate;  /* row (b, t, :) of B and C */
+      double y = 0.0;
+      if (t < Lv) {
+        const double dt = ref_load(delta, dtype, e);
+        const double xv = ref_load(x, dtype, e);
+        double acc = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) {
+          const double An = (double)A[d * dstate + n];
+#if REF_PLANT == 2
+          const double a = exp(-dt);                       /* planted: decay without A */
+#elif REF_PLANT == 3
+          const double a = exp(dt * fabs(An));             /* planted: sign of A lost */
+#else
+          const double a = exp(dt * An);                   /* [P1 s2.4] Abar = exp(delta A) */
+#endif
+#if REF_PLANT == 4
+          const double bb = ref_load(B, dtype, r + n) * xv; /* planted: delta dropped */
+#else
+          const double bb = dt * ref_load(B, dtype, r + n) * xv; /* [P1 s3.3] b = Bbar x */
+#endif
+          h[n] = a * h[n] + bb;                            /* [P1 s1.1] the recurrence */
+          acc += ref_load(C, dtype, r + n) * h[n];         /* y = C h */
+        }
+#if REF_PLANT == 5
+        y = acc;                                           /* planted: D residual dropped */
+#else
+        y = acc + (D ? (double)D[d] * xv : 0.0);           /* [P1 s1.1] + D x */
+#endif
+        if (z) {
+#if REF_PLANT == 6
+          y *= ref_silu(xv);                               /* planted: gate on x */
+#else
+          y *= ref_silu(ref_load(z, dtype, e));            /* gate y * silu(z) */
+#endif
+        }
+      }
+      y_out[e] = y;
+#if REF_PLANT == 7
+      if (want_states && ((t + 2) % chunk_len == 0 || t == seqlen - 1)) { /* planted: off by one */
+#else
+      if (want_states && ((t + 1) % chunk_len == 0 || t == seqlen - 1)) { /* [P1 s3.4] */
+#endif
+        double* s = states_out + ((b * n_chunks + t / chunk_len) * dim + d) * dstate;
+        for (int64_t n = 0; n < dstate; ++n) s[n] = h[n];
+      }
+    }
+    free(h);
+  }
+  return failed ? -1 : 0;
+}
+
+/* Version tag so a loader can tell which oracle build (plain or planted) it has. */
+int ref_plant_id(void) { return REF_PLANT; }

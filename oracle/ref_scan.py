@@ -1,0 +1,121 @@
+"""ctypes front end of the fp64 CPU oracle (``ref_scan.c``).
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the plain definition of the selective
+scan forward that the CUDA library is checked against.  Only the test suite,
+``__graft_entry__.smoke()`` and the benchmark's ``cpu_baseline`` leg may import
+this module.  It imports nothing from the CUDA package and the CUDA package
+imports nothing from it.
+
+Arrays are numpy: fp32 tensors as ``float32``; bf16 tensors as ``uint16``
+holding the raw bf16 bit patterns.  Results are ``float64``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ref_scan.c")
+_LIB_CACHE: dict[str, ctypes.CDLL] = {}
+
+
+def lib_path(plant: int = 0) -> str:
+    name = "libref_scan.so" if plant == 0 else f"libref_scan_plant{plant}.so"
+    return os.path.join(_HERE, name)
+
+
+def build(plant: int = 0, force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP, no fast-math).  ``plant`` > 0
+    builds a mutant with one known mistake, for the tests that check the pins
+    catch it."""
+    out = lib_path(plant)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
+               f"-DREF_PLANT={int(plant)}", _SRC, "-o", out + ".tmp", "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(out + ".tmp", out)
+    return out
+
+
+def _load(plant: int = 0) -> ctypes.CDLL:
+    key = str(plant)
+    if key in _LIB_CACHE:
+        return _LIB_CACHE[key]
+    lib = ctypes.CDLL(build(plant))
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.ref_scan_fwd.restype = I32
+    lib.ref_scan_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I32, I32]
+    D = ctypes.c_double
+    lib.ref_combine.restype = None
+    lib.ref_combine.argtypes = [D, D, D, D, ctypes.POINTER(D), ctypes.POINTER(D)]
+    lib.ref_linear_recurrence.restype = None
+    lib.ref_linear_recurrence.argtypes = [P, P, I64, D, P]
+    lib.ref_plant_id.restype = I32
+    _LIB_CACHE[key] = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def combine(a1: float, b1: float, a2: float, b2: float, plant: int = 0) -> tuple[float, float]:
+    """The affine composition: (a1, b1) first, then (a2, b2)."""
+    ao, bo = ctypes.c_double(), ctypes.c_double()
+    _load(plant).ref_combine(a1, b1, a2, b2, ctypes.byref(ao), ctypes.byref(bo))
+    return ao.value, bo.value
+
+
+def linear_recurrence(a, b, h0: float = 0.0, plant: int = 0) -> np.ndarray:
+    """h_t = a_t h_{t-1} + b_t from h_{-1} = h0, for 1-D arrays a and b."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    assert a.shape == b.shape and a.ndim == 1
+    h = np.empty_like(a)
+    _load(plant).ref_linear_recurrence(_ptr(a), _ptr(b), a.shape[0], float(h0), _ptr(h))
+    return h
+
+
+def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int = 0,
+             threads: int = 0, plant: int = 0):
+    """Run the oracle.  Returns ``(y, states)``: y is float64 [batch, L, dim];
+    states is float64 [batch, ceil(L/chunk_len), dim, dstate], or None when
+    ``chunk_len`` is 0."""
+    if x.dtype == np.float32:
+        dtype = 0
+    elif x.dtype == np.uint16:
+        dtype = 1
+    else:
+        raise TypeError("x must be float32 or uint16 (bf16 bits)")
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    for name, t, shape in (("delta", delta, (batch, L, dim)), ("B", B, (batch, L, dstate)),
+                           ("C", C, (batch, L, dstate))):
+        if t.shape != shape or t.dtype != x.dtype:
+            raise ValueError(f"{name}: expected {shape} {x.dtype}, got {t.shape} {t.dtype}")
+    if A.shape != (dim, dstate) or A.dtype != np.float32:
+        raise ValueError("A must be float32 [dim, dstate]")
+    if D is not None and (D.shape != (dim,) or D.dtype != np.float32):
+        raise ValueError("D must be float32 [dim]")
+    if z is not None and (z.shape != (batch, L, dim) or z.dtype != x.dtype):
+        raise ValueError("z must match x")
+    if valid_len is not None and (valid_len.shape != (batch,) or valid_len.dtype != np.int32):
+        raise ValueError("valid_len must be int32 [batch]")
+    arrs = [np.ascontiguousarray(t) if t is not None else None
+            for t in (x, delta, A, B, C, D, z, valid_len)]
+    y = np.empty((batch, L, dim), dtype=np.float64)
+    states = None
+    if chunk_len > 0:
+        states = np.empty((batch, (L + chunk_len - 1) // chunk_len, dim, dstate), dtype=np.float64)
+    rc = _load(plant).ref_scan_fwd(*[_ptr(t) for t in arrs], _ptr(y), _ptr(states),
+                                   batch, L, dim, dstate, int(chunk_len), dtype, int(threads))
+    if rc != 0:
+        raise RuntimeError("ref_scan_fwd failed")
+    return y, states
+
+
+def plant_id(plant: int = 0) -> int:
+    return _load(plant).ref_plant_id()

@@ -1,0 +1,328 @@
+"""Pins of the fp64 oracle: checks against what the pages and the mathematics
+fix, independently of the oracle's own loop.  Each pin is a function taking
+``plant`` (0 = the real oracle, k > 0 = a build of the oracle with planted
+mistake k) and raising AssertionError when the oracle disagrees.
+
+Page keys:
+  [P1] the article at pwwt.cn/news/6372990 on Mamba's hardware-aware algorithm
+       and parallel associative scan.
+  [P2] "Mamba并行扫描与硬件感知优化：从SSM递推到GPU高效实现" (bjdmk.com.cn/news/5218626).
+  [P3] the article at m.nxbn.cn/news/191302 (only its unrolled-sum formula of
+       s1 is used, as the brute-force form of the recurrence).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+from oracle import ref_scan as R
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden_closed_form() -> np.ndarray:
+    vals = [float(l) for l in open(os.path.join(GOLDEN, "closed_form_a05_b1_L8.txt"))
+            if l.strip() and not l.startswith("#")]
+    return np.array(vals)
+
+
+def golden_bf16() -> list[tuple[int, float]]:
+    out = []
+    for l in open(os.path.join(GOLDEN, "bf16_widening.txt")):
+        if l.strip() and not l.startswith("#"):
+            bits, val = l.split()
+            out.append((int(bits, 16), float(val)))
+    return out
+
+
+def _fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len=0, plant=0, threads=1):
+    return R.scan_fwd(x, delta, A, B, C, D, z, valid_len, chunk_len=chunk_len, threads=threads,
+                      plant=plant)
+
+
+def _rand_inputs(rng, batch, L, dim, N, gate=False, mask=None):
+    x = rng.standard_normal((batch, L, dim)).astype(np.float32)
+    delta = np.exp(rng.uniform(np.log(1e-2), np.log(0.5), (batch, L, dim))).astype(np.float32)
+    A = -np.exp(rng.uniform(np.log(0.5), np.log(4.0), (dim, N))).astype(np.float32)
+    B = rng.standard_normal((batch, L, N)).astype(np.float32)
+    C = rng.standard_normal((batch, L, N)).astype(np.float32)
+    D = rng.standard_normal(dim).astype(np.float32)
+    z = rng.standard_normal((batch, L, dim)).astype(np.float32) if gate else None
+    return x, delta, A, B, C, D, z
+
+
+# ---------------------------------------------------------------------------
+# The combine and the serial recurrence
+
+
+def pin_closed_form_recurrence(plant=0):
+    """[P1] s2.3 note, s4.1: a = 0.5, b = 1, 8 steps, h = 2 (1 - 0.5^k)."""
+    h = R.linear_recurrence(np.full(8, 0.5), np.ones(8), plant=plant)
+    assert np.array_equal(h, golden_closed_form()), h
+
+
+def pin_closed_form_forward(plant=0):
+    """The same closed form driven through the full forward: N = 1, dim = 1,
+    delta = 1, A = -ln 2 (so exp(delta A) = 1/2), B = C = 1, x = 1, D = 0, so y_t = h_t."""
+    L = 8
+    one = np.ones((1, L, 1), np.float32)
+    A = np.array([[-math.log(2.0)]], np.float32)
+    y, _ = _fwd(one, one, A, np.ones((1, L, 1), np.float32), np.ones((1, L, 1), np.float32),
+                D=np.zeros(1, np.float32), plant=plant)
+    np.testing.assert_allclose(y[0, :, 0], golden_closed_form(), rtol=1e-7, atol=0)
+
+
+def pin_combine_is_composition(plant=0):
+    """[P1] s2.1, [P2] s2.2: combine((a1,b1),(a2,b2)) applied to h equals applying
+    (a1,b1) first and (a2,b2) second."""
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        a1, b1, a2, b2, h = rng.uniform(-2, 2, 5)
+        a, b = R.combine(a1, b1, a2, b2, plant=plant)
+        direct = a2 * (a1 * h + b1) + b2
+        assert abs((a * h + b) - direct) <= 1e-12 * max(1.0, abs(direct)), (a1, b1, a2, b2)
+
+
+def _tree_reduce(ops, rng, plant):
+    if len(ops) == 1:
+        return ops[0]
+    k = int(rng.integers(1, len(ops)))
+    l = _tree_reduce(ops[:k], rng, plant)
+    r = _tree_reduce(ops[k:], rng, plant)
+    return R.combine(l[0], l[1], r[0], r[1], plant=plant)
+
+
+def pin_associativity_bruteforce(plant=0):
+    """[P1] s2.1, [P2] s2.2: the combine is associative.  All five bracketings of
+    four random ops agree, and random bracketings of up to 16 ops agree with the
+    left fold, to 1e-12 in fp64."""
+    rng = np.random.default_rng(12)
+    c = lambda p, q: R.combine(p[0], p[1], q[0], q[1], plant=plant)
+    for _ in range(50):
+        o = [tuple(rng.uniform(-1.5, 1.5, 2)) for _ in range(4)]
+        forms = [c(c(c(o[0], o[1]), o[2]), o[3]), c(c(o[0], c(o[1], o[2])), o[3]),
+                 c(c(o[0], o[1]), c(o[2], o[3])), c(o[0], c(c(o[1], o[2]), o[3])),
+                 c(o[0], c(o[1], c(o[2], o[3])))]
+        for f in forms[1:]:
+            assert abs(f[0] - forms[0][0]) < 1e-12 and abs(f[1] - forms[0][1]) < 1e-12
+    for n in range(2, 17):
+        ops = [tuple(rng.uniform(-1.2, 1.2, 2)) for _ in range(n)]
+        left = ops[0]
+        for o in ops[1:]:
+            left = c(left, o)
+        for _ in range(5):
+            t = _tree_reduce(ops, rng, plant)
+            assert abs(t[0] - left[0]) < 1e-12 and abs(t[1] - left[1]) < 1e-12
+
+
+def pin_recurrence_is_prefix_of_combines(plant=0):
+    """The serial recurrence from h = 0 equals the b part of the inclusive prefix
+    of combines (h_t = prefix_t applied to 0), [P1] s2.2."""
+    rng = np.random.default_rng(13)
+    a = rng.uniform(0, 1, 40)
+    b = rng.standard_normal(40)
+    h = R.linear_recurrence(a, b, plant=plant)
+    acc = (a[0], b[0])
+    assert abs(h[0] - acc[1]) < 1e-12
+    for t in range(1, 40):
+        acc = R.combine(acc[0], acc[1], a[t], b[t], plant=plant)
+        assert abs(h[t] - acc[1]) < 1e-12 * max(1, abs(acc[1]))
+
+
+def pin_reverse_identity(plant=0):
+    """[P1] s2.3: the backward recurrence g_t = a_{t+1} g_{t+1} + c_t (g_{L-1} = c_{L-1})
+    equals the forward recurrence run on the flipped sequence with the a's
+    shifted by one."""
+    rng = np.random.default_rng(14)
+    L = 33
+    a = rng.uniform(0, 1, L)
+    c = rng.standard_normal(L)
+    g = np.empty(L)
+    g[L - 1] = c[L - 1]
+    for t in range(L - 2, -1, -1):
+        g[t] = a[t + 1] * g[t + 1] + c[t]
+    a_shift = np.concatenate([a[1:], [0.0]])  # the coefficient that multiplies g_{t+1}
+    fwd = R.linear_recurrence(a_shift[::-1].copy(), c[::-1].copy(), plant=plant)
+    np.testing.assert_allclose(fwd[::-1], g, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# The full forward
+
+
+def pin_lti_convolution(plant=0):
+    """[P1] s1.2, [P2] s1.3: with delta, B and C constant in time the SSM is a
+    causal convolution, y_t = sum_k K_k x_{t-k} + D x_t with
+    K_k = sum_n C_n exp(delta A_n)^k delta B_n.  Checked with numpy's convolution."""
+    rng = np.random.default_rng(15)
+    L, dim, N = 64, 3, 5
+    x = rng.standard_normal((1, L, dim)).astype(np.float32)
+    dts = np.array([0.05, 0.3, 1.0], np.float32)
+    delta = np.broadcast_to(dts, (1, L, dim)).astype(np.float32).copy()
+    A = -rng.uniform(0.2, 3.0, (dim, N)).astype(np.float32)
+    Bn = rng.standard_normal(N).astype(np.float32)
+    Cn = rng.standard_normal(N).astype(np.float32)
+    B = np.broadcast_to(Bn, (1, L, N)).astype(np.float32).copy()
+    C = np.broadcast_to(Cn, (1, L, N)).astype(np.float32).copy()
+    D = rng.standard_normal(dim).astype(np.float32)
+    y, _ = _fwd(x, delta, A, B, C, D=D, plant=plant)
+    k = np.arange(L)
+    for d in range(dim):
+        dt = float(dts[d])
+        abar = np.exp(dt * A[d].astype(np.float64))
+        K = (Cn.astype(np.float64)[None, :] * abar[None, :] ** k[:, None]
+             * (dt * Bn.astype(np.float64))[None, :]).sum(1)
+        xd = x[0, :, d].astype(np.float64)
+        ref = np.convolve(xd, K)[:L] + float(D[d]) * xd
+        np.testing.assert_allclose(y[0, :, d], ref, rtol=1e-10, atol=1e-12)
+
+
+def pin_unrolled_sum_bruteforce(plant=0):
+    """[P3] s1 unrolled form, [P1] s2.1: h_T = sum_s (prod_{j=s+1..T} a_j) b_s
+    with a_j = exp(delta_j A), b_s = delta_s B_s x_s, evaluated with explicit
+    products on a tiny time-varying input; y = C h + D x."""
+    rng = np.random.default_rng(16)
+    batch, L, dim, N = 2, 11, 3, 4
+    x, delta, A, B, C, D, _ = _rand_inputs(rng, batch, L, dim, N)
+    y, _ = _fwd(x, delta, A, B, C, D=D, plant=plant)
+    f = lambda v: v.astype(np.float64)
+    for b in range(batch):
+        for d in range(dim):
+            for T in range(L):
+                h = np.zeros(N)
+                for s in range(T + 1):
+                    prod = np.ones(N)
+                    for j in range(s + 1, T + 1):
+                        prod *= np.exp(f(delta[b, j, d]) * f(A[d]))
+                    h += prod * f(delta[b, s, d]) * f(B[b, s]) * f(x[b, s, d])
+                ref = float((f(C[b, T]) * h).sum() + f(D[d]) * f(x[b, T, d]))
+                assert abs(y[b, T, d] - ref) <= 1e-11 * max(1.0, abs(ref)), (b, T, d)
+
+
+def pin_d_residual(plant=0):
+    """[P1] s1.1: with C = 0 the output is exactly D x; with D absent and C = 0 it is 0."""
+    rng = np.random.default_rng(17)
+    x, delta, A, B, C, D, _ = _rand_inputs(rng, 2, 9, 4, 3)
+    C0 = np.zeros_like(C)
+    y, _ = _fwd(x, delta, A, B, C0, D=D, plant=plant)
+    np.testing.assert_array_equal(y, D.astype(np.float64)[None, None, :] * x.astype(np.float64))
+    y0, _ = _fwd(x, delta, A, B, C0, D=None, plant=plant)
+    assert np.all(y0 == 0)
+
+
+def pin_gate(plant=0):
+    """The gate multiplies the whole output by silu(z) = z sigmoid(z) (sigmoid
+    from scipy), and z = 0 gives exactly 0."""
+    from scipy.special import expit
+    rng = np.random.default_rng(18)
+    x, delta, A, B, C, D, z = _rand_inputs(rng, 2, 17, 5, 4, gate=True)
+    y, _ = _fwd(x, delta, A, B, C, D=D, plant=plant)
+    yg, _ = _fwd(x, delta, A, B, C, D=D, z=z, plant=plant)
+    zz = z.astype(np.float64)
+    np.testing.assert_allclose(yg, y * zz * expit(zz), rtol=1e-12, atol=1e-14)
+    yz, _ = _fwd(x, delta, A, B, C, D=D, z=np.zeros_like(z), plant=plant)
+    assert np.all(yz == 0)
+
+
+def pin_masking(plant=0):
+    """[P1] s2.3, s5.3: steps at or past valid_len are the identity (a=1, b=0):
+    a row with valid_len = k matches an unpadded run of length k for t < k,
+    its outputs after that are exactly 0 and its chunk states stay frozen at
+    h_{k-1}.  valid_len is clamped to [0, L]."""
+    rng = np.random.default_rng(19)
+    batch, L, dim, N, chunk = 4, 24, 3, 4, 5
+    x, delta, A, B, C, D, z = _rand_inputs(rng, batch, L, dim, N, gate=True)
+    vl = np.array([7, 0, 30, -3], np.int32)  # 30 -> L, -3 -> 0
+    y, s = _fwd(x, delta, A, B, C, D=D, z=z, valid_len=vl, chunk_len=chunk, plant=plant)
+    for b, k in enumerate([7, 0, 24, 0]):
+        if k > 0:
+            yk, sk = _fwd(x[b:b + 1, :k].copy(), delta[b:b + 1, :k].copy(), A, B[b:b + 1, :k].copy(),
+                          C[b:b + 1, :k].copy(), D=D, z=z[b:b + 1, :k].copy(), chunk_len=k,
+                          plant=plant)
+            np.testing.assert_allclose(y[b, :k], yk[0], rtol=1e-13, atol=1e-14)
+            frozen = sk[0, -1]
+        else:
+            frozen = np.zeros((dim, N))
+        assert np.all(y[b, k:] == 0)
+        # chunks that end at or after k hold the frozen state
+        for c in range(s.shape[1]):
+            t_end = min((c + 1) * chunk, L) - 1
+            if t_end >= k - 1 and k < L:
+                np.testing.assert_allclose(s[b, c], frozen, rtol=1e-13, atol=1e-14)
+
+
+def pin_chunk_states_and_carry(plant=0):
+    """[P1] s3.4: chunk c stores h at step min((c+1) chunk, L) - 1; and [P2] s4.2:
+    the state inside the next chunk equals its zero-start local state plus the
+    running product of a times the carried state (h = h_local + cumprod(a) h_in)."""
+    rng = np.random.default_rng(20)
+    batch, L, dim, N, chunk = 2, 23, 3, 4, 6
+    x, delta, A, B, C, D, _ = _rand_inputs(rng, batch, L, dim, N)
+    _, s = _fwd(x, delta, A, B, C, D=D, chunk_len=chunk, plant=plant)
+    assert s.shape == (batch, 4, dim, N)
+    f = lambda v: v.astype(np.float64)
+    for b in range(batch):
+        for d in range(dim):
+            a = np.exp(f(delta[b, :, d])[:, None] * f(A[d])[None, :])        # [L, N]
+            bb = (f(delta[b, :, d]) * f(x[b, :, d]))[:, None] * f(B[b])        # [L, N]
+            h = np.zeros(N)
+            hs = []
+            for t in range(L):
+                h = a[t] * h + bb[t]
+                hs.append(h.copy())
+            hs = np.array(hs)
+            for c in range(4):
+                t_end = min((c + 1) * chunk, L) - 1
+                np.testing.assert_allclose(s[b, c, d], hs[t_end], rtol=1e-12, atol=1e-14)
+            for c in range(1, 4):  # carry identity across chunk c-1 -> c
+                t0, t1 = c * chunk, min((c + 1) * chunk, L)
+                hl = np.zeros(N)
+                for t in range(t0, t1):
+                    hl = a[t] * hl + bb[t]
+                carried = hl + np.prod(a[t0:t1], axis=0) * s[b, c - 1, d]
+                np.testing.assert_allclose(carried, s[b, c, d], rtol=1e-12, atol=1e-14)
+
+
+def pin_bf16_widening(plant=0):
+    """bf16 inputs are read as their exact values: known bit patterns widen to
+    the hand-computed numbers, and a bf16 run equals the fp32 run on the
+    widened values bit for bit."""
+    vals = golden_bf16()
+    bits = np.array([b for b, _ in vals], np.uint16).reshape(1, -1, 1)
+    L = bits.shape[1]
+    ones16 = np.full((1, L, 1), 0x3F80, np.uint16)  # 1.0
+    zero16 = np.zeros((1, L, 1), np.uint16)
+    A = np.zeros((1, 1), np.float32)  # a = 1
+    # x = bits, delta = 1, B = 0, C = 0: y = D x with D = 1 -> y is the widened x
+    y, _ = _fwd(bits, ones16, A, zero16, zero16, D=np.ones(1, np.float32), plant=plant)
+    for i, (_, v) in enumerate(vals):
+        assert y[0, i, 0] == v, (i, v)
+    rng = np.random.default_rng(21)
+    x, delta, A, B, C, D, z = _rand_inputs(rng, 2, 13, 3, 4, gate=True)
+    from selective_state_space_fwd_gb300.workloads import f32_to_bf16_bits, bf16_bits_to_f32
+    t16 = [f32_to_bf16_bits(t) for t in (x, delta, B, C, z)]
+    t32 = [bf16_bits_to_f32(t) for t in t16]
+    y16, _ = _fwd(t16[0], t16[1], A, t16[2], t16[3], D=D, z=t16[4], plant=plant)
+    y32, _ = _fwd(t32[0], t32[1], A, t32[2], t32[3], D=D, z=t32[4], plant=plant)
+    assert np.array_equal(y16, y32)
+
+
+def pin_long_sequence_sane(plant=0):
+    """[P1] s4.1: with a in (0,1) and b ~ N(0,1) a long run stays finite, and
+    with a bounded by a_max the state is bounded by max|b| / (1 - a_max)."""
+    rng = np.random.default_rng(22)
+    L = 20000
+    a = rng.uniform(0.0, 0.99, L)
+    b = rng.standard_normal(L)
+    h = R.linear_recurrence(a, b, plant=plant)
+    assert np.all(np.isfinite(h))
+    assert np.max(np.abs(h)) <= np.max(np.abs(b)) / (1 - 0.99) + 1e-9
+
+
+ALL_PINS = [pin_closed_form_recurrence, pin_closed_form_forward, pin_combine_is_composition,
+            pin_associativity_bruteforce, pin_recurrence_is_prefix_of_combines,
+            pin_reverse_identity, pin_lti_convolution, pin_unrolled_sum_bruteforce,
+            pin_d_residual, pin_gate, pin_masking, pin_chunk_states_and_carry,
+            pin_bf16_widening, pin_long_sequence_sane]
