@@ -1,0 +1,386 @@
+"""Benchmark of the fused selective-scan forward (libssmscan) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--kernel auto]
+    python bench.py --impl reference ...     # the fp64 CPU oracle as the reference arm
+
+A step is one forward over one batch of the workload (workload 2 by default:
+fp32, batch 8, L 4096, dim 1024, N 16).  Inputs are resident in HBM before the
+timed region; each step's kernel is bracketed by CUDA events on the launch
+stream and L2 is flushed between steps (a 256 MiB memset outside the events).
+Prints one JSON line.  Under torchrun every rank runs its own copy of the
+workload (weak scaling, no collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan fwd B·L·D elems/s and achieved % of roofline, 1×GB300"
+UNIT = "elements/s"
+# Per-SM unit rates of GB300 (sm_103a) used for the ALU roof: MUFU ex2 is 32
+# lanes/clk/SM (measured with a throughput probe), FP32 is 128 lanes/clk/SM.
+MUFU_PER_SM_CLK = 32
+FP32_PER_SM_CLK = 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_counts(w, inp) -> dict:
+    """Work the method must do for one forward (independent of the kernel):
+    valid (b,t,d) elements, exps, fp32 ops and HBM bytes (inputs read once,
+    y and chunk states written once; the O(B L D N) state is never stored)."""
+    L, Dm, N = w.seqlen, w.dim, w.dstate
+    if inp["valid_len"] is not None:
+        valid_rows = int(np.clip(inp["valid_len"], 0, L).sum())
+    else:
+        valid_rows = w.batch * L
+    ev = valid_rows * Dm
+    es = 2 if w.dtype == "bf16" else 4
+    n_act_in = 3 if w.gate else 2
+    nch = (L + w.chunk_len - 1) // w.chunk_len if w.chunk_len else 0
+    bytes_ = (n_act_in * ev * es                  # x, delta (, z) of valid steps
+              + w.batch * L * Dm * es              # y, every step
+              + 2 * valid_rows * N * es            # B, C rows of valid steps
+              + Dm * N * 4 + Dm * 4                # A, D
+              + (w.batch * 4 if inp["valid_len"] is not None else 0)
+              + w.batch * nch * Dm * N * 4)        # chunk states
+    exps = ev * N + (ev if w.gate else 0)
+    fp32 = 4 * ev * N + 2 * ev + (4 * ev if w.gate else 0)
+    return dict(elements=w.batch * L * Dm, valid_elements=ev, n_elements=ev * N, exps=exps,
+                fp32_ops=fp32, bytes=bytes_)
+
+
+def roof(counts, peaks, sms, sm_mhz) -> dict:
+    hbm = peaks["hbm_gbs"] * 1e9
+    clk = sm_mhz * 1e6
+    t_hbm = counts["bytes"] / hbm
+    t_mufu = counts["exps"] / (MUFU_PER_SM_CLK * sms * clk)
+    t_fp32 = counts["fp32_ops"] / (FP32_PER_SM_CLK * sms * clk)
+    return dict(t_hbm=t_hbm, t_mufu=t_mufu, t_fp32=t_fp32, t_roof=max(t_hbm, t_mufu, t_fp32))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 7]
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows]
+        smax = max(float(r[1]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[4 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[2]) for r in rows)}
+
+
+def cpu_sample_inputs(inp: dict, channels: int) -> dict:
+    """The first ``channels`` channels of every batch row: a bounded sample of
+    the same workload for the oracle (pure indexing)."""
+    out = dict(inp)
+    for k in ("x", "delta", "z"):
+        if inp[k] is not None:
+            out[k] = np.ascontiguousarray(inp[k][:, :, :channels])
+    out["A"] = np.ascontiguousarray(inp["A"][:channels])
+    out["D"] = np.ascontiguousarray(inp["D"][:channels]) if inp["D"] is not None else None
+    return out
+
+
+def time_oracle(inp: dict, target_s: float, threads: int) -> dict:
+    """Time the oracle on a bounded channel sample sized for about target_s."""
+    from oracle import ref_scan
+    ref_scan.build()
+    Bt, L, Dm = inp["x"].shape
+
+    def run(ch):
+        s = cpu_sample_inputs(inp, ch)
+        t0 = time.perf_counter()
+        ref_scan.scan_fwd(s["x"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"],
+                          s["valid_len"], chunk_len=inp["chunk_len"], threads=threads)
+        return time.perf_counter() - t0
+
+    ch = 1
+    dt = run(ch)
+    while dt < 0.5 and ch < Dm:
+        ch = min(Dm, ch * 4)
+        dt = run(ch)
+    ch_target = int(min(Dm, max(1, ch * target_s / max(dt, 1e-6))))
+    if ch_target != ch:
+        ch = ch_target
+        dt = run(ch)
+    elems = Bt * L * ch
+    return {"value": elems / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"all {Bt} batch rows x first {ch} of {Dm} channels x {L} steps "
+                      f"({elems} elements, {dt:.1f} s)", "seconds": dt}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--kernel", default="auto")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-flush", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reference_arm(args, w):
+    """The fp64 CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from selective_state_space_fwd_gb300 import workloads as W
+    inp = W.make_inputs(w)
+    threads = os.cpu_count() or 1
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    budget = 150.0 / (steps + warm)  # whole run within a few minutes
+    probe = time_oracle(inp, min(budget, 5.0), threads)
+    rate = probe["value"]
+    ch = max(1, min(w.dim, int(budget * rate / (w.batch * w.seqlen))))
+    from oracle import ref_scan
+    s = cpu_sample_inputs(inp, ch)
+
+    def step():
+        ref_scan.scan_fwd(s["x"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"],
+                          s["valid_len"], chunk_len=inp["chunk_len"], threads=threads)
+
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    elems = w.batch * w.seqlen * ch
+    val = elems / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
+                       "dstate": w.dstate},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"each step: all {w.batch} batch rows x first {ch} of "
+                                       f"{w.dim} channels x {w.seqlen} steps ({elems} elements)"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from selective_state_space_fwd_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import selective_state_space_fwd_gb300 as S
+    from selective_state_space_fwd_gb300 import build as B
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    B.build()
+    S.load()
+
+    inp = W.make_inputs(w)
+    t = W.to_torch(inp, dev)
+    counts = algorithmic_counts(w, inp)
+    kernel, grid = S.plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
+                          mask=w.mask is not None, chunk_len=w.chunk_len, kernel=args.kernel)
+    stream = torch.cuda.Stream(dev)
+    y = torch.empty_like(t["x"])
+    nch = (w.seqlen + w.chunk_len - 1) // w.chunk_len if w.chunk_len else 0
+    states = (torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+              if w.chunk_len else None)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
+                   chunk_len=w.chunk_len, out=y, out_states=states, kernel=args.kernel,
+                   stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms, one launch each
+    ms = sum(per_step) / K
+    if world > 1:
+        m = torch.tensor([ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        ms = float(m.item())
+    value = world * counts["elements"] / (ms * 1e-3)
+
+    # End to end through the C ABI with host buffers: H2D of the step's inputs from
+    # pinned memory, the forward, D2H of y (and chunk states), every step.
+    th = W.to_torch(inp, "cpu")
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in th.items()}
+    y_h = torch.empty(tuple(t["x"].shape), dtype=t["x"].dtype, pin_memory=True)
+    s_h = (torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32, pin_memory=True)
+           if w.chunk_len else None)
+    ws = torch.empty(S.host_workspace_bytes(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
+                                            has_D=True, gate=w.gate, mask=w.mask is not None,
+                                            chunk_len=w.chunk_len),
+                     dtype=torch.uint8, device=dev)
+
+    def step_host():
+        S.scan_fwd_host(pinned["x"], pinned["delta"], pinned["A"], pinned["B"], pinned["C"],
+                        pinned["D"], pinned["z"], pinned["valid_len"], chunk_len=w.chunk_len,
+                        out=y_h, out_states=s_h, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step_host()
+    torch.cuda.synchronize(dev)
+    KE = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        step_host()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / KE
+    if world > 1:
+        m = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        ms_e2e = float(m.item())
+    es = 2 if w.dtype == "bf16" else 4
+    h2d = sum(v.numel() * v.element_size() for k, v in pinned.items()
+              if isinstance(v, torch.Tensor))
+    d2h = y_h.numel() * es + (s_h.numel() * 4 if s_h is not None else 0)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peaks_src = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz_peak = float(peaks.get("sm_max_mhz", 2070.0))
+    r = roof(counts, peaks, sms, sm_mhz_peak)
+    t_meas = ms * 1e-3
+    if r["t_hbm"] >= max(r["t_mufu"], r["t_fp32"]):
+        achieved = counts["bytes"] / t_meas / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+    else:
+        pk = MUFU_PER_SM_CLK * sms * sm_mhz_peak * 1e6 / 1e9
+        achieved = counts["exps"] / t_meas / 1e9
+        roofline = {"bound": "alu", "achieved": achieved, "peak": pk, "unit": "Gex2/s",
+                    "frac": achieved / pk, "traffic": None}
+    roofline.update({
+        "peak_source": f"{peaks_src} (HBM copy GB/s); ALU = {MUFU_PER_SM_CLK} ex2 and "
+                       f"{FP32_PER_SM_CLK} fp32 lanes/clk/SM x {sms} SMs x {sm_mhz_peak:.0f} MHz",
+        "kernel": S.kernel_name(kernel), "grid": grid,
+        "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
+                    "fp32": r["t_fp32"] * 1e6},
+        "frac_of_roof": r["t_roof"] / t_meas,
+        "algorithmic": {"bytes": counts["bytes"], "exps": counts["exps"],
+                        "fp32_ops": counts["fp32_ops"]}})
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = time_oracle(inp, args.cpu_seconds, os.cpu_count() or 1)
+        cpu.pop("seconds", None)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
+                   "dstate": w.dstate, "gate": w.gate, "chunk_len": w.chunk_len,
+                   "masked": w.mask is not None,
+                   "l2": "flushed between steps (256 MiB memset outside the timed events)"
+                         if not args.no_flush else "not flushed",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * counts["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": K,
+        "clocks": clk,
+        "timed_wall_s": wall,
+        "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
+                        "max": max(per_step)},
+    }
+    if counts["valid_elements"] != counts["elements"]:
+        line["valid_elements_per_s"] = world * counts["valid_elements"] / (ms * 1e-3)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

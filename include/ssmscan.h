@@ -1,0 +1,173 @@
+/*
+ * ssmscan.h -- C ABI of libssmscan, the fused selective-scan forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (page, then section):
+ *   [P1] the article at pwwt.cn/news/6372990 on Mamba's hardware-aware
+ *        algorithm and parallel associative scan;
+ *   [P2] "Mamba并行扫描与硬件感知优化：从SSM递推到GPU高效实现"
+ *        (bjdmk.com.cn/news/5218626).
+ *
+ * For every batch row b, channel d and state n, with h_{-1} = 0 ([P1] s4.1):
+ *     a_t   = exp(delta[b,t,d] * A[d,n])              ([P1] s2.4: Abar = exp(delta A))
+ *     h_t   = a_t * h_{t-1} + delta[b,t,d] * B[b,t,n] * x[b,t,d]
+ *                                                     ([P1] s1.1 recurrence, s3.3 b = Bbar x)
+ *     y[b,t,d] = (sum_n C[b,t,n] * h_t + D[d] * x[b,t,d]) * silu(z[b,t,d])
+ *                                                     ([P1] s1.1 output and D residual;
+ *                                                      the gate is optional)
+ * The recurrence is evaluated as a parallel associative scan over (a, b)
+ * pairs with the combine (a1,b1) o (a2,b2) = (a1 a2, a2 b1 + b2)
+ * ([P1] s2.1, [P2] s2.2), or as a register-resident serial sweep where the
+ * batch and channel dimensions already fill the GPU.  The state h stays in
+ * registers: only x, delta, z, B, C, A, D are read and y (plus optional chunk
+ * boundary states, [P1] s3.4) is written.
+ *
+ * Steps t >= valid_len[b] are the identity step (a = 1, b = 0, [P1] s2.3): the
+ * state is frozen and y there is exactly 0.
+ *
+ * Conventions for every entry point below:
+ *   - All tensors are dense, row-major, contiguous.  Shapes:
+ *       x, delta, z, y : [batch, seqlen, dim]       dtype of the call
+ *       B, C           : [batch, seqlen, dstate]    dtype of the call (shared by all d)
+ *       A              : [dim, dstate]              fp32 (A < 0 expected, not required)
+ *       D              : [dim]                      fp32
+ *       valid_len      : [batch]                    int32
+ *       chunk states   : [batch, ceil(seqlen/chunk_len), dim, dstate]  fp32
+ *   - The caller owns every buffer; the library keeps no pointer after a call
+ *     returns and allocates no device memory on this path.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
+ *     synchronise the host.  Argument errors are detected on the host before
+ *     any launch and are returned as a status; nothing is launched then.  A
+ *     launch failure is returned as SSM_ERR_CUDA (cudaGetLastError() tells
+ *     which).  No entry point aborts, throws or traps.
+ *   - Inputs and outputs must not overlap.
+ */
+#ifndef SSMSCAN_H_
+#define SSMSCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_NULL = 1,        /* a required pointer is NULL */
+  SSM_ERR_SHAPE = 2,       /* a size is negative or zero where it must not be, or overflows */
+  SSM_ERR_UNSUPPORTED = 3, /* dstate not in {1,2,4,8,16,32,64}, unknown dtype, kernel or flag */
+  SSM_ERR_ALIGN = 4,       /* a pointer is not aligned to its element size */
+  SSM_ERR_CUDA = 5,        /* a CUDA runtime call or a kernel launch failed */
+  SSM_ERR_TIMEOUT = 6      /* reserved for bounded device-side waits */
+} ssm_status;
+
+/* Element type of x, delta, B, C, z and y.  A, D and the chunk states are
+ * always fp32 and all arithmetic is fp32 ([P1] s2.4: the prefix is accumulated
+ * in fp32 even when the inputs are bf16). */
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+typedef struct {
+  int64_t batch;     /* >= 1 */
+  int64_t seqlen;    /* L >= 1 */
+  int64_t dim;       /* channels D >= 1 */
+  int64_t dstate;    /* N, one of 1, 2, 4, 8, 16, 32, 64 */
+  int64_t chunk_len; /* steps per boundary-state chunk; 0 = no chunk states */
+} ssm_shapes;
+
+/* Kernel tiers.  AUTO picks the fastest eligible tier for the shape. */
+typedef enum {
+  SSM_KERNEL_AUTO = 0,
+  SSM_KERNEL_SERIAL = 1,   /* one thread per (b, d), all N states serial; any shape */
+  SSM_KERNEL_WARPSCAN = 2, /* [P1] s3.1 hierarchy: thread-serial run of k steps,
+                              5-round shuffle scan across the warp, serial carry
+                              between windows; one warp per (b, d) */
+  SSM_KERNEL_STREAM = 3    /* state-split register sweep with TMA-staged tiles and
+                              paired fp32 math; needs batch*dim*dstate to fill the GPU */
+} ssm_kernel;
+
+typedef struct {
+  ssm_kernel kernel; /* SSM_KERNEL_AUTO unless forcing a tier (tests, benchmarks) */
+  int32_t reserved;  /* must be 0 */
+} ssm_options;
+
+/*
+ * ssm_scan_fwd -- the fused selective-scan forward on device buffers.
+ *
+ *   x, delta, B, C : device, dtype `dtype`, required.
+ *   A              : device fp32 [dim, dstate], required.
+ *   D              : device fp32 [dim], or NULL for no D residual.
+ *   z              : device, dtype `dtype`, or NULL for no gate.
+ *   valid_len      : device int32 [batch], or NULL (every step valid).  Values
+ *                    outside [0, seqlen] are clamped on the device.
+ *   out_y          : device, dtype `dtype`, required.  bf16 results are rounded
+ *                    to nearest even.
+ *   out_chunk_states: device fp32, or NULL.  Written only when
+ *                    shapes->chunk_len > 0: chunk c holds h at step
+ *                    min((c+1)*chunk_len, seqlen) - 1 ([P1] s3.4).
+ *   shapes         : host pointer, required.
+ *   stream         : CUDA stream of the call.
+ * Returns SSM_OK once the work is enqueued.
+ */
+ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const int32_t* valid_len,
+                        void* out_y, float* out_chunk_states, const ssm_shapes* shapes,
+                        ssm_dtype dtype, cudaStream_t stream);
+
+/* As ssm_scan_fwd, with an explicit kernel tier (opts may be NULL = AUTO).
+ * A forced tier that cannot run the shape returns SSM_ERR_UNSUPPORTED. */
+ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z,
+                           const int32_t* valid_len, void* out_y, float* out_chunk_states,
+                           const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
+                           const ssm_options* opts);
+
+/* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
+ * arguments, without launching anything.  `has_*` describe which optional
+ * tensors the call passes.  Writes the tier to *kernel and the launch grid
+ * (number of thread blocks) to *grid_blocks; either output may be NULL. */
+ssm_status ssm_scan_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z, int has_valid_len,
+                         int has_states, const ssm_options* opts, ssm_kernel* kernel,
+                         int64_t* grid_blocks);
+
+/*
+ * ssm_scan_fwd_host -- the same forward on HOST buffers (end-to-end form).
+ *
+ * Every tensor pointer is a host pointer with the layout above (pinned memory
+ * gives asynchronous copies; pageable memory works but copies synchronously).
+ * The call copies the inputs into `workspace` (device memory owned by the
+ * caller, at least ssm_scan_host_workspace_bytes() bytes, 256-byte aligned),
+ * runs the forward there, and copies y (and the chunk states when requested)
+ * back to out_y / out_chunk_states, all in order on `stream`.  It returns once
+ * the work is enqueued; the host buffers must stay valid until the stream
+ * reaches that point.  One cudaMemcpyAsync per tensor and direction.
+ */
+ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const int32_t* valid_len, void* out_y, float* out_chunk_states,
+                             const ssm_shapes* shapes, ssm_dtype dtype, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* Device bytes ssm_scan_fwd_host needs for these shapes and optional tensors;
+ * 0 on invalid shapes. */
+size_t ssm_scan_host_workspace_bytes(const ssm_shapes* shapes, ssm_dtype dtype, int has_D,
+                                     int has_z, int has_valid_len, int has_states);
+
+/* Number of boundary-state chunks, ceil(seqlen / chunk_len); 0 when
+ * chunk_len <= 0 or shapes is NULL. */
+int64_t ssm_chunk_count(const ssm_shapes* shapes);
+
+/* Static, human-readable text for a status / a kernel tier. */
+const char* ssm_status_string(ssm_status status);
+const char* ssm_kernel_name(ssm_kernel kernel);
+
+/* Library version, e.g. "0.1.0". */
+const char* ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSMSCAN_H_ */

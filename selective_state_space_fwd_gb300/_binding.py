@@ -1,0 +1,276 @@
+"""ctypes binding of libssmscan (include/ssmscan.h): argument marshalling only.
+
+Every step of the forward runs in the CUDA library.  Tensors are PyTorch CUDA
+tensors (PyTorch provides device memory and streams); this module checks their
+dtypes, shapes and devices, allocates outputs when the caller passes none, and
+forwards raw pointers.  If the compiled library is missing the import fails
+loudly: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "ssmscan.h")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_UNSUPPORTED = 3
+    ERR_ALIGN = 4
+    ERR_CUDA = 5
+    ERR_TIMEOUT = 6
+
+
+class Kernel(enum.IntEnum):
+    AUTO = 0
+    SERIAL = 1
+    WARPSCAN = 2
+    STREAM = 3
+
+
+class DType(enum.IntEnum):
+    F32 = 0
+    BF16 = 1
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status)
+        super().__init__(f"{where}: {self.status.name} ({status_string(status)})")
+
+
+class Shapes(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("chunk_len", ctypes.c_int64)]
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libssmscan.so (built in-tree by ``selective_state_space_fwd_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m selective_state_space_fwd_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    SP, OP = ctypes.POINTER(Shapes), ctypes.POINTER(Options)
+    lib.ssm_scan_fwd.restype = I32
+    lib.ssm_scan_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P]
+    lib.ssm_scan_fwd_ex.restype = I32
+    lib.ssm_scan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
+    lib.ssm_scan_plan.restype = I32
+    lib.ssm_scan_plan.argtypes = [SP, I32, I32, I32, I32, OP, ctypes.POINTER(I32),
+                                  ctypes.POINTER(I64)]
+    lib.ssm_scan_fwd_host.restype = I32
+    lib.ssm_scan_fwd_host.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P, SZ, P]
+    lib.ssm_scan_host_workspace_bytes.restype = SZ
+    lib.ssm_scan_host_workspace_bytes.argtypes = [SP, I32, I32, I32, I32, I32]
+    lib.ssm_chunk_count.restype = I64
+    lib.ssm_chunk_count.argtypes = [SP]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [I32]
+    lib.ssm_kernel_name.restype = ctypes.c_char_p
+    lib.ssm_kernel_name.argtypes = [I32]
+    lib.ssm_version.restype = ctypes.c_char_p
+    lib.ssm_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/ssmscan.h declares (for export checks)."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load().ssm_status_string(int(status)).decode()
+
+
+def kernel_name(kernel: int) -> str:
+    return load().ssm_kernel_name(int(kernel)).decode()
+
+
+def version() -> str:
+    return load().ssm_version().decode()
+
+
+def _shapes(batch, seqlen, dim, dstate, chunk_len) -> Shapes:
+    return Shapes(int(batch), int(seqlen), int(dim), int(dstate), int(chunk_len))
+
+
+def chunk_count(seqlen: int, chunk_len: int) -> int:
+    s = _shapes(1, seqlen, 1, 1, chunk_len)
+    return int(load().ssm_chunk_count(ctypes.byref(s)))
+
+
+def plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False, mask=False, chunk_len=0,
+         kernel: Kernel | str = Kernel.AUTO) -> tuple[Kernel, int]:
+    """The tier and grid the library would launch for this call (no GPU needed)."""
+    s = _shapes(batch, seqlen, dim, dstate, chunk_len)
+    o = Options(int(_kernel(kernel)), 0)
+    k, g = ctypes.c_int32(), ctypes.c_int64()
+    st = load().ssm_scan_plan(ctypes.byref(s), int(_dtype_code(dtype)), int(gate), int(mask),
+                              int(chunk_len > 0), ctypes.byref(o), ctypes.byref(k),
+                              ctypes.byref(g))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_plan")
+    return Kernel(k.value), int(g.value)
+
+
+def _kernel(k) -> Kernel:
+    return Kernel[k.upper()] if isinstance(k, str) else Kernel(k)
+
+
+def _dtype_code(dtype) -> DType:
+    if isinstance(dtype, str):
+        return {"f32": DType.F32, "fp32": DType.F32, "float32": DType.F32,
+                "bf16": DType.BF16, "bfloat16": DType.BF16}[dtype]
+    import torch
+    if dtype == torch.float32:
+        return DType.F32
+    if dtype == torch.bfloat16:
+        return DType.BF16
+    raise TypeError(f"unsupported dtype {dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, shape, dtype, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
+             out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO, stream=None):
+    """The fused selective-scan forward on CUDA tensors.
+
+    x, delta, z: [batch, L, dim]; B, C: [batch, L, dstate] (fp32 or bf16, all the
+    same dtype); A: fp32 [dim, dstate]; D: fp32 [dim]; valid_len: int32 [batch].
+    Returns ``(y, states)`` with y like x and states fp32
+    [batch, ceil(L/chunk_len), dim, dstate] (None when chunk_len == 0).
+    Runs on ``stream`` (default: the current PyTorch stream of x's device).
+    """
+    import torch
+    lib = load()
+    if x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev, dt = x.device, x.dtype
+    code = _dtype_code(dt)
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    _check(x, "x", (batch, L, dim), dt, dev)
+    _check(delta, "delta", (batch, L, dim), dt, dev)
+    _check(B, "B", (batch, L, dstate), dt, dev)
+    _check(C, "C", (batch, L, dstate), dt, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, dev)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", (batch, L, dim), dt, dev)
+    states = None
+    if chunk_len > 0:
+        nch = (L + chunk_len - 1) // chunk_len
+        states = (torch.empty((batch, nch, dim, dstate), dtype=torch.float32, device=dev)
+                  if out_states is None else out_states)
+        _check(states, "out_states", (batch, nch, dim, dstate), torch.float32, dev)
+    s = _shapes(batch, L, dim, dstate, chunk_len)
+    o = Options(int(_kernel(kernel)), 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 _ptr(z), _ptr(valid_len), _ptr(y), _ptr(states),
+                                 ctypes.byref(s), int(code), ctypes.c_void_p(handle),
+                                 ctypes.byref(o))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd")
+    return y, states
+
+
+def host_workspace_bytes(batch, seqlen, dim, dstate, *, dtype="f32", has_D=True, gate=False,
+                         mask=False, chunk_len=0) -> int:
+    s = _shapes(batch, seqlen, dim, dstate, chunk_len)
+    return int(load().ssm_scan_host_workspace_bytes(ctypes.byref(s), int(_dtype_code(dtype)),
+                                                    int(has_D), int(gate), int(mask),
+                                                    int(chunk_len > 0)))
+
+
+def scan_fwd_host(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
+                  out=None, out_states=None, workspace=None, stream=None):
+    """End-to-end form on HOST tensors (pinned CPU tensors give async copies).
+
+    The library copies inputs into ``workspace`` (a CUDA uint8 tensor; allocated
+    here when None), runs the forward and copies y (and states) back into
+    ``out`` / ``out_states`` (CPU tensors; allocated pinned when None), all on
+    ``stream``.  The call returns once the work is enqueued: synchronise the
+    stream before reading the outputs."""
+    import torch
+    lib = load()
+    dt = x.dtype
+    code = _dtype_code(dt)
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    cpu = torch.device("cpu")
+    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, dim), dt),
+                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
+                                ("A", A, (dim, dstate), torch.float32)):
+        _check(t, name, shape, tdt, cpu)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, cpu)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, cpu)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, cpu)
+    y = torch.empty((batch, L, dim), dtype=dt, pin_memory=True) if out is None else out
+    states = None
+    if chunk_len > 0:
+        nch = (L + chunk_len - 1) // chunk_len
+        states = (torch.empty((batch, nch, dim, dstate), dtype=torch.float32, pin_memory=True)
+                  if out_states is None else out_states)
+    need = host_workspace_bytes(batch, L, dim, dstate, dtype=dt, has_D=D is not None,
+                                gate=z is not None, mask=valid_len is not None,
+                                chunk_len=chunk_len)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    s = _shapes(batch, L, dim, dstate, chunk_len)
+    with torch.cuda.device(workspace.device):
+        st = lib.ssm_scan_fwd_host(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                   _ptr(z), _ptr(valid_len), _ptr(y), _ptr(states),
+                                   ctypes.byref(s), int(code), _ptr(workspace),
+                                   workspace.numel(), ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd_host")
+    return y, states

@@ -1,0 +1,77 @@
+// common.cuh -- device helpers shared by the selective-scan kernels of libssmscan.
+//
+// Page keys used in comments:
+//   [P1] the article at pwwt.cn/news/6372990 on Mamba's hardware-aware algorithm
+//        and parallel associative scan.
+//   [P2] "Mamba并行扫描与硬件感知优化：从SSM递推到GPU高效实现" (bjdmk.com.cn/news/5218626).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+// log2(e): exp(v) = 2^(v * log2 e).  A is pre-scaled by it once per kernel so
+// that the per-(t, n) decay is one FMUL and one MUFU ex2 ([P1] s2.4 Abar = exp(delta A)).
+constexpr float kLog2e = 1.4426950408889634f;
+
+// All arguments of one forward call, passed to every tier by value.
+struct ScanParams {
+  const void* x;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;             // nullable
+  const void* z;              // nullable
+  const int32_t* valid_len;   // nullable
+  void* y;
+  float* states;              // nullable
+  int64_t batch, seqlen, dim;
+  int dstate;
+  int64_t chunk_len;          // > 0 when states != nullptr
+  int64_t n_chunks;
+};
+
+// 2^v with the MUFU unit (PTX ex2.approx.ftz.f32: results below 2^-126 flush
+// to zero, which the method tolerates: a product of decays that underflows
+// only removes contributions already below fp32 resolution, [P1] s2.4).
+__device__ __forceinline__ float ex2(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// silu(v) = v * sigmoid(v) = v / (1 + e^-v), the optional output gate.
+__device__ __forceinline__ float silu(float v) { return __fdividef(v, 1.0f + ex2(-v * kLog2e)); }
+
+// Element access for the two I/O types.  bf16 widens exactly to fp32; stores
+// round to nearest even.
+template <typename T> struct IO;
+template <> struct IO<float> {
+  static __device__ __forceinline__ float load(const void* p, int64_t i) {
+    return __ldg(static_cast<const float*>(p) + i);
+  }
+  static __device__ __forceinline__ void store(void* p, int64_t i, float v) {
+    static_cast<float*>(p)[i] = v;
+  }
+};
+template <> struct IO<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const void* p, int64_t i) {
+    return __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(p) + i));
+  }
+  static __device__ __forceinline__ void store(void* p, int64_t i, float v) {
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  }
+};
+
+// Clamped number of valid steps of batch row b ([P1] s2.3, s5.3: steps past
+// the valid length act as the identity (1, 0)).
+__device__ __forceinline__ int64_t valid_steps(const ScanParams& p, int64_t b) {
+  if (p.valid_len == nullptr) return p.seqlen;
+  int64_t v = p.valid_len[b];
+  return v < 0 ? 0 : (v > p.seqlen ? p.seqlen : v);
+}
+
+}  // namespace ssm

@@ -1,0 +1,101 @@
+"""C ABI checks that need no GPU: the library builds for sm_103a, loads, exports
+every function include/ssmscan.h declares, and rejects bad arguments with a
+status before anything is launched."""
+import ctypes
+
+import pytest
+
+from selective_state_space_fwd_gb300 import _binding as Bd
+
+EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_plan", "ssm_scan_fwd_host",
+            "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
+            "ssm_kernel_name", "ssm_version"}
+
+
+def test_every_declared_symbol_is_exported(ssmlib):
+    declared = set(Bd.declared_functions())
+    assert EXPECTED <= declared, EXPECTED - declared
+    lib = ctypes.CDLL(Bd.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in ssmscan.h but not exported"
+
+
+def test_status_and_kernel_strings(ssmlib):
+    for s in Bd.Status:
+        assert Bd.status_string(s) and Bd.status_string(s) != "unknown status"
+    for k in Bd.Kernel:
+        assert Bd.kernel_name(k) != "unknown"
+    assert Bd.version().count(".") == 2
+
+
+def test_chunk_count(ssmlib):
+    assert Bd.chunk_count(2048, 256) == 8
+    assert Bd.chunk_count(2049, 256) == 9
+    assert Bd.chunk_count(5, 0) == 0
+    assert Bd.chunk_count(1, 7) == 1
+
+
+FAKE = 0x10000  # never dereferenced: validation returns before any device work
+
+
+def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None, y=FAKE,
+          states=None, shapes=(2, 8, 4, 16, 0), dtype=0, kernel=0, reserved=0, shapes_ptr=True):
+    lib = Bd.load()
+    s = Bd.Shapes(*shapes)
+    o = Bd.Options(kernel, reserved)
+    P = ctypes.c_void_p
+    return lib.ssm_scan_fwd_ex(P(x), P(delta), P(A), P(B), P(C), P(D), P(z), P(valid), P(y),
+                               P(states), ctypes.byref(s) if shapes_ptr else None, dtype, None,
+                               ctypes.byref(o))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(shapes_ptr=False), Bd.Status.ERR_NULL),
+    (dict(x=None), Bd.Status.ERR_NULL),
+    (dict(delta=None), Bd.Status.ERR_NULL),
+    (dict(A=None), Bd.Status.ERR_NULL),
+    (dict(B=None), Bd.Status.ERR_NULL),
+    (dict(C=None), Bd.Status.ERR_NULL),
+    (dict(y=None), Bd.Status.ERR_NULL),
+    (dict(shapes=(0, 8, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, -1, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 8, 0, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 8, 4, 0, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 8, 4, 16, -5)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(1 << 40, 1 << 20, 1 << 20, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(states=FAKE, shapes=(2, 8, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 8, 4, 3, 0)), Bd.Status.ERR_UNSUPPORTED),
+    (dict(shapes=(2, 8, 4, 128, 0)), Bd.Status.ERR_UNSUPPORTED),
+    (dict(dtype=7), Bd.Status.ERR_UNSUPPORTED),
+    (dict(kernel=99), Bd.Status.ERR_UNSUPPORTED),
+    (dict(reserved=1), Bd.Status.ERR_UNSUPPORTED),
+    (dict(x=FAKE + 2), Bd.Status.ERR_ALIGN),
+    (dict(y=FAKE + 1, dtype=1), Bd.Status.ERR_ALIGN),
+    (dict(A=FAKE + 2, dtype=1), Bd.Status.ERR_ALIGN),
+    (dict(D=FAKE + 3), Bd.Status.ERR_ALIGN),
+    (dict(valid=FAKE + 2), Bd.Status.ERR_ALIGN),
+    (dict(states=FAKE + 2, shapes=(2, 8, 4, 16, 4)), Bd.Status.ERR_ALIGN),
+])
+def test_argument_errors_return_status(ssmlib, kw, status):
+    assert _call(**kw) == status
+
+
+def test_plan_serial_always_available(ssmlib):
+    for n in (1, 2, 4, 8, 16, 32, 64):
+        k, g = Bd.plan(3, 100, 70, n, kernel="serial")
+        assert k == Bd.Kernel.SERIAL and g == (3 * 70 + 127) // 128
+
+
+def test_plan_auto_picks_a_tier(ssmlib):
+    for n in (1, 16, 64):
+        k, g = Bd.plan(8, 4096, 1024, n)
+        assert k in (Bd.Kernel.SERIAL, Bd.Kernel.WARPSCAN, Bd.Kernel.STREAM) and g > 0
+
+
+def test_host_workspace_bytes(ssmlib):
+    b = Bd.host_workspace_bytes(2, 8, 4, 16, dtype="f32", has_D=True, gate=True, mask=True,
+                                chunk_len=4)
+    need = 3 * 2 * 8 * 4 * 4 + 2 * 2 * 8 * 16 * 4 + 4 * 16 * 4 + 4 * 4 + 2 * 4 + 2 * 8 * 4 * 4 \
+        + 2 * 2 * 4 * 16 * 4
+    assert need <= b <= need + 11 * 256
+    assert Bd.host_workspace_bytes(0, 8, 4, 16) == 0

@@ -1,0 +1,247 @@
+"""Parity of the CUDA library with the fp64 oracle, through the C ABI, on a GPU.
+
+Tolerances, from the path's precision contract (fp32 state and arithmetic):
+  fp32 I/O:  max|y - y_ref| / max|y_ref| <= 1e-5
+  bf16 I/O:  max|y - y_ref| / max|y_ref| <= 1e-2 (y is rounded to bf16)
+  chunk states (fp32 always): max|s - s_ref| / max|s_ref| <= 1e-5
+Outputs past valid_len must be exactly 0.
+"""
+import numpy as np
+import pytest
+import torch
+
+import selective_state_space_fwd_gb300 as S
+from selective_state_space_fwd_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TIERS = ["serial", "warpscan", "stream", "auto"]
+TOL_Y = {"f32": 1e-5, "bf16": 1e-2}
+TOL_STATES = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(ssmlib, oracle):
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    yield
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(inp: dict, kernel="auto"):
+    t = W.to_torch(inp, "cuda")
+    y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=kernel)
+    torch.cuda.synchronize()
+    return to_f64(y), (to_f64(s) if s is not None else None)
+
+
+def run_oracle(oracle, inp: dict, threads=0):
+    return oracle.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           inp["z"], inp["valid_len"], chunk_len=inp["chunk_len"],
+                           threads=threads)
+
+
+def rel_err(a, ref):
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(a - ref)) / den) if den > 0 else float(np.max(np.abs(a)))
+
+
+def check(inp, y, s, y_ref, s_ref):
+    tol = TOL_Y[inp["dtype"]]
+    e = rel_err(y, y_ref)
+    assert e <= tol, f"y rel err {e:.3e} > {tol}"
+    if inp["valid_len"] is not None:
+        L = y.shape[1]
+        for b, v in enumerate(inp["valid_len"]):
+            v = min(max(int(v), 0), L)
+            assert np.all(y[b, v:] == 0), f"row {b}: nonzero output past valid_len {v}"
+    if s_ref is not None:
+        es = rel_err(s, s_ref)
+        assert es <= TOL_STATES, f"chunk-state rel err {es:.3e} > {TOL_STATES}"
+    return e
+
+
+def tier_supported(inp, kernel):
+    if kernel == "auto":
+        return True
+    Bt, L, Dm = inp["x"].shape
+    try:
+        S.plan(Bt, L, Dm, inp["B"].shape[-1], dtype=inp["dtype"], gate=inp["z"] is not None,
+               mask=inp["valid_len"] is not None, chunk_len=inp["chunk_len"], kernel=kernel)
+        return True
+    except S.SsmError as e:
+        assert e.status == S.Status.ERR_UNSUPPORTED
+        return False
+
+
+# Scaled-down versions of the five workloads: several tiles of every tier and
+# ragged tails in L and dim, small enough for the oracle to finish in seconds.
+SMALL = {
+    "w1-tiny-full": W.WORKLOADS[1],
+    "w2-fp32": W.WORKLOADS[2].scaled(batch=2, seqlen=1000, dim=72),
+    "w3-bf16-gate-states": W.WORKLOADS[3].scaled(batch=2, seqlen=700, dim=80),
+    "w4-varlen": W.WORKLOADS[4].scaled(batch=6, seqlen=600, dim=48),
+    "w5-long-n64": W.WORKLOADS[5].scaled(batch=1, seqlen=3000, dim=40),
+}
+
+
+def small_inputs(name):
+    w = SMALL[name]
+    inp = W.make_inputs(w)
+    if w.mask is not None:  # span the edge cases: 0, 1, mid, L, > L
+        inp["valid_len"] = np.array([0, 1, 64, 333, w.seqlen, w.seqlen + 100][:w.batch], np.int32)
+    return inp
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_small(oracle, name):
+    if name not in _ORACLE_CACHE:
+        inp = small_inputs(name)
+        _ORACLE_CACHE[name] = (inp, run_oracle(oracle, inp))
+    return _ORACLE_CACHE[name]
+
+
+@pytest.mark.parametrize("kernel", TIERS)
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_workload_small(oracle, name, kernel):
+    inp, (y_ref, s_ref) = oracle_small(oracle, name)
+    if not tier_supported(inp, kernel):
+        pytest.skip(f"{kernel} does not take this shape")
+    y, s = run_gpu(inp, kernel)
+    check(inp, y, s, y_ref, s_ref)
+
+
+def _edge(batch, L, dim, N, dtype="f32", gate=False, mask=None, chunk=0, seed=7):
+    w = W.Workload(0, "edge", batch, L, dim, N, dtype, "loguniform", "s4d", "normal", gate, None,
+                   chunk, seed)
+    inp = W.make_inputs(w)
+    if mask is not None:
+        inp["valid_len"] = np.array(mask, np.int32)
+    return inp
+
+
+EDGES = {
+    "L1": dict(batch=2, L=1, dim=33, N=16),
+    "L7-gate": dict(batch=1, L=7, dim=5, N=4, gate=True),
+    "L31-N1": dict(batch=3, L=31, dim=64, N=1),
+    "L33-N2-bf16": dict(batch=2, L=33, dim=48, N=2, dtype="bf16"),
+    "N4-chunk1": dict(batch=1, L=40, dim=16, N=4, chunk=1),
+    "N8-chunkL": dict(batch=2, L=100, dim=24, N=8, chunk=100),
+    "N32-chunk-gtL": dict(batch=1, L=90, dim=40, N=32, chunk=1000),
+    "N64-ragged": dict(batch=1, L=517, dim=9, N=64, chunk=128),
+    "dim1": dict(batch=4, L=300, dim=1, N=16, chunk=64),
+    "fp32-all-options": dict(batch=4, L=513, dim=37, N=16, gate=True, mask=[513, 0, 200, 1],
+                             chunk=100),
+    "bf16-mask-nogate": dict(batch=3, L=257, dim=64, N=16, dtype="bf16", mask=[5, 257, 128]),
+    "chunk-not-mult-32": dict(batch=2, L=300, dim=32, N=16, chunk=48),
+    "dim-odd-long": dict(batch=1, L=2500, dim=3, N=16, chunk=512),
+}
+
+
+@pytest.mark.parametrize("kernel", TIERS)
+@pytest.mark.parametrize("name", sorted(EDGES))
+def test_edge_cases(oracle, name, kernel):
+    inp = _edge(**EDGES[name])
+    if not tier_supported(inp, kernel):
+        pytest.skip(f"{kernel} does not take this shape")
+    y_ref, s_ref = run_oracle(oracle, inp)
+    y, s = run_gpu(inp, kernel)
+    check(inp, y, s, y_ref, s_ref)
+
+
+def test_error_grows_slowly_with_length(oracle):
+    """[P1] s4.4: the error against the reference stays at fp32 level as L grows
+    from 256 to 8192 (fp32 accumulation of the prefix)."""
+    errs = []
+    for L in (256, 1024, 4096, 8192):
+        inp = _edge(batch=1, L=L, dim=64, N=16, seed=40)
+        y_ref, _ = run_oracle(oracle, inp)
+        y, _ = run_gpu(inp)
+        errs.append(check(inp, y, None, y_ref, None))
+    assert errs[-1] <= 1e-5
+
+
+def test_deterministic_bitwise():
+    inp = W.make_inputs(SMALL["w2-fp32"])
+    for kernel in TIERS:
+        if not tier_supported(inp, kernel):
+            continue
+        y1, _ = run_gpu(inp, kernel)
+        y2, _ = run_gpu(inp, kernel)
+        assert np.array_equal(y1, y2), kernel
+
+
+def test_tiers_agree_closely(oracle):
+    """All tiers compute the same function; they may round differently."""
+    inp = small_inputs("w3-bf16-gate-states")
+    outs = {k: run_gpu(inp, k) for k in TIERS if tier_supported(inp, k)}
+    ref = outs["serial"]
+    for k, (y, s) in outs.items():
+        assert rel_err(s, ref[1]) <= 2 * TOL_STATES, k
+
+
+def test_host_entry_point_matches_device(oracle):
+    inp = small_inputs("w4-varlen")
+    t = W.to_torch(inp, "cpu")
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    y_h, s_h = S.scan_fwd_host(pinned["x"], pinned["delta"], pinned["A"], pinned["B"],
+                               pinned["C"], pinned["D"], pinned["z"], pinned["valid_len"],
+                               chunk_len=inp["chunk_len"])
+    torch.cuda.synchronize()
+    y_d, s_d = run_gpu(inp)
+    assert np.array_equal(to_f64(y_h), y_d)
+    assert np.array_equal(to_f64(s_h), s_d)
+
+
+def test_stream_argument_is_respected():
+    inp = W.make_inputs(SMALL["w2-fp32"])
+    t = W.to_torch(inp, "cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        y, _ = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"])
+    st.synchronize()
+    y_ref, _ = run_gpu(inp)
+    assert np.array_equal(to_f64(y), y_ref)
+
+
+# Full-size workloads, in the launch configuration the benchmark times (AUTO),
+# checked on sampled channels: the oracle recomputes those channels one by one.
+def _sample_channels(w, k=12, seed=0):
+    rng = np.random.default_rng(seed)
+    pts = {(0, 0), (w.batch - 1, w.dim - 1), (0, w.dim - 1), (w.batch - 1, 0)}
+    while len(pts) < k:
+        pts.add((int(rng.integers(w.batch)), int(rng.integers(w.dim))))
+    return sorted(pts)
+
+
+@pytest.mark.parametrize("key", [1, 2, 3, 4, 5])
+def test_full_size_sampled(oracle, key):
+    w = W.WORKLOADS[key]
+    inp = W.make_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                      t["valid_len"], chunk_len=w.chunk_len)
+    torch.cuda.synchronize()
+    del t
+    ys, yr, ss, sr = [], [], [], []
+    for b, d in _sample_channels(w):
+        ci = W.channel_slice(inp, b, d)
+        y_ref, s_ref = run_oracle(oracle, ci, threads=1)
+        ys.append(to_f64(y[b, :, d]))
+        yr.append(y_ref[0, :, 0])
+        if s is not None:
+            ss.append(to_f64(s[b, :, d]))
+            sr.append(s_ref[0, :, 0])
+        if inp["valid_len"] is not None:
+            v = int(inp["valid_len"][b])
+            assert torch.all(y[b, v:, d] == 0)
+    e = rel_err(np.concatenate(ys), np.concatenate(yr))
+    assert e <= TOL_Y[w.dtype], f"workload {key}: sampled y rel err {e:.3e}"
+    if ss:
+        es = rel_err(np.concatenate(ss), np.concatenate(sr))
+        assert es <= TOL_STATES, f"workload {key}: sampled state rel err {es:.3e}"
