@@ -89,8 +89,10 @@ typedef enum {
 } ssm_kernel;
 
 typedef struct {
-  ssm_kernel kernel; /* SSM_KERNEL_AUTO unless forcing a tier (tests, benchmarks) */
-  int32_t reserved;  /* must be 0 */
+  ssm_kernel kernel;       /* SSM_KERNEL_AUTO unless forcing a tier (tests, benchmarks) */
+  int32_t warps_per_block; /* 0 = the tier's default; STREAM accepts 1, 2 or 4 */
+  int32_t states_per_lane; /* 0 = the tier's default; STREAM: 2, 4, 8 or 16 states of one
+                              channel per thread (fewer = more threads, more reduction) */
 } ssm_options;
 
 /*
@@ -162,6 +164,12 @@ int64_t ssm_chunk_count(const ssm_shapes* shapes);
 /* Static, human-readable text for a status / a kernel tier. */
 const char* ssm_status_string(ssm_status status);
 const char* ssm_kernel_name(ssm_kernel kernel);
+
+/* Reads and clears the library's sticky device error word.  A kernel whose
+ * bounded wait on a copy gives up sets it and returns early (its outputs are
+ * then undefined).  Synchronises the current device.  Returns SSM_OK,
+ * SSM_ERR_TIMEOUT, or SSM_ERR_CUDA if the word cannot be read. */
+ssm_status ssm_check_device_errors(void);
 
 /* Library version, e.g. "0.1.0". */
 const char* ssm_version(void);

@@ -4,10 +4,11 @@ The compute lives in ``libssmscan.so`` (C ABI, include/ssmscan.h, hand-written
 sm_103a kernels under csrc/).  This package is its Python binding plus the
 seeded synthetic workloads used by the benchmark and tests.
 """
-from ._binding import (Kernel, SsmError, Status, chunk_count, declared_functions,
+from ._binding import (Kernel, SsmError, Status, check_device_errors, chunk_count,
+                       declared_functions,
                        host_workspace_bytes, kernel_name, load, plan, scan_fwd, scan_fwd_host,
                        status_string, version)
 
-__all__ = ["Kernel", "SsmError", "Status", "chunk_count", "declared_functions",
+__all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "declared_functions",
            "host_workspace_bytes", "kernel_name", "load", "plan", "scan_fwd", "scan_fwd_host",
            "status_string", "version"]

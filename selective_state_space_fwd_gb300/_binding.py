@@ -52,7 +52,8 @@ class Shapes(ctypes.Structure):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+    _fields_ = [("kernel", ctypes.c_int32), ("warps_per_block", ctypes.c_int32),
+                ("states_per_lane", ctypes.c_int32)]
 
 
 _lib = None
@@ -88,6 +89,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_kernel_name.argtypes = [I32]
     lib.ssm_version.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []
+    lib.ssm_check_device_errors.restype = I32
+    lib.ssm_check_device_errors.argtypes = []
     _lib = lib
     return lib
 
@@ -120,11 +123,20 @@ def chunk_count(seqlen: int, chunk_len: int) -> int:
     return int(load().ssm_chunk_count(ctypes.byref(s)))
 
 
+def check_device_errors() -> None:
+    """Raise SsmError if a kernel's bounded wait gave up since the last check
+    (synchronises the device)."""
+    st = load().ssm_check_device_errors()
+    if st != 0:
+        raise SsmError(st, "ssm_check_device_errors")
+
+
 def plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False, mask=False, chunk_len=0,
-         kernel: Kernel | str = Kernel.AUTO) -> tuple[Kernel, int]:
+         kernel: Kernel | str = Kernel.AUTO, warps_per_block: int = 0,
+         states_per_lane: int = 0) -> tuple[Kernel, int]:
     """The tier and grid the library would launch for this call (no GPU needed)."""
     s = _shapes(batch, seqlen, dim, dstate, chunk_len)
-    o = Options(int(_kernel(kernel)), 0)
+    o = Options(int(_kernel(kernel)), int(warps_per_block), int(states_per_lane))
     k, g = ctypes.c_int32(), ctypes.c_int64()
     st = load().ssm_scan_plan(ctypes.byref(s), int(_dtype_code(dtype)), int(gate), int(mask),
                               int(chunk_len > 0), ctypes.byref(o), ctypes.byref(k),
@@ -166,7 +178,8 @@ def _check(t, name, shape, dtype, device):
 
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
-             out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO, stream=None):
+             out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO,
+             warps_per_block: int = 0, states_per_lane: int = 0, stream=None):
     """The fused selective-scan forward on CUDA tensors.
 
     x, delta, z: [batch, L, dim]; B, C: [batch, L, dstate] (fp32 or bf16, all the
@@ -203,7 +216,7 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
                   if out_states is None else out_states)
         _check(states, "out_states", (batch, nch, dim, dstate), torch.float32, dev)
     s = _shapes(batch, L, dim, dstate, chunk_len)
-    o = Options(int(_kernel(kernel)), 0)
+    o = Options(int(_kernel(kernel)), int(warps_per_block), int(states_per_lane))
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

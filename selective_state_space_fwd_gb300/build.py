@@ -63,6 +63,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                      "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
     if verbose:
         common += ["-Xptxas", "-v"]
+    common += os.environ.get("SSM_NVCC_EXTRA", "").split()  # extra defines for comparison builds
 
     def compile_one(src: str) -> str:
         obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")

@@ -55,24 +55,40 @@ ssm_status check_shapes(const ssm_shapes* s, ssm_dtype dtype, bool want_states) 
 
 ssm_status check_options(const ssm_options* o) {
   if (o == nullptr) return SSM_OK;
-  if (o->reserved != 0) return SSM_ERR_UNSUPPORTED;
+  if (o->warps_per_block != 0 && o->warps_per_block != 1 && o->warps_per_block != 2 &&
+      o->warps_per_block != 4)
+    return SSM_ERR_UNSUPPORTED;
   if (o->kernel < SSM_KERNEL_AUTO || o->kernel > SSM_KERNEL_STREAM) return SSM_ERR_UNSUPPORTED;
+  if (o->states_per_lane != 0 && o->states_per_lane != 2 && o->states_per_lane != 4 &&
+      o->states_per_lane != 8 && o->states_per_lane != 16)
+    return SSM_ERR_UNSUPPORTED;
   return SSM_OK;
 }
 
 struct Plan {
   ssm_kernel kernel;
   int64_t grid;
+  ssm::StreamShape shape;
 };
 
 // Tier choice.  `forced` is the caller's request (AUTO = let the library pick).
-ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, ssm_kernel forced, Plan* out) {
-  (void)dtype;
-  ssm_kernel k = forced == SSM_KERNEL_AUTO ? SSM_KERNEL_SERIAL : forced;
+ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o, Plan* out) {
+  const bool bf16 = dtype == SSM_BF16;
+  const ssm_kernel forced = o ? o->kernel : SSM_KERNEL_AUTO;
+  const ssm::StreamShape shape =
+      ssm::stream_shape(p, o ? o->warps_per_block : 0, o ? o->states_per_lane : 0);
+  ssm_kernel k = forced;
+  if (k == SSM_KERNEL_AUTO)
+    k = ssm::stream_eligible(p, bf16, shape) ? SSM_KERNEL_STREAM : SSM_KERNEL_SERIAL;
+  out->kernel = k;
+  out->shape = shape;
   switch (k) {
     case SSM_KERNEL_SERIAL:
-      out->kernel = k;
       out->grid = ssm::serial_grid(p);
+      return SSM_OK;
+    case SSM_KERNEL_STREAM:
+      if (!ssm::stream_eligible(p, bf16, shape)) return SSM_ERR_UNSUPPORTED;
+      out->grid = ssm::stream_grid(p, shape);
       return SSM_OK;
     default:
       return SSM_ERR_UNSUPPORTED;
@@ -130,6 +146,12 @@ extern "C" {
 
 const char* ssm_version(void) { return "0.1.0"; }
 
+ssm_status ssm_check_device_errors(void) {
+  unsigned int word = 0;
+  if (!ssm::read_and_clear_device_errors(&word)) return SSM_ERR_CUDA;
+  return word ? SSM_ERR_TIMEOUT : SSM_OK;
+}
+
 const char* ssm_status_string(ssm_status status) {
   switch (status) {
     case SSM_OK: return "ok";
@@ -165,7 +187,7 @@ ssm_status ssm_scan_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z, i
   if (st != SSM_OK) return st;
   if ((st = check_options(opts)) != SSM_OK) return st;
   // Placeholder pointers: planning looks only at shapes and which tensors exist.
-  static const char dummy[16] = {0};
+  alignas(256) static const char dummy[256] = {0};
   ScanParams p = make_params(dummy, dummy, reinterpret_cast<const float*>(dummy), dummy, dummy,
                              nullptr, has_z ? dummy : nullptr,
                              has_valid_len ? reinterpret_cast<const int32_t*>(dummy) : nullptr,
@@ -173,7 +195,7 @@ ssm_status ssm_scan_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z, i
                              has_states ? reinterpret_cast<float*>(const_cast<char*>(dummy)) : nullptr,
                              shapes);
   Plan plan;
-  if ((st = make_plan(p, dtype, opts ? opts->kernel : SSM_KERNEL_AUTO, &plan)) != SSM_OK) return st;
+  if ((st = make_plan(p, dtype, opts, &plan)) != SSM_OK) return st;
   if (kernel) *kernel = plan.kernel;
   if (grid_blocks) *grid_blocks = plan.grid;
   return SSM_OK;
@@ -197,11 +219,12 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
   const ScanParams p = make_params(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states,
                                    shapes);
   Plan plan;
-  if ((st = make_plan(p, dtype, opts ? opts->kernel : SSM_KERNEL_AUTO, &plan)) != SSM_OK) return st;
+  if ((st = make_plan(p, dtype, opts, &plan)) != SSM_OK) return st;
   const bool bf16 = dtype == SSM_BF16;
   cudaError_t err = cudaErrorInvalidValue;
   switch (plan.kernel) {
     case SSM_KERNEL_SERIAL: err = ssm::launch_serial(p, bf16, stream); break;
+    case SSM_KERNEL_STREAM: err = ssm::launch_stream(p, bf16, stream, plan.shape); break;
     default: return SSM_ERR_UNSUPPORTED;
   }
   return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -12,4 +12,18 @@ namespace ssm {
 cudaError_t launch_serial(const ScanParams& p, bool bf16, cudaStream_t s);
 int64_t serial_grid(const ScanParams& p);
 
+// STREAM tier: state-split register sweep with TMA-staged tiles.
+struct StreamShape {
+  int wpc;  // warps per thread block
+  int g;    // states per lane
+};
+// The launch shape for a request (0 = default); {0, 0} when no instance exists.
+StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane);
+bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
+int64_t stream_grid(const ScanParams& p, StreamShape sh);
+cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);
+
+// Sticky device error word of the tiers with bounded waits: read and clear.
+bool read_and_clear_device_errors(unsigned int* word);
+
 }  // namespace ssm

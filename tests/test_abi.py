@@ -9,7 +9,7 @@ from selective_state_space_fwd_gb300 import _binding as Bd
 
 EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_plan", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
-            "ssm_kernel_name", "ssm_version"}
+            "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
 
 def test_every_declared_symbol_is_exported(ssmlib):
@@ -39,10 +39,10 @@ FAKE = 0x10000  # never dereferenced: validation returns before any device work
 
 
 def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None, y=FAKE,
-          states=None, shapes=(2, 8, 4, 16, 0), dtype=0, kernel=0, reserved=0, shapes_ptr=True):
+          states=None, shapes=(2, 8, 4, 16, 0), dtype=0, kernel=0, wpb=0, spl=0, shapes_ptr=True):
     lib = Bd.load()
     s = Bd.Shapes(*shapes)
-    o = Bd.Options(kernel, reserved)
+    o = Bd.Options(kernel, wpb, spl)
     P = ctypes.c_void_p
     return lib.ssm_scan_fwd_ex(P(x), P(delta), P(A), P(B), P(C), P(D), P(z), P(valid), P(y),
                                P(states), ctypes.byref(s) if shapes_ptr else None, dtype, None,
@@ -68,7 +68,10 @@ def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None
     (dict(shapes=(2, 8, 4, 128, 0)), Bd.Status.ERR_UNSUPPORTED),
     (dict(dtype=7), Bd.Status.ERR_UNSUPPORTED),
     (dict(kernel=99), Bd.Status.ERR_UNSUPPORTED),
-    (dict(reserved=1), Bd.Status.ERR_UNSUPPORTED),
+    (dict(wpb=3), Bd.Status.ERR_UNSUPPORTED),
+    (dict(wpb=-1), Bd.Status.ERR_UNSUPPORTED),
+    (dict(spl=3), Bd.Status.ERR_UNSUPPORTED),
+    (dict(spl=32), Bd.Status.ERR_UNSUPPORTED),
     (dict(x=FAKE + 2), Bd.Status.ERR_ALIGN),
     (dict(y=FAKE + 1, dtype=1), Bd.Status.ERR_ALIGN),
     (dict(A=FAKE + 2, dtype=1), Bd.Status.ERR_ALIGN),
