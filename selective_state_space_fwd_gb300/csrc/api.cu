@@ -90,6 +90,10 @@ ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o,
       if (!ssm::stream_eligible(p, bf16, shape)) return SSM_ERR_UNSUPPORTED;
       out->grid = ssm::stream_grid(p, shape);
       return SSM_OK;
+    case SSM_KERNEL_WARPSCAN:
+      if (!ssm::warpscan_eligible(p)) return SSM_ERR_UNSUPPORTED;
+      out->grid = ssm::warpscan_grid(p);
+      return SSM_OK;
     default:
       return SSM_ERR_UNSUPPORTED;
   }
@@ -225,6 +229,7 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
   switch (plan.kernel) {
     case SSM_KERNEL_SERIAL: err = ssm::launch_serial(p, bf16, stream); break;
     case SSM_KERNEL_STREAM: err = ssm::launch_stream(p, bf16, stream, plan.shape); break;
+    case SSM_KERNEL_WARPSCAN: err = ssm::launch_warpscan(p, bf16, stream); break;
     default: return SSM_ERR_UNSUPPORTED;
   }
   return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;

@@ -174,6 +174,26 @@ template <> struct Elem<__nv_bfloat16> {
   }
 };
 
+// Sum over the NG lanes of a channel, scattered: lane g of the channel returns
+// the full sum for step g of the NG partials it was given.  Each round halves
+// the values a lane holds: it keeps the half selected by its lane bit and adds
+// the half its partner sends (shuffles, so the shared-memory pipe stays free
+// for the input loads).
+template <int NG>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NG], int g) {
+#pragma unroll
+  for (int m = NG / 2; m >= 1; m /= 2) {
+    const bool upper = (g & m) != 0;
+#pragma unroll
+    for (int k = 0; k < m; ++k) {
+      const float keep = upper ? v[k + m] : v[k];
+      const float send = upper ? v[k] : v[k + m];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return v[0];
+}
+
 template <int N_, int NG_, int T_, int STAGES_, int WPC_, typename IO_, bool GATE_>
 struct Cfg {
   static constexpr int N = N_, NG = NG_, T = T_, STAGES = STAGES_, WPC = WPC_;
@@ -190,17 +210,12 @@ struct Cfg {
   static constexpr int BODY_STEPS = BODY * U;
   static constexpr int PAD = U;             // rows read past a tile by the last prefetch
   static constexpr int ES = Elem<IO>::kBytes;
-  // stage slot: x, delta (, z) tiles [T][CPC]; B, C tiles [T + PAD][N]
-  static constexpr int ACT = (T * CPC * ES + 127) / 128 * 128;
+  // stage slot: x, delta (, z) tiles [T + PAD][CPC]; B, C tiles [T + PAD][N]
+  static constexpr int ACT = ((T + PAD) * CPC * ES + 127) / 128 * 128;
   static constexpr int ROW = ((T + PAD) * N * ES + 127) / 128 * 128;
   static constexpr int STAGE_BYTES = ACT * (GATE ? 3 : 2) + 2 * ROW;
   static constexpr int TX_BYTES = T * CPC * ES * (GATE ? 3 : 2) + 2 * T * N * ES;
-  // per warp: {delta, delta, delta*x, delta*x} rows [T + PAD][CH] and the
-  // reduce scratch [CH][NG][NG + 1] fp32
-  static constexpr int PRE = (T + PAD) * CH * 16;
-  static constexpr int RED = CH * NG * (NG + 1) * 4;
-  static constexpr int WARP_BYTES = (PRE + RED + 127) / 128 * 128;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES + WPC * WARP_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8;
   static_assert(G >= 2 && G % 2 == 0, "a lane holds whole state pairs");
   static_assert(NG >= 2 && NG <= 8 && (NG & (NG - 1)) == 0, "NG is 2, 4 or 8");
@@ -236,31 +251,38 @@ __device__ __forceinline__ void load_tile(char* slot, uint64_t* full, const CUte
 }
 
 // Inputs of one step for this lane's states: Abar = exp(delta A) as
-// 2^(delta * A log2 e) ([P1] s2.4), the input term delta * B * x ([P1] s3.3)
-// and the C row.  `pre` points at this lane's {delta, delta, u, u} row
-// (u = delta * x), `brow` / `crow` at this lane's slice of the B and C rows.
+// 2^(delta * A log2 e) ([P1] s2.4), the input term delta * B * x ([P1] s3.3),
+// the C row and x.  `dl` / `xl` point at this lane's channel in the delta and
+// x tiles (row stride CPC), `brow` / `crow` at this lane's slice of the B and
+// C rows of the step.
 template <class K>
-__device__ __forceinline__ void step_inputs(const float4* pre, const typename K::IO* brow,
-                                            const typename K::IO* crow, const u64 (&a2)[K::P],
-                                            u64 (&ab)[K::P], u64 (&bi)[K::P], u64 (&cq)[K::P]) {
+__device__ __forceinline__ void step_inputs(const typename K::IO* dl, const typename K::IO* xl,
+                                            const typename K::IO* brow, const typename K::IO* crow,
+                                            const u64 (&a2)[K::P], u64 (&ab)[K::P],
+                                            u64 (&bi)[K::P], u64 (&cq)[K::P], float& xv) {
   using E = Elem<typename K::IO>;
-  const ulonglong2 du = *reinterpret_cast<const ulonglong2*>(pre);  // {dd, uu} pairs
+  const float dt = E::get(dl, 0);
+  xv = E::get(xl, 0);
+  const float uu = dt * xv;
+  const u64 dd = pk2(dt, dt), ux = pk2(uu, uu);
   u64 bq[K::P];
   E::template pairs<K::P>(brow, bq);
   E::template pairs<K::P>(crow, cq);
 #pragma unroll
   for (int q = 0; q < K::P; ++q) {
-    const float2 arg = upk2(mul2(a2[q], du.x));
+    const float2 arg = upk2(mul2(a2[q], dd));
     ab[q] = pk2(ex2(arg.x), ex2(arg.y));
-    bi[q] = mul2(bq[q], du.y);
+    bi[q] = mul2(bq[q], ux);
   }
 }
 
 // One step of h = Abar h + delta B x for this lane's states ([P1] s1.1), and
-// this lane's part of the contraction sum_n C_n h_n.
+// this lane's part of the output sum_n C_n h_n (+ D x on the channel's lane 0,
+// so the reduction over the channel's lanes also adds the D residual).
 template <class K>
 __device__ __forceinline__ float step_update(u64 (&h2)[K::P], const u64 (&ab)[K::P],
-                                             const u64 (&bi)[K::P], const u64 (&cq)[K::P]) {
+                                             const u64 (&bi)[K::P], const u64 (&cq)[K::P],
+                                             float xv, float dg) {
   u64 acc = 0;
 #pragma unroll
   for (int q = 0; q < K::P; ++q) {
@@ -268,30 +290,33 @@ __device__ __forceinline__ float step_update(u64 (&h2)[K::P], const u64 (&ab)[K:
     acc = q == 0 ? mul2(cq[q], h2[q]) : fma2(cq[q], h2[q], acc);
   }
   const float2 a = upk2(acc);
-  return a.x + a.y;
+  return fmaf(dg, xv, a.x + a.y);
 }
 
 // The inputs of U consecutive steps, formed ahead of the recurrence.
 template <class K>
 struct Batch {
   u64 ab[K::U][K::P], bi[K::U][K::P], cq[K::U][K::P];
+  float xv[K::U];
 };
 
 template <class K>
-__device__ __forceinline__ void batch_inputs(const float4* pre, const typename K::IO* brow,
+__device__ __forceinline__ void batch_inputs(const typename K::IO* dl, const typename K::IO* xl,
+                                             const typename K::IO* brow,
                                              const typename K::IO* crow, int s,
                                              const u64 (&a2)[K::P], Batch<K>& bt) {
 #pragma unroll
   for (int u = 0; u < K::U; ++u)
-    step_inputs<K>(pre + (s + u) * K::CH, brow + (s + u) * K::N, crow + (s + u) * K::N, a2,
-                   bt.ab[u], bt.bi[u], bt.cq[u]);
+    step_inputs<K>(dl + (s + u) * K::CPC, xl + (s + u) * K::CPC, brow + (s + u) * K::N,
+                   crow + (s + u) * K::N, a2, bt.ab[u], bt.bi[u], bt.cq[u], bt.xv[u]);
 }
 
 template <class K>
-__device__ __forceinline__ void batch_update(u64 (&h2)[K::P], const Batch<K>& bt,
+__device__ __forceinline__ void batch_update(u64 (&h2)[K::P], const Batch<K>& bt, float dg,
                                              float (&part)[K::BODY_STEPS], int off) {
 #pragma unroll
-  for (int u = 0; u < K::U; ++u) part[off + u] = step_update<K>(h2, bt.ab[u], bt.bi[u], bt.cq[u]);
+  for (int u = 0; u < K::U; ++u)
+    part[off + u] = step_update<K>(h2, bt.ab[u], bt.bi[u], bt.cq[u], bt.xv[u], dg);
 }
 
 template <class K>
@@ -301,7 +326,7 @@ __global__ void __launch_bounds__(K::WPC * 32)
                   const __grid_constant__ CUtensorMap tm_c, const ScanParams p) {
   using IO = typename K::IO;
   using E = Elem<IO>;
-  // Dynamic shared memory: the stage ring, per-warp buffers, then the
+  // Dynamic shared memory: the stage ring, then the
   // mbarriers.  Used through pointers derived from the __shared__ array so
   // that every access compiles to a shared-memory instruction.
   extern __shared__ __align__(128) char smem[];
@@ -309,9 +334,6 @@ __global__ void __launch_bounds__(K::WPC * 32)
   uint64_t* empty = full + K::STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  char* wbuf = smem + K::STAGES * K::STAGE_BYTES + warp * K::WARP_BYTES;
-  float4* pre = reinterpret_cast<float4*>(wbuf);                // [T + PAD][CH]
-  float* red = reinterpret_cast<float*>(wbuf + K::PRE);         // [CH][NG][NG + 1]
 
   const int64_t n_cg = (p.dim + K::CPC - 1) / K::CPC;
   const int64_t b = blockIdx.x / n_cg;
@@ -353,6 +375,7 @@ __global__ void __launch_bounds__(K::WPC * 32)
     h2[q] = pk2(0.f, 0.f);  // [P1] s4.1: h_0 = 0
   }
   const float dskip = (d_ok && p.D) ? __ldg(p.D + d) : 0.f;
+  const float dg = g == 0 ? dskip : 0.f;  // the channel's lane 0 adds D x to its partial
   IO* __restrict__ yout = static_cast<IO*>(p.y);
   const bool want_states = p.states != nullptr;
   // Chunk c ends at step min((c+1) chunk_len, L) - 1 ([P1] s3.4).
@@ -387,39 +410,19 @@ __global__ void __launch_bounds__(K::WPC * 32)
     const int64_t t0 = static_cast<int64_t>(i) * K::T;
     const int steps = static_cast<int>(lv - t0 < K::T ? lv - t0 : K::T);  // valid steps in tile
 
-    // Per-warp prepass: {delta, delta, delta*x, delta*x} once per (step,
-    // channel), so a step's broadcast pairs are one 16-byte load per lane.
-    {
-      const IO* ds = Slot<K>::dt(st);
-#pragma unroll 4
-      for (int j = lane; j < K::T * K::CH; j += 32) {
-        const int t = j / K::CH, c = j % K::CH;
-        const float dt = E::get(ds, t * K::CPC + warp * K::CH + c);
-        const float u = dt * E::get(xs, t * K::CPC + warp * K::CH + c);
-        pre[j] = make_float4(dt, dt, u, u);
-      }
-      __syncwarp();
-    }
-    const float4* pre_l = pre + cw;                                   // this lane's channel
+    const IO* dl = Slot<K>::dt(st) + c_loc;                          // this lane's channel
+    const IO* xl = xs + c_loc;
     const IO* b_l = Slot<K>::B(st) + g * K::G;                        // this lane's states
     const IO* c_l = Slot<K>::C(st) + g * K::G;
     IO* yrow = yout + (b * L + t0) * p.dim + d;                       // y[b, t0, d]
 
-    // Output of one finished group [s, s + NG): the NG lanes of a channel swap
-    // their partial sums through `red`, and lane g finishes step s + g.
-    auto finish_group = [&](const float (&v)[K::NG], int s) {
-      float* r = red + cw * K::NG * (K::NG + 1);
-#pragma unroll
-      for (int u = 0; u < K::NG; ++u) r[u * (K::NG + 1) + g] = v[u];
-      __syncwarp();
-      float ysum = 0.f;
-#pragma unroll
-      for (int k = 0; k < K::NG; ++k) ysum += r[g * (K::NG + 1) + k];
-      __syncwarp();
+    // Output of one finished group [s, s + NG): a shuffle reduce-scatter over
+    // the channel's NG lanes leaves lane g with the full sum of step s + g
+    // (sum_n C_n h_n + D x); the gate and the store follow.
+    auto finish_group = [&](float (&v)[K::NG], int s) {
+      float yv = reduce_scatter<K::NG>(v, g);
       const int sg = s + g;
       if (d_ok && sg < steps) {
-        const float xv = E::get(xs, sg * K::CPC + c_loc);
-        float yv = fmaf(dskip, xv, ysum);                          // + D x
         if (K::GATE) yv *= silu(E::get(zs, sg * K::CPC + c_loc));  // * silu(z)
         E::put(yrow, static_cast<int64_t>(sg) * p.dim, yv);
       }
@@ -437,18 +440,18 @@ __global__ void __launch_bounds__(K::WPC * 32)
         // runs its recurrence and finished groups are reduced.  The last
         // prefetch of a run reads at most PAD rows past it, inside the slot.
         Batch<K> bA, bB;
-        batch_inputs<K>(pre_l, b_l, c_l, s0, a2, bA);
+        batch_inputs<K>(dl, xl, b_l, c_l, s0, a2, bA);
         for (int s = s0; s < run_end; s += K::BODY_STEPS) {
           float part[K::BODY_STEPS];
 #pragma unroll
           for (int k = 0; k < K::BODY; ++k) {
             const int sn = s + (k + 1) * K::U;
             if (k % 2 == 0) {
-              batch_inputs<K>(pre_l, b_l, c_l, sn, a2, bB);
-              batch_update<K>(h2, bA, part, k * K::U);
+              batch_inputs<K>(dl, xl, b_l, c_l, sn, a2, bB);
+              batch_update<K>(h2, bA, dg, part, k * K::U);
             } else {
-              batch_inputs<K>(pre_l, b_l, c_l, sn, a2, bA);
-              batch_update<K>(h2, bB, part, k * K::U);
+              batch_inputs<K>(dl, xl, b_l, c_l, sn, a2, bA);
+              batch_update<K>(h2, bB, dg, part, k * K::U);
             }
             if (((k + 1) * K::U) % K::NG == 0) {
               const int j = ((k + 1) * K::U) / K::NG - 1;  // group within the body
@@ -468,12 +471,14 @@ __global__ void __launch_bounds__(K::WPC * 32)
         for (int u = 0; u < K::NG; ++u) {
           const int s = s0 + u;
           u64 ab[K::P], bi[K::P], cq[K::P];
-          step_inputs<K>(pre_l + s * K::CH, b_l + s * K::N, c_l + s * K::N, a2, ab, bi, cq);
+          float xv;
+          step_inputs<K>(dl + s * K::CPC, xl + s * K::CPC, b_l + s * K::N, c_l + s * K::N, a2,
+                         ab, bi, cq, xv);
           if (s >= steps) {  // identity step (a = 1, b = 0), [P1] s2.3
 #pragma unroll
             for (int q = 0; q < K::P; ++q) { ab[q] = pk2(1.f, 1.f); bi[q] = pk2(0.f, 0.f); }
           }
-          part[u] = step_update<K>(h2, ab, bi, cq);
+          part[u] = step_update<K>(h2, ab, bi, cq, xv, dg);
           if (t0 + s == next_ce) {  // [P1] s3.4 chunk boundary state
             store_state(next_ce);
             ++next_c;

@@ -23,6 +23,11 @@ bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
 int64_t stream_grid(const ScanParams& p, StreamShape sh);
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);
 
+// WARPSCAN tier: one warp per (b, d), lanes along time, 5-round shuffle scan.
+bool warpscan_eligible(const ScanParams& p);
+int64_t warpscan_grid(const ScanParams& p);
+cudaError_t launch_warpscan(const ScanParams& p, bool bf16, cudaStream_t s);
+
 // Sticky device error word of the tiers with bounded waits: read and clear.
 bool read_and_clear_device_errors(unsigned int* word);
 
