@@ -42,6 +42,30 @@ def load_peaks() -> tuple[dict, str]:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def measured_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes (read + write) per launch from an ncu capture recorded in
+    profiles/traffic.json, if that capture was taken on the kernel sources as
+    they are now (sha256 of each listed file); None otherwise."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f)
+    for e in entries:
+        if e.get("kernel") != kernel or e.get("workload") != workload:
+            continue
+        ok = True
+        for rel, sha in e.get("sources", {}).items():
+            fp = os.path.join(ROOT, rel)
+            if not os.path.exists(fp) or hashlib.sha256(open(fp, "rb").read()).hexdigest() != sha:
+                ok = False
+                break
+        if ok:
+            return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
+    return None
+
+
 def algorithmic_counts(w, inp) -> dict:
     """Work the method must do for one forward (independent of the kernel):
     valid (b,t,d) elements, exps, fp32 ops and HBM bytes (inputs read once,
@@ -174,6 +198,33 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks (identity when not distributed).
+    Each rank runs its own replica of the workload, so the job's time is the
+    slowest rank's time; this is the only collective the benchmark uses."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: int, ms: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes
+    units_per_rank units, and the job takes the slowest rank's ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
+def shard_rows(batch: int, rank: int, world: int) -> tuple[int, int]:
+    """Batch rows [lo, hi) of a rank when one workload is split across ranks by
+    batch row (rows are independent recurrences; no data-path exchange)."""
+    per, extra = divmod(batch, world)
+    lo = rank * per + min(rank, extra)
+    return lo, lo + per + (1 if rank < extra else 0)
+
+
 def reference_arm(args, w):
     """The fp64 CPU oracle, as it stands, on the host cores (rank 0 only)."""
     rank, world, _ = dist_env()
@@ -283,12 +334,8 @@ def main():
     if world > 1:
         dist.barrier()
     per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms, one launch each
-    ms = sum(per_step) / K
-    if world > 1:
-        m = torch.tensor([ms], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        ms = float(m.item())
-    value = world * counts["elements"] / (ms * 1e-3)
+    ms = max_over_ranks(sum(per_step) / K, dev)
+    value = job_rate(world, counts["elements"], ms)
 
     # End to end through the C ABI with host buffers: H2D of the step's inputs from
     # pinned memory, the forward, D2H of y (and chunk states), every step.
@@ -317,11 +364,7 @@ def main():
         step_host()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms_e2e = e0.elapsed_time(e1) / KE
-    if world > 1:
-        m = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        ms_e2e = float(m.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / KE, dev)
     es = 2 if w.dtype == "bf16" else 4
     h2d = sum(v.numel() * v.element_size() for k, v in pinned.items()
               if isinstance(v, torch.Tensor))
@@ -340,12 +383,14 @@ def main():
     if r["t_hbm"] >= max(r["t_mufu"], r["t_fp32"]):
         achieved = counts["bytes"] / t_meas / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None}
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": measured_traffic(S.kernel_name(kernel), w.name)}
     else:
         pk = MUFU_PER_SM_CLK * sms * sm_mhz_peak * 1e6 / 1e9
         achieved = counts["exps"] / t_meas / 1e9
         roofline = {"bound": "alu", "achieved": achieved, "peak": pk, "unit": "Gex2/s",
-                    "frac": achieved / pk, "traffic": None}
+                    "frac": achieved / pk,
+                    "traffic": measured_traffic(S.kernel_name(kernel), w.name)}
     roofline.update({
         "peak_source": f"{peaks_src} (HBM copy GB/s); ALU = {MUFU_PER_SM_CLK} ex2 and "
                        f"{FP32_PER_SM_CLK} fp32 lanes/clk/SM x {sms} SMs x {sm_mhz_peak:.0f} MHz",
@@ -373,7 +418,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * counts["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_rate(world, counts["elements"], ms_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": K,
         "clocks": clk,
@@ -382,7 +427,7 @@ def main():
                         "max": max(per_step)},
     }
     if counts["valid_elements"] != counts["elements"]:
-        line["valid_elements_per_s"] = world * counts["valid_elements"] / (ms * 1e-3)
+        line["valid_elements_per_s"] = job_rate(world, counts["valid_elements"], ms)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

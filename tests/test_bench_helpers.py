@@ -1,0 +1,44 @@
+"""Benchmark bookkeeping on CPU: algorithmic work counts and the roofline
+arithmetic, checked against hand-computed values for two workloads."""
+import numpy as np
+import pytest
+
+import bench
+from selective_state_space_fwd_gb300 import workloads as W
+
+
+def test_counts_fp32_workload():
+    w = W.WORKLOADS[2]
+    inp = {"valid_len": None}
+    c = bench.algorithmic_counts(w, inp)
+    e = 8 * 4096 * 1024
+    assert c["elements"] == e and c["valid_elements"] == e
+    assert c["exps"] == e * 16                       # one exp per (t, d, n)
+    assert c["fp32_ops"] == 4 * e * 16 + 2 * e
+    # x, delta read + y written (4 B each) + B, C rows + A + D
+    assert c["bytes"] == 3 * e * 4 + 2 * 8 * 4096 * 16 * 4 + 1024 * 16 * 4 + 1024 * 4
+
+
+def test_counts_masked_gated_workload():
+    w = W.WORKLOADS[4]
+    vl = np.array([64, 2048, 3000, 0] + [100] * 28, np.int32)
+    c = bench.algorithmic_counts(w, {"valid_len": vl})
+    rows = 64 + 2048 + 2048 + 0 + 100 * 28             # clamped to L
+    ev = rows * 1536
+    assert c["valid_elements"] == ev
+    assert c["exps"] == ev * 16 + ev                   # + one exp per gated element
+    nch = 2048 // 256
+    assert c["bytes"] == (3 * ev * 2 + 32 * 2048 * 1536 * 2 + 2 * rows * 16 * 2
+                          + 1536 * 16 * 4 + 1536 * 4 + 32 * 4 + 32 * nch * 1536 * 16 * 4)
+
+
+def test_roof_terms():
+    c = {"bytes": 6684.5e9, "exps": 32 * 152 * 2070e6, "fp32_ops": 128 * 152 * 2070e6}
+    r = bench.roof(c, {"hbm_gbs": 6684.5}, 152, 2070.0)
+    assert r["t_hbm"] == pytest.approx(1.0) and r["t_mufu"] == pytest.approx(1.0)
+    assert r["t_fp32"] == pytest.approx(1.0) and r["t_roof"] == pytest.approx(1.0)
+
+
+def test_measured_traffic_requires_matching_sources():
+    assert bench.measured_traffic("stream", "no-such-workload") is None
+    assert bench.measured_traffic("serial", W.WORKLOADS[2].name) is None
