@@ -93,6 +93,9 @@ typedef struct {
   int32_t warps_per_block; /* 0 = the tier's default; STREAM accepts 1, 2 or 4 */
   int32_t states_per_lane; /* 0 = the tier's default; STREAM: 2, 4, 8 or 16 states of one
                               channel per thread (fewer = more threads, more reduction) */
+  int32_t time_split;      /* 0 = the tier's default; STREAM: 1, or 2 = the two half-warps
+                              take consecutive runs of each 16-step sub-tile and join them
+                              with a one-round scan ([P1] s3.1), doubling the threads */
 } ssm_options;
 
 /*

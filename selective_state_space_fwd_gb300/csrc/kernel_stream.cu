@@ -194,14 +194,18 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NG], int g) {
   return v[0];
 }
 
-template <int N_, int NG_, int T_, int STAGES_, int WPC_, typename IO_, bool GATE_>
+template <int N_, int NG_, int T_, int STAGES_, int WPC_, typename IO_, bool GATE_, int TS_ = 1>
 struct Cfg {
-  static constexpr int N = N_, NG = NG_, T = T_, STAGES = STAGES_, WPC = WPC_;
+  static constexpr int N = N_, NG = NG_, T = T_, STAGES = STAGES_, WPC = WPC_, TS = TS_;
   static constexpr bool GATE = GATE_;
   using IO = IO_;
   static constexpr int G = N / NG;          // states per lane
   static constexpr int P = G / 2;           // state pairs per lane
-  static constexpr int CH = 32 / NG;        // channels per warp
+  static constexpr int CH = 32 / NG / TS;   // channels per warp
+  // time split (TS = 2): each half-warp takes KS consecutive steps of a
+  // sub-tile of TS * KS steps
+  static constexpr int KS = 8;
+  static constexpr int SUB = TS * KS;
   static constexpr int CPC = CH * WPC;      // channels per CTA
   // Steps per input batch: about 8 state pairs of inputs formed ahead.
   static constexpr int U = (8 / P < 1) ? 1 : (8 / P > NG ? NG : 8 / P);
@@ -222,6 +226,7 @@ struct Cfg {
   static_assert((CPC * ES) % 16 == 0 && (N * ES) % 16 == 0, "TMA box rows are 16-byte multiples");
   static_assert(T <= 256 && T % NG == 0 && T % BODY_STEPS == 0, "tile steps");
   static_assert(NG % U == 0 && BODY % 2 == 0, "pipelined body alternates two input buffers");
+  static_assert(TS == 1 || (TS == 2 && KS % NG == 0 && T % SUB == 0), "time split shape");
 };
 
 template <class K>
@@ -268,6 +273,26 @@ __device__ __forceinline__ void step_inputs(const typename K::IO* dl, const type
   u64 bq[K::P];
   E::template pairs<K::P>(brow, bq);
   E::template pairs<K::P>(crow, cq);
+#pragma unroll
+  for (int q = 0; q < K::P; ++q) {
+    const float2 arg = upk2(mul2(a2[q], dd));
+    ab[q] = pk2(ex2(arg.x), ex2(arg.y));
+    bi[q] = mul2(bq[q], ux);
+  }
+}
+
+// As step_inputs, without the C row (the first pass of a time-split run).
+template <class K>
+__device__ __forceinline__ void step_inputs_ab(const typename K::IO* dl, const typename K::IO* xl,
+                                               const typename K::IO* brow, const u64 (&a2)[K::P],
+                                               u64 (&ab)[K::P], u64 (&bi)[K::P], float& xv) {
+  using E = Elem<typename K::IO>;
+  const float dt = E::get(dl, 0);
+  xv = E::get(xl, 0);
+  const float uu = dt * xv;
+  const u64 dd = pk2(dt, dt), ux = pk2(uu, uu);
+  u64 bq[K::P];
+  E::template pairs<K::P>(brow, bq);
 #pragma unroll
   for (int q = 0; q < K::P; ++q) {
     const float2 arg = upk2(mul2(a2[q], dd));
@@ -338,7 +363,8 @@ __global__ void __launch_bounds__(K::WPC * 32)
   const int64_t n_cg = (p.dim + K::CPC - 1) / K::CPC;
   const int64_t b = blockIdx.x / n_cg;
   const int d0 = static_cast<int>((blockIdx.x % n_cg) * K::CPC);
-  const int cw = lane / K::NG;                     // channel within the warp
+  const int hf = K::TS == 2 ? lane >> 4 : 0;      // time half of this lane (TS = 2)
+  const int cw = (lane % (32 / K::TS)) / K::NG;    // channel within the warp
   const int c_loc = warp * K::CH + cw;             // channel within the CTA tile
   const int g = lane % K::NG;                      // state group of this lane
   const int64_t d = d0 + c_loc;
@@ -428,6 +454,92 @@ __global__ void __launch_bounds__(K::WPC * 32)
       }
     };
 
+    if constexpr (K::TS == 2) {
+      // Time split: half-warp hf takes steps [s + hf KS, s + hf KS + KS) of each
+      // sub-tile.  Each lane folds its run into (A, Bsum) keeping every step's
+      // (a, b) ([P1] s3.1 first level), the halves exchange the state in one
+      // shuffle round (a two-element Hillis-Steele scan, [P1] s2.2), and both
+      // replay their runs to form h and C h.
+      for (int s = 0; s < steps; s += K::SUB) {
+        const int r0 = s + hf * K::KS;                        // first step of this lane's run
+        const int64_t sub_end = t0 + s + K::SUB - 1;          // last step of the sub-tile
+        const bool full = s + K::SUB <= steps;
+        const bool inner_ce = next_ce < sub_end;              // a chunk end before the last step
+        u64 ab[K::KS][K::P], bi[K::KS][K::P];
+        float xv[K::KS];
+#pragma unroll
+        for (int j = 0; j < K::KS; ++j) {
+          step_inputs_ab<K>(dl + (r0 + j) * K::CPC, xl + (r0 + j) * K::CPC, b_l + (r0 + j) * K::N,
+                            a2, ab[j], bi[j], xv[j]);
+          if (!full && r0 + j >= steps) {  // identity step (a = 1, b = 0), [P1] s2.3
+#pragma unroll
+            for (int q = 0; q < K::P; ++q) { ab[j][q] = pk2(1.f, 1.f); bi[j][q] = pk2(0.f, 0.f); }
+          }
+        }
+        u64 A[K::P], Bs[K::P], h[K::P];
+#pragma unroll
+        for (int q = 0; q < K::P; ++q) {
+          A[q] = ab[0][q];
+          Bs[q] = bi[0][q];
+#pragma unroll
+          for (int j = 1; j < K::KS; ++j) {  // (A, Bs) o (a_j, b_j)
+            Bs[q] = fma2(ab[j][q], Bs[q], bi[j][q]);
+            A[q] = mul2(A[q], ab[j][q]);
+          }
+          // state after the first half, sent to the second half
+          const float2 e1 = upk2(fma2(A[q], h2[q], Bs[q]));
+          const float r1x = __shfl_xor_sync(0xffffffffu, e1.x, 16);
+          const float r1y = __shfl_xor_sync(0xffffffffu, e1.y, 16);
+          h[q] = hf ? pk2(r1x, r1y) : h2[q];                  // state before this lane's run
+          const float2 e2 = upk2(fma2(A[q], h[q], Bs[q]));    // second half: sub-tile end
+          const float r2x = __shfl_xor_sync(0xffffffffu, e2.x, 16);
+          const float r2y = __shfl_xor_sync(0xffffffffu, e2.y, 16);
+          h2[q] = hf ? pk2(e2.x, e2.y) : pk2(r2x, r2y);       // carried to the next sub-tile
+        }
+        float part[K::KS];
+        int64_t ce = INT64_MAX;  // first chunk end at or after this lane's run
+        if (inner_ce) {
+          ce = ((t0 + r0) / p.chunk_len + 1) * p.chunk_len - 1;
+          if (ce > L - 1) ce = L - 1;
+        }
+#pragma unroll
+        for (int j = 0; j < K::KS; ++j) {
+          u64 cq[K::P];
+          E::template pairs<K::P>(c_l + (r0 + j) * K::N, cq);
+          u64 acc = 0;
+#pragma unroll
+          for (int q = 0; q < K::P; ++q) {
+            h[q] = fma2(ab[j][q], h[q], bi[j][q]);
+            acc = q == 0 ? mul2(cq[q], h[q]) : fma2(cq[q], h[q], acc);
+          }
+          const float2 a = upk2(acc);
+          part[j] = fmaf(dg, xv[j], a.x + a.y);
+          if (inner_ce && t0 + r0 + j == ce) {  // [P1] s3.4: a chunk ends inside this run
+            if (d_ok) {
+              float* sp = p.states + ((b * p.n_chunks + ce / p.chunk_len) * p.dim + d) * K::N +
+                          g * K::G;
+#pragma unroll
+              for (int q = 0; q < K::P; ++q) reinterpret_cast<float2*>(sp)[q] = upk2(h[q]);
+            }
+            ce = ce + p.chunk_len > L - 1 ? (ce == L - 1 ? INT64_MAX : L - 1) : ce + p.chunk_len;
+          }
+        }
+        // chunk ends in this sub-tile: interior ones were stored above by the
+        // owning half; the one at the sub-tile's last step is the carried state
+        while (next_ce <= sub_end) {
+          if (next_ce == sub_end && hf == 1) store_state(next_ce);
+          ++next_c;
+          next_ce = next_c < p.n_chunks ? chunk_end(next_c) : INT64_MAX;
+        }
+#pragma unroll
+        for (int k0 = 0; k0 < K::KS; k0 += K::NG) {
+          float v[K::NG];
+#pragma unroll
+          for (int i2 = 0; i2 < K::NG; ++i2) v[i2] = part[k0 + i2];
+          finish_group(v, r0 + k0);
+        }
+      }
+    } else {
     int s0 = 0;
     while (s0 < steps) {
       // Longest run [s0, run_end) of whole bodies with no chunk end inside.
@@ -489,6 +601,7 @@ __global__ void __launch_bounds__(K::WPC * 32)
         s0 += K::NG;
       }
     }
+    }  // TS
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
   }
@@ -500,7 +613,7 @@ __global__ void __launch_bounds__(K::WPC * 32)
   // Steps past valid_len: exact zeros, frozen state for the remaining chunk ends.
   if (lv < L) {
     const int per = 32 / K::CH;  // steps covered by one pass of the warp
-    const int cz = lane % K::CH, sz = lane / K::CH;
+    const int cz = lane % K::CH, sz = lane / K::CH;  // (channel, step) of this lane
     const int64_t dz = d0 + warp * K::CH + cz;
     if (dz < p.dim)
       for (int64_t t = lv + sz; t < L; t += per) E::put(yout, (b * L + t) * p.dim + dz, 0.f);
@@ -584,24 +697,24 @@ cudaError_t launch_k(const ScanParams& p, cudaStream_t s) {
 
 // Instances: (N, NG = N / G) per state size, tile T, ring depth, warps per CTA.
 #define SSM_STREAM_INSTANCES(X)                                          \
-  X(8, 2, 1) X(8, 2, 2) X(8, 4, 1) X(8, 4, 2)                            \
-  X(16, 2, 2) X(16, 2, 4) X(16, 4, 1) X(16, 4, 2) X(16, 4, 4)            \
-  X(16, 8, 1) X(16, 8, 2)                                                \
-  X(32, 4, 2) X(32, 8, 1) X(32, 8, 2)                                    \
-  X(64, 8, 2) X(64, 8, 4) X(64, 16, 2) X(64, 16, 4)
+  X(8, 4, 1, 1) X(8, 4, 2, 1)                                            \
+  X(16, 4, 1, 1) X(16, 4, 2, 1) X(16, 4, 4, 1) X(16, 8, 2, 1)            \
+  X(16, 4, 2, 2) X(16, 4, 4, 2)                                          \
+  X(32, 4, 2, 1) X(32, 8, 2, 1) X(32, 4, 4, 2)                           \
+  X(64, 8, 2, 1) X(64, 8, 4, 1) X(64, 16, 2, 1) X(64, 8, 4, 2)
 
 template <typename IO, bool GATE>
 cudaError_t launch_io(const ScanParams& p, cudaStream_t s, StreamShape sh) {
-#define SSM_CASE(n_, g_, w_)                                                          \
-  if (p.dstate == n_ && sh.g == g_ && sh.wpc == w_)                                   \
-    return launch_k<Cfg<n_, n_ / g_, SSM_STREAM_T, SSM_STREAM_STAGES, w_, IO, GATE>>(p, s);
+#define SSM_CASE(n_, g_, w_, ts_)                                                     \
+  if (p.dstate == n_ && sh.g == g_ && sh.wpc == w_ && sh.ts == ts_)                   \
+    return launch_k<Cfg<n_, n_ / g_, SSM_STREAM_T, SSM_STREAM_STAGES, w_, IO, GATE, ts_>>(p, s);
   SSM_STREAM_INSTANCES(SSM_CASE)
 #undef SSM_CASE
   return cudaErrorInvalidValue;
 }
 
-bool has_instance(int n, int g, int w) {
-#define SSM_HAS(n_, g_, w_) if (n == n_ && g == g_ && w == w_) return true;
+bool has_instance(int n, int g, int w, int ts) {
+#define SSM_HAS(n_, g_, w_, ts_) if (n == n_ && g == g_ && w == w_ && ts == ts_) return true;
   SSM_STREAM_INSTANCES(SSM_HAS)
 #undef SSM_HAS
   return false;
@@ -609,16 +722,18 @@ bool has_instance(int n, int g, int w) {
 
 }  // namespace
 
-StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane) {
+StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane,
+                         int time_split) {
   StreamShape sh;
   sh.g = states_per_lane ? states_per_lane : (p.dstate >= 64 ? 8 : 4);
   sh.wpc = warps_per_block ? warps_per_block : 2;
-  if (!has_instance(p.dstate, sh.g, sh.wpc)) return StreamShape{0, 0};
+  sh.ts = time_split ? time_split : 1;
+  if (!has_instance(p.dstate, sh.g, sh.wpc, sh.ts)) return StreamShape{0, 0, 0};
   return sh;
 }
 
 static int stream_cpc(StreamShape sh, int dstate) {
-  return sh.g ? (32 / (dstate / sh.g)) * sh.wpc : 0;
+  return sh.g ? (32 / (dstate / sh.g) / sh.ts) * sh.wpc : 0;
 }
 
 bool read_and_clear_device_errors(unsigned int* word) {

@@ -60,7 +60,26 @@ __device__ __forceinline__ u64 shfl_idx2(u64 v, int src) {
   return pk2(__shfl_sync(0xffffffffu, f.x, src), __shfl_sync(0xffffffffu, f.y, src));
 }
 
+// Asynchronous global -> shared copies of 4 or 8 bytes (cp.async); when `pred`
+// is false nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void cp_async4(float* dst, const float* src, bool pred) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(pred ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(float* dst, const float* src, bool pred) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(pred ? 8 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 constexpr int kWarps = 4;  // channels per block
+constexpr int kQ = 2;      // state pairs interleaved per pass
 
 // Position of step r of a per-channel row in shared memory.  Lane l = r / K
 // owns K consecutive steps; with K = 8 its two float4 halves are stored in an
@@ -111,7 +130,8 @@ __device__ __forceinline__ void load_run(const float* tile, int lane, float (&v)
   }
 }
 
-template <int N, typename T, bool GATE>
+// ASYNC: fp32 inputs with 8-byte aligned B and C, staged with cp.async.
+template <int N, typename T, bool GATE, bool ASYNC>
 __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams p) {
   using C = WCfg<N, T>;
   constexpr int K = C::K, W = C::W;
@@ -144,31 +164,61 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
     const int nv = static_cast<int>(rem <= 0 ? 0 : (rem < nw ? rem : nw));  // valid steps
     __syncthreads();  // the previous window is fully consumed
     if (nv > 0) {
-      // Stage the window: x, delta (, z) transposed per channel, B and C rows.
-      for (int r = threadIdx.x; r < W; r += blockDim.x) {
-        const bool in = r < nv;  // identity steps read as zero
-        const int pos = act_pos<K>(r);
-        const int64_t e = (b * L + t0 + r) * p.dim + d0;
+      // Stage the window: x, delta (, z) transposed per channel, B and C rows
+      // (steps past the valid length are zero-filled: identity steps).
+      if constexpr (ASYNC) {
+        const float* gx = static_cast<const float*>(p.x);
+        const float* gd = static_cast<const float*>(p.delta);
+        const float* gz = static_cast<const float*>(p.z);
+        const float* gb = static_cast<const float*>(p.B);
+        const float* gc = static_cast<const float*>(p.C);
+        for (int r = threadIdx.x; r < W; r += blockDim.x) {
+          const bool in = r < nv;
+          const int pos = act_pos<K>(r);
+          const int64_t e = in ? (b * L + t0 + r) * p.dim + d0 : 0;
 #pragma unroll
-        for (int c = 0; c < kWarps; ++c) {
-          const bool ok = in && d0 + c < p.dim;
-          xs[c * W + pos] = ok ? IO<T>::load(p.x, e + c) : 0.f;
-          ds[c * W + pos] = ok ? IO<T>::load(p.delta, e + c) : 0.f;
-          if (GATE) zs[c * W + pos] = ok ? IO<T>::load(p.z, e + c) : 0.f;
+          for (int c = 0; c < kWarps; ++c) {
+            const bool ok = in && d0 + c < p.dim;
+            cp_async4(xs + c * W + pos, gx + (ok ? e + c : 0), ok);
+            cp_async4(ds + c * W + pos, gd + (ok ? e + c : 0), ok);
+            if (GATE) cp_async4(zs + c * W + pos, gz + (ok ? e + c : 0), ok);
+          }
         }
-      }
-      for (int i = threadIdx.x; i < W * N / 2; i += blockDim.x) {  // state pairs
-        const int r = (2 * i) / N, n = (2 * i) % N;
-        const bool in = r < nv;
-        const int64_t e = (b * L + t0 + r) * N + n;
-        const int col = bc_col<N>(n, r / K);
-        float2 bv = make_float2(0.f, 0.f), cv = make_float2(0.f, 0.f);
-        if (in) {
-          bv = make_float2(IO<T>::load(p.B, e), IO<T>::load(p.B, e + 1));
-          cv = make_float2(IO<T>::load(p.C, e), IO<T>::load(p.C, e + 1));
+        for (int i = threadIdx.x; i < W * N / 2; i += blockDim.x) {  // state pairs
+          const int r = (2 * i) / N, n = (2 * i) % N;
+          const bool in = r < nv;
+          const int64_t e = in ? (b * L + t0 + r) * N + n : 0;
+          const int col = bc_col<N>(n, r / K);
+          cp_async8(bs + r * N + col, gb + e, in);
+          cp_async8(cs + r * N + col, gc + e, in);
         }
-        *reinterpret_cast<float2*>(bs + r * N + col) = bv;
-        *reinterpret_cast<float2*>(cs + r * N + col) = cv;
+        cp_async_wait_all();
+      } else {
+        for (int r = threadIdx.x; r < W; r += blockDim.x) {
+          const bool in = r < nv;
+          const int pos = act_pos<K>(r);
+          const int64_t e = (b * L + t0 + r) * p.dim + d0;
+#pragma unroll
+          for (int c = 0; c < kWarps; ++c) {
+            const bool ok = in && d0 + c < p.dim;
+            xs[c * W + pos] = ok ? IO<T>::load(p.x, e + c) : 0.f;
+            ds[c * W + pos] = ok ? IO<T>::load(p.delta, e + c) : 0.f;
+            if (GATE) zs[c * W + pos] = ok ? IO<T>::load(p.z, e + c) : 0.f;
+          }
+        }
+        for (int i = threadIdx.x; i < W * N / 2; i += blockDim.x) {  // state pairs
+          const int r = (2 * i) / N, n = (2 * i) % N;
+          const bool in = r < nv;
+          const int64_t e = (b * L + t0 + r) * N + n;
+          const int col = bc_col<N>(n, r / K);
+          float2 bv = make_float2(0.f, 0.f), cv = make_float2(0.f, 0.f);
+          if (in) {
+            bv = make_float2(IO<T>::load(p.B, e), IO<T>::load(p.B, e + 1));
+            cv = make_float2(IO<T>::load(p.C, e), IO<T>::load(p.C, e + 1));
+          }
+          *reinterpret_cast<float2*>(bs + r * N + col) = bv;
+          *reinterpret_cast<float2*>(cs + r * N + col) = cv;
+        }
       }
       __syncthreads();
 
@@ -193,62 +243,91 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
       }
       const bool run_has_ce = ce0 < t0 + row0 + K;
 
-      for (int n = 0; n < N; n += 2) {
-        const int col = bc_col<N>(n, lane);
-        float alo = 0.f, ahi = 0.f;
-        if (d_ok) {
-          alo = __ldg(p.A + d * N + n) * kLog2e;
-          ahi = __ldg(p.A + d * N + n + 1) * kLog2e;
+      // kQ state pairs per pass: their folds, scans and replays are independent,
+      // so their shuffle and MUFU latencies overlap.
+      for (int n0 = 0; n0 < N; n0 += 2 * kQ) {
+        int col[kQ];
+        u64 a2[kQ];
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const int n = n0 + 2 * q;
+          col[q] = bc_col<N>(n, lane);
+          float alo = 0.f, ahi = 0.f;
+          if (d_ok) {
+            alo = __ldg(p.A + d * N + n) * kLog2e;
+            ahi = __ldg(p.A + d * N + n + 1) * kLog2e;
+          }
+          a2[q] = pk2(alo, ahi);
         }
-        const u64 a2 = pk2(alo, ahi);
         // 1. thread-serial fold of the lane's K steps, keeping each (a, b)
-        u64 av[K], bv[K];
-        u64 A = 0, Bsum = 0;
+        u64 av[kQ][K], bv[kQ][K], A[kQ], Bsum[kQ];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-          const u64 bq = *reinterpret_cast<const u64*>(bs + (row0 + j) * N + col);
-          const float2 arg = upk2(mul2(a2, dd[j]));
-          av[j] = pk2(ex2(arg.x), ex2(arg.y));  // Abar = exp(delta A)
-          bv[j] = mul2(bq, uu[j]);               // delta B x
-          if (j == 0) {
-            A = av[0];
-            Bsum = bv[0];
-          } else {  // (A, Bsum) o (a_j, b_j)
-            Bsum = fma2(av[j], Bsum, bv[j]);
-            A = mul2(A, av[j]);
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            const u64 bq = *reinterpret_cast<const u64*>(bs + (row0 + j) * N + col[q]);
+            const float2 arg = upk2(mul2(a2[q], dd[j]));
+            av[q][j] = pk2(ex2(arg.x), ex2(arg.y));  // Abar = exp(delta A)
+            bv[q][j] = mul2(bq, uu[j]);               // delta B x
+            if (j == 0) {
+              A[q] = av[q][0];
+              Bsum[q] = bv[q][0];
+            } else {  // (A, Bsum) o (a_j, b_j)
+              Bsum[q] = fma2(av[q][j], Bsum[q], bv[q][j]);
+              A[q] = mul2(A[q], av[q][j]);
+            }
           }
         }
         // 2. 5-round Hillis-Steele inclusive scan across the warp, b before a
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-          const u64 Aup = shfl_up2(A, off), Bup = shfl_up2(Bsum, off);
-          if (lane >= off) {
-            Bsum = fma2(A, Bup, Bsum);  // b = a_self * b_prev + b_self (old a)
-            A = mul2(A, Aup);
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            const u64 Aup = shfl_up2(A[q], off), Bup = shfl_up2(Bsum[q], off);
+            if (lane >= off) {
+              Bsum[q] = fma2(A[q], Bup, Bsum[q]);  // b = a_self * b_prev + b_self (old a)
+              A[q] = mul2(A[q], Aup);
+            }
           }
         }
         // 3. window carry: the state before this lane's run, then the replay
-        const u64 hin = pk2(carry[warp * N + n], carry[warp * N + n + 1]);
-        const u64 hend = fma2(A, hin, Bsum);  // state after this lane's run
-        u64 h = shfl_up2(hend, 1);
-        if (lane == 0) h = hin;
-        const u64 hlast = shfl_idx2(hend, 31);  // state entering the next window
+        u64 h[kQ], hlast[kQ];
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          const int n = n0 + 2 * q;
+          const u64 hin = pk2(carry[warp * N + n], carry[warp * N + n + 1]);
+          const u64 hend = fma2(A[q], hin, Bsum[q]);  // state after this lane's run
+          h[q] = shfl_up2(hend, 1);
+          if (lane == 0) h[q] = hin;
+          hlast[q] = shfl_idx2(hend, 31);  // state entering the next window
+        }
         int64_t ce = ce0;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-          h = fma2(av[j], h, bv[j]);
-          const u64 cq = *reinterpret_cast<const u64*>(cs + (row0 + j) * N + col);
-          y2[j] = fma2(cq, h, y2[j]);
-          if (run_has_ce && t0 + row0 + j == ce) {
+#pragma unroll
+          for (int q = 0; q < kQ; ++q) {
+            h[q] = fma2(av[q][j], h[q], bv[q][j]);
+            const u64 cq = *reinterpret_cast<const u64*>(cs + (row0 + j) * N + col[q]);
+            y2[j] = fma2(cq, h[q], y2[j]);
+          }
+          if (run_has_ce && t0 + row0 + j == ce) {  // [P1] s3.4 chunk boundary state
             if (d_ok) {
-              float* sp = p.states + ((b * p.n_chunks + ce / p.chunk_len) * p.dim + d) * N + n;
-              *reinterpret_cast<float2*>(sp) = upk2(h);
+#pragma unroll
+              for (int q = 0; q < kQ; ++q) {
+                float* sp = p.states +
+                            ((b * p.n_chunks + ce / p.chunk_len) * p.dim + d) * N + n0 + 2 * q;
+                *reinterpret_cast<float2*>(sp) = upk2(h[q]);
+              }
             }
             ce = ce + p.chunk_len > L - 1 ? (ce == L - 1 ? INT64_MAX : L - 1) : ce + p.chunk_len;
           }
         }
         __syncwarp();
-        if (lane == 0) *reinterpret_cast<float2*>(carry + warp * N + n) = upk2(hlast);
+        if (lane == 0) {
+#pragma unroll
+          for (int q = 0; q < kQ; ++q)
+            *reinterpret_cast<float2*>(carry + warp * N + n0 + 2 * q) = upk2(hlast[q]);
+        }
         __syncwarp();
       }
       // epilogue: y = (sum_n C h + D x) * silu(z); exact 0 at identity steps
@@ -295,10 +374,14 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
 template <int N, typename T>
 cudaError_t launch_nt(const ScanParams& p, cudaStream_t s) {
   using C = WCfg<N, T>;
-  static bool attr_done[2] = {false, false};
+  static bool attr_done[4] = {false, false, false, false};
   const int64_t grid = (p.dim + kWarps - 1) / kWarps * p.batch;
-  const int gi = p.z ? 1 : 0;
-  auto kern = p.z ? warpscan_kernel<N, T, true> : warpscan_kernel<N, T, false>;
+  constexpr bool kF32 = sizeof(T) == 4;
+  const bool async = kF32 && (reinterpret_cast<uintptr_t>(p.B) % 8 == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.C) % 8 == 0);
+  const int gi = (p.z ? 1 : 0) + (async ? 2 : 0);
+  auto kern = async ? (p.z ? warpscan_kernel<N, T, true, kF32> : warpscan_kernel<N, T, false, kF32>)
+                    : (p.z ? warpscan_kernel<N, T, true, false> : warpscan_kernel<N, T, false, false>);
   if (!attr_done[gi]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;

@@ -16,9 +16,11 @@ int64_t serial_grid(const ScanParams& p);
 struct StreamShape {
   int wpc;  // warps per thread block
   int g;    // states per lane
+  int ts;   // time split: 1, or 2 half-warps on consecutive runs of a sub-tile
 };
-// The launch shape for a request (0 = default); {0, 0} when no instance exists.
-StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane);
+// The launch shape for a request (0 = default); all zero when no instance exists.
+StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane,
+                         int time_split);
 bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
 int64_t stream_grid(const ScanParams& p, StreamShape sh);
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);

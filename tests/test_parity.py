@@ -15,7 +15,15 @@ from selective_state_space_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-TIERS = ["serial", "warpscan", "stream", "auto"]
+# (tier, time_split): "stream2t" is the STREAM tier with its two half-warps on
+# consecutive runs of each sub-tile
+TIERS = ["serial", "warpscan", "stream", "stream2t", "auto"]
+
+
+def _tier(kernel):
+    return ("stream", 2) if kernel == "stream2t" else (kernel, 0)
+
+
 TOL_Y = {"f32": 1e-5, "bf16": 1e-2}
 TOL_STATES = 1e-5
 
@@ -32,8 +40,9 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 
 def run_gpu(inp: dict, kernel="auto"):
     t = W.to_torch(inp, "cuda")
+    k, ts = _tier(kernel)
     y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
-                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=kernel)
+                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, time_split=ts)
     torch.cuda.synchronize()
     return to_f64(y), (to_f64(s) if s is not None else None)
 
@@ -68,9 +77,11 @@ def tier_supported(inp, kernel):
     if kernel == "auto":
         return True
     Bt, L, Dm = inp["x"].shape
+    k, ts = _tier(kernel)
     try:
         S.plan(Bt, L, Dm, inp["B"].shape[-1], dtype=inp["dtype"], gate=inp["z"] is not None,
-               mask=inp["valid_len"] is not None, chunk_len=inp["chunk_len"], kernel=kernel)
+               mask=inp["valid_len"] is not None, chunk_len=inp["chunk_len"], kernel=k,
+               time_split=ts)
         return True
     except S.SsmError as e:
         assert e.status == S.Status.ERR_UNSUPPORTED
