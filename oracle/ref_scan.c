@@ -29,8 +29,9 @@
  *   - delta arrives already positive (after softplus); it is not transformed.
  *   - The optional gate multiplies the whole output by silu(z) = z / (1+e^-z),
  *     after the D residual is added.
- *   - h_0 = 0.  Steps t >= valid_len[b] are the identity map (a=1, b=0): the
- *     state is frozen and the output there is exactly 0.
+ *   - The state before the first step is h0 when given, else 0.  Steps
+ *     t >= valid_len[b] are the identity map (a=1, b=0): the state is frozen
+ *     and the output there is exactly 0.
  *   - The chunk boundary state of chunk c is the global state h at step
  *     min((c+1)*chunk_len, L) - 1.
  *
@@ -95,17 +96,21 @@ static double ref_silu(double z) { return z / (1.0 + exp(-z)); }
  * Layouts (row-major, contiguous): x, delta, z, y are [batch, seqlen, dim];
  * B, C are [batch, seqlen, dstate] (shared by every channel d); A is
  * [dim, dstate] fp32; D is [dim] fp32 (NULL = no residual); z NULL = no gate;
- * valid_len is [batch] int32 (NULL = every step valid).  y_out receives
+ * valid_len is [batch] int32 (NULL = every step valid); h0 is the state before
+ * the first step, [batch, dim, dstate] fp32 (NULL = zeros).  y_out receives
  * [batch, seqlen, dim] doubles.  states_out (NULL = not wanted, also when
- * chunk_len <= 0) receives [batch, ceil(seqlen/chunk_len), dim, dstate] doubles.
+ * chunk_len <= 0) receives [batch, ceil(seqlen/chunk_len), dim, dstate] doubles;
+ * final_out (NULL = not wanted) receives the state after the last step,
+ * [batch, dim, dstate] doubles.
  * nthreads <= 0 lets OpenMP choose.  The (b, d) loop is parallel only for
  * speed: each channel is computed by exactly one thread, in program order.
  * Returns 0, or -1 on bad sizes or a failed allocation.
  */
-int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
-                 const float* D, const void* z, const int32_t* valid_len, double* y_out,
-                 double* states_out, int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
-                 int64_t chunk_len, int dtype, int nthreads) {
+int ref_scan_fwd_h0(const void* x, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const int32_t* valid_len,
+                    const float* h0, double* y_out, double* states_out, double* final_out,
+                    int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t chunk_len,
+                    int dtype, int nthreads) {
   if (batch < 0 || seqlen < 0 || dim < 0 || dstate < 1) return -1;
   if (dtype != REF_F32 && dtype != REF_BF16) return -1;
   const int want_states = (states_out != NULL && chunk_len > 0);
@@ -121,7 +126,8 @@ int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B
     const int64_t b = bd / dim, d = bd % dim;
     double* h = (double*)malloc((size_t)dstate * sizeof(double));
     if (!h) { failed = 1; continue; }
-    for (int64_t n = 0; n < dstate; ++n) h[n] = 0.0; /* [P1 s4.1] h_0 = 0 */
+    for (int64_t n = 0; n < dstate; ++n) /* [P1 s4.1] h_0 = 0 unless given */
+      h[n] = h0 ? (double)h0[(b * dim + d) * dstate + n] : 0.0;
 
     int64_t Lv = seqlen; /* [P1 s2.3] steps from valid_len on are the identity */
     if (valid_len) {
@@ -178,9 +184,20 @@ int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B
         for (int64_t n = 0; n < dstate; ++n) s[n] = h[n];
       }
     }
+    if (final_out)
+      for (int64_t n = 0; n < dstate; ++n) final_out[(b * dim + d) * dstate + n] = h[n];
     free(h);
   }
   return failed ? -1 : 0;
+}
+
+/* The forward from a zero initial state (the call without h0). */
+int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const int32_t* valid_len, double* y_out,
+                 double* states_out, int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                 int64_t chunk_len, int dtype, int nthreads) {
+  return ref_scan_fwd_h0(x, delta, A, B, C, D, z, valid_len, NULL, y_out, states_out, NULL, batch,
+                         seqlen, dim, dstate, chunk_len, dtype, nthreads);
 }
 
 /* Version tag so a loader can tell which oracle build (plain or planted) it has. */

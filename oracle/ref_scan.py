@@ -48,6 +48,9 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ref_scan_fwd.restype = I32
     lib.ref_scan_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I32, I32]
+    lib.ref_scan_fwd_h0.restype = I32
+    lib.ref_scan_fwd_h0.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                    I32, I32]
     D = ctypes.c_double
     lib.ref_combine.restype = None
     lib.ref_combine.argtypes = [D, D, D, D, ctypes.POINTER(D), ctypes.POINTER(D)]
@@ -80,10 +83,12 @@ def linear_recurrence(a, b, h0: float = 0.0, plant: int = 0) -> np.ndarray:
 
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int = 0,
-             threads: int = 0, plant: int = 0):
+             threads: int = 0, plant: int = 0, h0=None, want_final: bool = False):
     """Run the oracle.  Returns ``(y, states)``: y is float64 [batch, L, dim];
     states is float64 [batch, ceil(L/chunk_len), dim, dstate], or None when
-    ``chunk_len`` is 0."""
+    ``chunk_len`` is 0.  With ``h0`` (float32 [batch, dim, dstate]) the state
+    starts there instead of at 0; with ``want_final`` the result is
+    ``(y, states, final)`` with the state after the last step."""
     if x.dtype == np.float32:
         dtype = 0
     elif x.dtype == np.uint16:
@@ -104,17 +109,21 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int =
         raise ValueError("z must match x")
     if valid_len is not None and (valid_len.shape != (batch,) or valid_len.dtype != np.int32):
         raise ValueError("valid_len must be int32 [batch]")
+    if h0 is not None and (h0.shape != (batch, dim, dstate) or h0.dtype != np.float32):
+        raise ValueError("h0 must be float32 [batch, dim, dstate]")
     arrs = [np.ascontiguousarray(t) if t is not None else None
-            for t in (x, delta, A, B, C, D, z, valid_len)]
+            for t in (x, delta, A, B, C, D, z, valid_len, h0)]
     y = np.empty((batch, L, dim), dtype=np.float64)
     states = None
     if chunk_len > 0:
         states = np.empty((batch, (L + chunk_len - 1) // chunk_len, dim, dstate), dtype=np.float64)
-    rc = _load(plant).ref_scan_fwd(*[_ptr(t) for t in arrs], _ptr(y), _ptr(states),
-                                   batch, L, dim, dstate, int(chunk_len), dtype, int(threads))
+    final = np.empty((batch, dim, dstate), dtype=np.float64) if want_final else None
+    rc = _load(plant).ref_scan_fwd_h0(*[_ptr(t) for t in arrs], _ptr(y), _ptr(states),
+                                      _ptr(final), batch, L, dim, dstate, int(chunk_len), dtype,
+                                      int(threads))
     if rc != 0:
         raise RuntimeError("ref_scan_fwd failed")
-    return y, states
+    return (y, states, final) if want_final else (y, states)
 
 
 def plant_id(plant: int = 0) -> int:

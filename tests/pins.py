@@ -321,8 +321,41 @@ def pin_long_sequence_sane(plant=0):
     assert np.max(np.abs(h)) <= np.max(np.abs(b)) / (1 - 0.99) + 1e-9
 
 
+def pin_initial_state_split(plant=0):
+    """[P1] s3.1, s3.4, [P2] s2.4: running [0, L) equals running [0, k) and then
+    [k, L) from the state after step k-1 (the carry between chunks), for the
+    outputs, the final state and the chunk states; and with h0 given on a
+    length-1 run, h = a h0 + b by hand."""
+    rng = np.random.default_rng(23)
+    batch, L, dim, N, k = 2, 30, 3, 4, 12
+    x, delta, A, B, C, D, z = _rand_inputs(rng, batch, L, dim, N, gate=True)
+    vl = np.array([30, 17], np.int32)
+    y, st, fin = R.scan_fwd(x, delta, A, B, C, D, z, vl, chunk_len=6, want_final=True,
+                            plant=plant)
+    y1, st1, f1 = R.scan_fwd(x[:, :k].copy(), delta[:, :k].copy(), A, B[:, :k].copy(),
+                             C[:, :k].copy(), D, z[:, :k].copy(), np.minimum(vl, k),
+                             chunk_len=6, want_final=True, plant=plant)
+    y2, st2, f2 = R.scan_fwd(x[:, k:].copy(), delta[:, k:].copy(), A, B[:, k:].copy(),
+                             C[:, k:].copy(), D, z[:, k:].copy(),
+                             np.clip(vl - k, 0, L - k).astype(np.int32), chunk_len=6,
+                             want_final=True, h0=f1.astype(np.float32), plant=plant)
+    # the carried state is rounded to fp32 once: compare with a tolerance
+    np.testing.assert_allclose(y[:, :k], y1, rtol=0, atol=0)
+    np.testing.assert_allclose(y[:, k:], y2, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(fin, f2, rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(st[:, :2], st1, rtol=0, atol=0)
+    np.testing.assert_allclose(st[:, 2:], st2, rtol=1e-6, atol=1e-7)
+    one = np.ones((1, 1, 1), np.float32)
+    h0 = np.array([[[0.75]]], np.float32)
+    A1 = np.array([[-0.5]], np.float32)
+    ys, _, fs = R.scan_fwd(one * 2, one * 0.5, A1, one * 3, one, None, None, None,
+                           want_final=True, h0=h0, plant=plant)
+    want = np.exp(0.5 * -0.5) * 0.75 + 0.5 * 3 * 2
+    assert abs(fs[0, 0, 0] - want) < 1e-12 and abs(ys[0, 0, 0] - want) < 1e-12
+
+
 ALL_PINS = [pin_closed_form_recurrence, pin_closed_form_forward, pin_combine_is_composition,
             pin_associativity_bruteforce, pin_recurrence_is_prefix_of_combines,
             pin_reverse_identity, pin_lti_convolution, pin_unrolled_sum_bruteforce,
             pin_d_residual, pin_gate, pin_masking, pin_chunk_states_and_carry,
-            pin_bf16_widening, pin_long_sequence_sane]
+            pin_bf16_widening, pin_long_sequence_sane, pin_initial_state_split]
