@@ -129,6 +129,21 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
                            const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                            const ssm_options* opts);
 
+/* As ssm_scan_fwd_ex, continuing from a given state and returning the final one.
+ *   h0              : device fp32 [batch, dim, dstate], the state before the first
+ *                     step (NULL = zeros, [P1] s4.1).
+ *   out_final_state : device fp32 [batch, dim, dstate], receives the state after
+ *                     the last step (frozen past valid_len), or NULL.
+ * Running steps [0, k) and then [k, L) from the first call's final state gives
+ * the same y and states as one call over [0, L): the serial carry between
+ * chunks of the sequence ([P1] s3.1 third level, [P2] s2.4). */
+ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const int32_t* valid_len, const float* h0, void* out_y,
+                              float* out_chunk_states, float* out_final_state,
+                              const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
+                              const ssm_options* opts);
+
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional
  * tensors the call passes.  Writes the tier to *kernel and the launch grid
@@ -145,9 +160,18 @@ ssm_status ssm_scan_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z, i
  * The call copies the inputs into `workspace` (device memory owned by the
  * caller, at least ssm_scan_host_workspace_bytes() bytes, 256-byte aligned),
  * runs the forward there, and copies y (and the chunk states when requested)
- * back to out_y / out_chunk_states, all in order on `stream`.  It returns once
- * the work is enqueued; the host buffers must stay valid until the stream
- * reaches that point.  One cudaMemcpyAsync per tensor and direction.
+ * back to out_y / out_chunk_states.  It returns once the work is enqueued;
+ * the host buffers must stay valid, and the workspace unused by other work,
+ * until `stream` reaches that point (synchronise `stream` before reading the
+ * outputs).
+ *
+ * The work is pipelined over pieces of the sequence: the inputs of piece i+1
+ * are copied in while piece i runs and piece i-1's outputs are copied out, on
+ * two library-owned copy streams per device chained to `stream` by events;
+ * each piece starts from the state the previous one ended in ([P1] s3.1 third
+ * level, [P2] s2.4), so the result equals ssm_scan_fwd's on the same inputs.
+ * Calls on the same device enqueue one at a time (a lock); the calling
+ * thread's current device is used.
  */
 ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, const void* B,
                              const void* C, const float* D, const void* z,

@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P]
     lib.ssm_scan_fwd_ex.restype = I32
     lib.ssm_scan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
+    lib.ssm_scan_fwd_carry.restype = I32
+    lib.ssm_scan_fwd_carry.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
     lib.ssm_scan_plan.restype = I32
     lib.ssm_scan_plan.argtypes = [SP, I32, I32, I32, I32, OP, ctypes.POINTER(I32),
                                   ctypes.POINTER(I64)]
@@ -181,13 +183,16 @@ def _check(t, name, shape, dtype, device):
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
              out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO,
              warps_per_block: int = 0, states_per_lane: int = 0, time_split: int = 0,
-             stream=None):
+             stream=None, h0=None, want_final: bool = False, out_final=None):
     """The fused selective-scan forward on CUDA tensors.
 
     x, delta, z: [batch, L, dim]; B, C: [batch, L, dstate] (fp32 or bf16, all the
     same dtype); A: fp32 [dim, dstate]; D: fp32 [dim]; valid_len: int32 [batch].
     Returns ``(y, states)`` with y like x and states fp32
     [batch, ceil(L/chunk_len), dim, dstate] (None when chunk_len == 0).
+    ``h0`` (fp32 [batch, dim, dstate]) is the state before the first step
+    (zeros when None); with ``want_final`` the result is ``(y, states, final)``,
+    final being the fp32 state after the last step.
     Runs on ``stream`` (default: the current PyTorch stream of x's device).
     """
     import torch
@@ -217,6 +222,13 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
         states = (torch.empty((batch, nch, dim, dstate), dtype=torch.float32, device=dev)
                   if out_states is None else out_states)
         _check(states, "out_states", (batch, nch, dim, dstate), torch.float32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, dstate), torch.float32, dev)
+    final = None
+    if want_final or out_final is not None:
+        final = (torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+                 if out_final is None else out_final)
+        _check(final, "out_final", (batch, dim, dstate), torch.float32, dev)
     s = _shapes(batch, L, dim, dstate, chunk_len)
     o = Options(int(_kernel(kernel)), int(warps_per_block), int(states_per_lane),
                 int(time_split))
@@ -224,12 +236,21 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     with torch.cuda.device(dev):
-        st = lib.ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                 _ptr(z), _ptr(valid_len), _ptr(y), _ptr(states),
-                                 ctypes.byref(s), int(code), ctypes.c_void_p(handle),
-                                 ctypes.byref(o))
+        if h0 is None and final is None:
+            st = lib.ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(z), _ptr(valid_len), _ptr(y), _ptr(states),
+                                     ctypes.byref(s), int(code), ctypes.c_void_p(handle),
+                                     ctypes.byref(o))
+        else:
+            st = lib.ssm_scan_fwd_carry(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                        _ptr(D), _ptr(z), _ptr(valid_len), _ptr(h0), _ptr(y),
+                                        _ptr(states), _ptr(final), ctypes.byref(s), int(code),
+                                        ctypes.c_void_p(handle), ctypes.byref(o))
     if st != 0:
-        raise SsmError(st, "ssm_scan_fwd")
+        raise SsmError(st, "ssm_scan_fwd_carry" if final is not None or h0 is not None
+                       else "ssm_scan_fwd")
+    if want_final or out_final is not None:
+        return y, states, final
     return y, states
 
 

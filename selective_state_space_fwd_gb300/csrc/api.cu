@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <new>
 
 #include "ssmscan.h"
@@ -103,24 +104,43 @@ ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o,
 
 ScanParams make_params(const void* x, const void* delta, const float* A, const void* B,
                        const void* C, const float* D, const void* z, const int32_t* valid_len,
-                       void* y, float* states, const ssm_shapes* s) {
+                       void* y, float* states, const ssm_shapes* s, const float* h0 = nullptr,
+                       float* h_final = nullptr) {
   ScanParams p;
   p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
-  p.valid_len = valid_len; p.y = y;
+  p.valid_len = valid_len; p.y = y; p.h0 = h0; p.h_final = h_final;
   p.batch = s->batch; p.seqlen = s->seqlen; p.dim = s->dim;
   p.dstate = static_cast<int>(s->dstate);
   const bool st = states != nullptr && s->chunk_len > 0;
   p.states = st ? states : nullptr;
   p.chunk_len = st ? s->chunk_len : 1;
   p.n_chunks = st ? (s->seqlen + s->chunk_len - 1) / s->chunk_len : 0;
+  p.len_offset = 0;
   return p;
+}
+
+// Launch the planned tier.
+ssm_status launch(const ScanParams& p, ssm_dtype dtype, const ssm_options* opts,
+                  cudaStream_t stream) {
+  Plan plan;
+  ssm_status st = make_plan(p, dtype, opts, &plan);
+  if (st != SSM_OK) return st;
+  const bool bf16 = dtype == SSM_BF16;
+  cudaError_t err = cudaErrorInvalidValue;
+  switch (plan.kernel) {
+    case SSM_KERNEL_SERIAL: err = ssm::launch_serial(p, bf16, stream); break;
+    case SSM_KERNEL_STREAM: err = ssm::launch_stream(p, bf16, stream, plan.shape); break;
+    case SSM_KERNEL_WARPSCAN: err = ssm::launch_warpscan(p, bf16, stream); break;
+    default: return SSM_ERR_UNSUPPORTED;
+  }
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte layout of the device workspace used by ssm_scan_fwd_host.
 struct HostLayout {
-  size_t x, delta, z, B, C, A, D, valid, y, states, total;
+  size_t x, delta, z, B, C, A, D, valid, y, states, carry, total;
 };
 
 HostLayout host_layout(const ssm_shapes* s, ssm_dtype dtype, int has_D, int has_z, int has_valid,
@@ -142,8 +162,157 @@ HostLayout host_layout(const ssm_shapes* s, ssm_dtype dtype, int has_D, int has_
   l.valid = has_valid ? take(size_t(s->batch) * 4) : 0;
   l.y = take(act);
   l.states = has_states ? take(size_t(s->batch) * nch * s->dim * s->dstate * 4) : 0;
+  l.carry = take(2 * size_t(s->batch) * s->dim * s->dstate * 4);
   l.total = off;
   return l;
+}
+
+// ---- the end-to-end form: copies and kernels pipelined over time pieces ----------
+//
+// The sequence is cut into pieces of `piece` steps.  Piece i's inputs are
+// copied host -> device on a copy stream, its kernel runs on the caller's
+// stream starting from the state piece i-1 ended in (the serial carry between
+// sequence chunks, [P1] s3.1 third level, [P2] s2.4), and its outputs are
+// copied device -> host on a second copy stream, so that the two copy
+// directions and the kernels of neighbouring pieces overlap.  In the workspace
+// every tensor is stored piece-major (piece i holds [batch, piece, ...]
+// contiguous), so each kernel sees an ordinary compact problem and each copy is
+// one strided 2-D copy.
+
+#ifndef SSM_HOST_PIECES
+#define SSM_HOST_PIECES 16  // pieces per call when the sequence is long enough
+#endif
+
+// Library-owned copy streams and the events that chain them, one set per device.
+struct HostStreams {
+  std::mutex mu;        // one call enqueues on a device's set at a time
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, in = nullptr, kern = nullptr, done = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+HostStreams g_host_streams[kMaxDevices];
+std::mutex g_host_streams_mu;
+
+HostStreams* host_streams(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostStreams* h = &g_host_streams[dev];
+  std::lock_guard<std::mutex> lk(g_host_streams_mu);
+  if (!h->ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->start, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->in, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->kern, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->done, ef) != cudaSuccess)
+      return nullptr;
+    h->ready = true;
+  }
+  return h;
+}
+
+// Steps per piece: about SSM_HOST_PIECES pieces, a multiple of 64 steps (the
+// STREAM tile), a multiple of chunk_len when chunk states are wanted (so that
+// every chunk lies inside one piece), and at least 1 MiB of input per piece.
+int64_t host_piece_steps(const ssm_shapes& s, ssm_dtype dtype, bool has_z, bool want_states) {
+  const int64_t L = s.seqlen;
+  const int64_t es = static_cast<int64_t>(elem_size(dtype));
+  const int64_t step_bytes = s.batch * es * ((has_z ? 3 : 2) * s.dim + 2 * s.dstate);
+  int64_t piece = (L + SSM_HOST_PIECES - 1) / SSM_HOST_PIECES;
+  const int64_t min_steps = ((int64_t(1) << 20) + step_bytes - 1) / step_bytes;
+  if (piece < min_steps) piece = min_steps;
+  piece = (piece + 63) / 64 * 64;
+  if (want_states) piece = (piece + s.chunk_len - 1) / s.chunk_len * s.chunk_len;
+  return piece < L ? piece : L;
+}
+
+ssm_status run_host_pipeline(const void* x, const void* delta, const float* A, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const int32_t* valid_len, void* out_y, float* out_states,
+                             const ssm_shapes& s, ssm_dtype dtype, char* ws, const HostLayout& l,
+                             cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  HostStreams* hs = host_streams(dev);
+  if (hs == nullptr) return SSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(hs->mu);
+
+  const bool want_states = out_states != nullptr;
+  const size_t es = elem_size(dtype);
+  const int64_t L = s.seqlen, Bt = s.batch, N = s.dstate;
+  const size_t dn4 = size_t(s.dim) * N * 4;
+  const int64_t nch = want_states ? (L + s.chunk_len - 1) / s.chunk_len : 0;
+  const int64_t piece = host_piece_steps(s, dtype, z != nullptr, want_states);
+  float* carry[2] = {reinterpret_cast<float*>(ws + l.carry),
+                     reinterpret_cast<float*>(ws + l.carry + size_t(Bt) * dn4)};
+
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t r) { if (e == cudaSuccess) e = r; return e == cudaSuccess; };
+  // [batch, L, w] host tensor, steps [t0, t0 + n) -> piece-major workspace region
+  auto copy_in = [&](size_t region, const void* src, int64_t w, int64_t t0, int64_t n) {
+    const size_t row = size_t(w) * es;
+    return ok(cudaMemcpy2DAsync(ws + region + size_t(Bt) * t0 * row, n * row,
+                                static_cast<const char*>(src) + t0 * row, L * row, n * row, Bt,
+                                cudaMemcpyHostToDevice, hs->h2d));
+  };
+
+  // the caller's earlier work on `stream` (e.g. on this workspace) comes first
+  ok(cudaEventRecord(hs->start, stream));
+  ok(cudaStreamWaitEvent(hs->h2d, hs->start, 0));
+  ok(cudaStreamWaitEvent(hs->d2h, hs->start, 0));
+  ok(cudaMemcpyAsync(ws + l.A, A, dn4, cudaMemcpyHostToDevice, hs->h2d));
+  if (D) ok(cudaMemcpyAsync(ws + l.D, D, size_t(s.dim) * 4, cudaMemcpyHostToDevice, hs->h2d));
+  if (valid_len)
+    ok(cudaMemcpyAsync(ws + l.valid, valid_len, size_t(Bt) * 4, cudaMemcpyHostToDevice, hs->h2d));
+
+  ssm_status st = SSM_OK;
+  int i = 0;
+  for (int64_t t0 = 0; t0 < L && e == cudaSuccess && st == SSM_OK; t0 += piece, ++i) {
+    const int64_t n = L - t0 < piece ? L - t0 : piece;
+    const size_t act_off = size_t(Bt) * t0 * s.dim * es, bc_off = size_t(Bt) * t0 * N * es;
+    copy_in(l.x, x, s.dim, t0, n);
+    copy_in(l.delta, delta, s.dim, t0, n);
+    if (z) copy_in(l.z, z, s.dim, t0, n);
+    copy_in(l.B, B, N, t0, n);
+    copy_in(l.C, C, N, t0, n);
+    ok(cudaEventRecord(hs->in, hs->h2d));
+    ok(cudaStreamWaitEvent(stream, hs->in, 0));
+    if (e != cudaSuccess) break;
+
+    const int64_t c0 = want_states ? t0 / s.chunk_len : 0;
+    const int64_t pch = want_states ? (n + s.chunk_len - 1) / s.chunk_len : 0;
+    float* pstates = want_states ? reinterpret_cast<float*>(ws + l.states) + size_t(Bt) * c0 *
+                                       (dn4 / 4)
+                                 : nullptr;
+    const ssm_shapes ps = {Bt, n, s.dim, N, want_states ? s.chunk_len : 0};
+    ScanParams p = make_params(ws + l.x + act_off, ws + l.delta + act_off,
+                               reinterpret_cast<const float*>(ws + l.A), ws + l.B + bc_off,
+                               ws + l.C + bc_off,
+                               D ? reinterpret_cast<const float*>(ws + l.D) : nullptr,
+                               z ? ws + l.z + act_off : nullptr,
+                               valid_len ? reinterpret_cast<const int32_t*>(ws + l.valid) : nullptr,
+                               ws + l.y + act_off, pstates, &ps,
+                               t0 == 0 ? nullptr : carry[i % 2],
+                               t0 + n < L ? carry[(i + 1) % 2] : nullptr);
+    p.len_offset = t0;
+    st = launch(p, dtype, nullptr, stream);
+    if (st != SSM_OK) break;
+    ok(cudaEventRecord(hs->kern, stream));
+    ok(cudaStreamWaitEvent(hs->d2h, hs->kern, 0));
+    const size_t row = size_t(s.dim) * es;
+    ok(cudaMemcpy2DAsync(static_cast<char*>(out_y) + t0 * row, L * row, ws + l.y + act_off,
+                         n * row, n * row, Bt, cudaMemcpyDeviceToHost, hs->d2h));
+    if (want_states)
+      ok(cudaMemcpy2DAsync(out_states + size_t(c0) * (dn4 / 4), nch * dn4, pstates, pch * dn4,
+                           pch * dn4, Bt, cudaMemcpyDeviceToHost, hs->d2h));
+  }
+  // join: the caller's stream reaches the end only after the last copy out
+  cudaError_t je = cudaEventRecord(hs->done, hs->d2h);
+  if (je == cudaSuccess) je = cudaStreamWaitEvent(stream, hs->done, 0);
+  if (st != SSM_OK) return st;
+  return (e == cudaSuccess && je == cudaSuccess) ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // namespace
@@ -212,6 +381,16 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
                            const int32_t* valid_len, void* out_y, float* out_chunk_states,
                            const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                            const ssm_options* opts) {
+  return ssm_scan_fwd_carry(x, delta, A, B, C, D, z, valid_len, nullptr, out_y, out_chunk_states,
+                            nullptr, shapes, dtype, stream, opts);
+}
+
+ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const int32_t* valid_len, const float* h0, void* out_y,
+                              float* out_chunk_states, float* out_final_state,
+                              const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
+                              const ssm_options* opts) {
   ssm_status st = check_shapes(shapes, dtype, out_chunk_states != nullptr);
   if (st != SSM_OK) return st;
   if ((st = check_options(opts)) != SSM_OK) return st;
@@ -219,22 +398,13 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
   const size_t es = elem_size(dtype);
   if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
       !aligned(out_y, es) || (z && !aligned(z, es)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
-      (valid_len && !aligned(valid_len, 4)) || (out_chunk_states && !aligned(out_chunk_states, 4)))
+      (valid_len && !aligned(valid_len, 4)) || (out_chunk_states && !aligned(out_chunk_states, 4)) ||
+      (h0 && !aligned(h0, 4)) || (out_final_state && !aligned(out_final_state, 4)))
     return SSM_ERR_ALIGN;
 
   const ScanParams p = make_params(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states,
-                                   shapes);
-  Plan plan;
-  if ((st = make_plan(p, dtype, opts, &plan)) != SSM_OK) return st;
-  const bool bf16 = dtype == SSM_BF16;
-  cudaError_t err = cudaErrorInvalidValue;
-  switch (plan.kernel) {
-    case SSM_KERNEL_SERIAL: err = ssm::launch_serial(p, bf16, stream); break;
-    case SSM_KERNEL_STREAM: err = ssm::launch_stream(p, bf16, stream, plan.shape); break;
-    case SSM_KERNEL_WARPSCAN: err = ssm::launch_warpscan(p, bf16, stream); break;
-    default: return SSM_ERR_UNSUPPORTED;
-  }
-  return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+                                   shapes, h0, out_final_state);
+  return launch(p, dtype, opts, stream);
 }
 
 ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A, const void* B,
@@ -264,39 +434,8 @@ ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, c
   const HostLayout l = host_layout(shapes, dtype, D != nullptr, z != nullptr,
                                    valid_len != nullptr, want_states);
   if (workspace_bytes < l.total) return SSM_ERR_SHAPE;
-  char* ws = static_cast<char*>(workspace);
-  const size_t es = elem_size(dtype);
-  const size_t act = size_t(shapes->batch) * shapes->seqlen * shapes->dim * es;
-  const size_t bc = size_t(shapes->batch) * shapes->seqlen * shapes->dstate * es;
-  const size_t nch = size_t(ssm_chunk_count(shapes));
-  const size_t states_bytes = size_t(shapes->batch) * nch * shapes->dim * shapes->dstate * 4;
-
-  auto h2d = [&](size_t off, const void* src, size_t bytes) {
-    return cudaMemcpyAsync(ws + off, src, bytes, cudaMemcpyHostToDevice, stream);
-  };
-  cudaError_t e = cudaSuccess;
-  if (e == cudaSuccess) e = h2d(l.x, x, act);
-  if (e == cudaSuccess) e = h2d(l.delta, delta, act);
-  if (e == cudaSuccess && z) e = h2d(l.z, z, act);
-  if (e == cudaSuccess) e = h2d(l.B, B, bc);
-  if (e == cudaSuccess) e = h2d(l.C, C, bc);
-  if (e == cudaSuccess) e = h2d(l.A, A, size_t(shapes->dim) * shapes->dstate * 4);
-  if (e == cudaSuccess && D) e = h2d(l.D, D, size_t(shapes->dim) * 4);
-  if (e == cudaSuccess && valid_len) e = h2d(l.valid, valid_len, size_t(shapes->batch) * 4);
-  if (e != cudaSuccess) return SSM_ERR_CUDA;
-
-  st = ssm_scan_fwd(ws + l.x, ws + l.delta, reinterpret_cast<const float*>(ws + l.A), ws + l.B,
-                    ws + l.C, D ? reinterpret_cast<const float*>(ws + l.D) : nullptr,
-                    z ? ws + l.z : nullptr,
-                    valid_len ? reinterpret_cast<const int32_t*>(ws + l.valid) : nullptr,
-                    ws + l.y, want_states ? reinterpret_cast<float*>(ws + l.states) : nullptr,
-                    shapes, dtype, stream);
-  if (st != SSM_OK) return st;
-  e = cudaMemcpyAsync(out_y, ws + l.y, act, cudaMemcpyDeviceToHost, stream);
-  if (e == cudaSuccess && want_states && states_bytes > 0)
-    e = cudaMemcpyAsync(out_chunk_states, ws + l.states, states_bytes, cudaMemcpyDeviceToHost,
-                        stream);
-  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return run_host_pipeline(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states, *shapes,
+                           dtype, static_cast<char*>(workspace), l, stream);
 }
 
 }  // extern "C"

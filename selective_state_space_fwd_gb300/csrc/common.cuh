@@ -26,12 +26,15 @@ struct ScanParams {
   const float* D;             // nullable
   const void* z;              // nullable
   const int32_t* valid_len;   // nullable
+  const float* h0;            // nullable: state before the first step, [B, D, N] fp32
   void* y;
   float* states;              // nullable
+  float* h_final;             // nullable: state after the last step, [B, D, N] fp32
   int64_t batch, seqlen, dim;
   int dstate;
   int64_t chunk_len;          // > 0 when states != nullptr
   int64_t n_chunks;
+  int64_t len_offset;         // this call's first step within the caller's sequence
 };
 
 // 2^v with the MUFU unit (PTX ex2.approx.ftz.f32: results below 2^-126 flush
@@ -67,10 +70,12 @@ template <> struct IO<__nv_bfloat16> {
 };
 
 // Clamped number of valid steps of batch row b ([P1] s2.3, s5.3: steps past
-// the valid length act as the identity (1, 0)).
+// the valid length act as the identity (1, 0)).  valid_len counts from the
+// start of the whole sequence; a call that covers steps [len_offset,
+// len_offset + seqlen) of it sees valid_len - len_offset of them.
 __device__ __forceinline__ int64_t valid_steps(const ScanParams& p, int64_t b) {
   if (p.valid_len == nullptr) return p.seqlen;
-  int64_t v = p.valid_len[b];
+  int64_t v = p.valid_len[b] - p.len_offset;
   return v < 0 ? 0 : (v > p.seqlen ? p.seqlen : v);
 }
 

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) serial_kernel(const ScanParams p) {
 #pragma unroll
   for (int n = 0; n < N; ++n) {
     a_l2[n] = __ldg(p.A + d * N + n) * kLog2e;
-    h[n] = 0.0f;  // [P1] s4.1: h_0 = 0
+    h[n] = p.h0 ? __ldg(p.h0 + bd * N + n) : 0.0f;  // [P1] s4.1: h_0 = 0 unless given
   }
   const float dskip = p.D ? __ldg(p.D + d) : 0.0f;
   const int64_t lv = valid_steps(p, b);
@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(128) serial_kernel(const ScanParams p) {
 #pragma unroll
       for (int n = 0; n < N; ++n) s[n] = h[n];
     }
+  }
+  if (p.h_final) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) p.h_final[bd * N + n] = h[n];
   }
 }
 

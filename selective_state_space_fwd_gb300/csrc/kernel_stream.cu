@@ -398,7 +398,9 @@ __global__ void __launch_bounds__(K::WPC * 32)
       hi = __ldg(p.A + d * K::N + g * K::G + 2 * q + 1) * kLog2e;
     }
     a2[q] = pk2(lo, hi);
-    h2[q] = pk2(0.f, 0.f);  // [P1] s4.1: h_0 = 0
+    h2[q] = pk2(0.f, 0.f);  // [P1] s4.1: h_0 = 0 unless given
+    if (d_ok && p.h0)
+      h2[q] = *reinterpret_cast<const u64*>(p.h0 + (b * p.dim + d) * K::N + g * K::G + 2 * q);
   }
   const float dskip = (d_ok && p.D) ? __ldg(p.D + d) : 0.f;
   const float dg = g == 0 ? dskip : 0.f;  // the channel's lane 0 adds D x to its partial
@@ -620,6 +622,11 @@ __global__ void __launch_bounds__(K::WPC * 32)
   }
   if (want_states)
     for (; next_c < p.n_chunks; ++next_c) store_state(chunk_end(next_c));  // frozen state
+  if (p.h_final && d_ok && hf == 0) {  // state after the last step
+    float* fp = p.h_final + (b * p.dim + d) * K::N + g * K::G;
+#pragma unroll
+    for (int q = 0; q < K::P; ++q) reinterpret_cast<float2*>(fp)[q] = upk2(h2[q]);
+  }
 }
 
 // ---- host side --------------------------------------------------------------------
@@ -753,6 +760,8 @@ bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh) {
                         reinterpret_cast<uintptr_t>(p.B) | reinterpret_cast<uintptr_t>(p.C) |
                         reinterpret_cast<uintptr_t>(p.z);
   if (mis % 16 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(p.h0) | reinterpret_cast<uintptr_t>(p.h_final)) % 8 != 0)
+    return false;
   if (encode_fn() == nullptr) return false;
   const int64_t grid = (p.dim + cpc - 1) / cpc * p.batch;
   return grid <= INT32_MAX;

@@ -156,7 +156,10 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
   const bool want_states = p.states != nullptr;
   const int row0 = lane * K;
 
-  for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) carry[i] = 0.f;  // h_0 = 0
+  for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) {  // h_0 = 0 unless given
+    const int64_t dc = d0 + i / N;
+    carry[i] = (p.h0 && dc < p.dim) ? __ldg(p.h0 + (b * p.dim + dc) * N + i % N) : 0.f;
+  }
 
   for (int64_t t0 = 0; t0 < L; t0 += W) {
     const int nw = static_cast<int>(L - t0 < W ? L - t0 : W);  // steps of this window
@@ -367,6 +370,13 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
           ce = ce + p.chunk_len > L - 1 ? L - 1 : ce + p.chunk_len;
         }
       }
+    }
+  }
+  if (p.h_final) {  // state after the last step
+    __syncthreads();
+    for (int i = threadIdx.x; i < kWarps * N; i += blockDim.x) {
+      const int64_t dc = d0 + i / N;
+      if (dc < p.dim) p.h_final[(b * p.dim + dc) * N + i % N] = carry[i];
     }
   }
 }

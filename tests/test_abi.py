@@ -7,7 +7,7 @@ import pytest
 
 from selective_state_space_fwd_gb300 import _binding as Bd
 
-EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_plan", "ssm_scan_fwd_host",
+EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_plan", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
@@ -84,6 +84,25 @@ def test_argument_errors_return_status(ssmlib, kw, status):
     assert _call(**kw) == status
 
 
+def _carry(h0=None, final=None, **kw):
+    lib = Bd.load()
+    s = Bd.Shapes(2, 8, 4, 16, 0)
+    o = Bd.Options(0, 0, 0, 0)
+    P = ctypes.c_void_p
+    return lib.ssm_scan_fwd_carry(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, None, None,
+                                  P(h0), P(FAKE), None, P(final), ctypes.byref(s), 0, None,
+                                  ctypes.byref(o))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(h0=FAKE + 2), Bd.Status.ERR_ALIGN),
+    (dict(final=FAKE + 1), Bd.Status.ERR_ALIGN),
+    (dict(h0=FAKE + 6, final=FAKE), Bd.Status.ERR_ALIGN),
+])
+def test_carry_argument_errors_return_status(ssmlib, kw, status):
+    assert _carry(**kw) == status
+
+
 def test_plan_serial_always_available(ssmlib):
     for n in (1, 2, 4, 8, 16, 32, 64):
         k, g = Bd.plan(3, 100, 70, n, kernel="serial")
@@ -99,7 +118,8 @@ def test_plan_auto_picks_a_tier(ssmlib):
 def test_host_workspace_bytes(ssmlib):
     b = Bd.host_workspace_bytes(2, 8, 4, 16, dtype="f32", has_D=True, gate=True, mask=True,
                                 chunk_len=4)
+    # x, delta, z; B, C; A; D; valid_len; y; chunk states; two carried states
     need = 3 * 2 * 8 * 4 * 4 + 2 * 2 * 8 * 16 * 4 + 4 * 16 * 4 + 4 * 4 + 2 * 4 + 2 * 8 * 4 * 4 \
-        + 2 * 2 * 4 * 16 * 4
-    assert need <= b <= need + 11 * 256
+        + 2 * 2 * 4 * 16 * 4 + 2 * 2 * 4 * 16 * 4
+    assert need <= b <= need + 12 * 256
     assert Bd.host_workspace_bytes(0, 8, 4, 16) == 0

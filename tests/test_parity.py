@@ -209,6 +209,30 @@ def test_host_entry_point_matches_device(oracle):
     assert np.array_equal(to_f64(s_h), s_d)
 
 
+@pytest.mark.parametrize("case", [
+    dict(batch=1, L=8192, dim=64, N=16, gate=True, mask=[5000], chunk=256),
+    dict(batch=3, L=6000, dim=40, N=8, dtype="bf16", mask=[6000, 0, 2345], chunk=100),
+    dict(batch=2, L=7777, dim=32, N=64),
+])
+def test_host_entry_pipelined_pieces(oracle, case):
+    """Long sequences go through several pipelined pieces chained by the
+    carried state: the result is the device entry point's, bit for bit, and
+    within tolerance of the oracle."""
+    inp = _edge(**case)
+    t = W.to_torch(inp, "cpu")
+    pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    y_h, s_h = S.scan_fwd_host(pinned["x"], pinned["delta"], pinned["A"], pinned["B"],
+                               pinned["C"], pinned["D"], pinned["z"], pinned["valid_len"],
+                               chunk_len=inp["chunk_len"])
+    torch.cuda.synchronize()
+    y_d, s_d = run_gpu(inp)
+    assert np.array_equal(to_f64(y_h), y_d)
+    if s_d is not None:
+        assert np.array_equal(to_f64(s_h), s_d)
+    y_ref, s_ref = run_oracle(oracle, inp)
+    check(inp, to_f64(y_h), None if s_h is None else to_f64(s_h), y_ref, s_ref)
+
+
 def test_stream_argument_is_respected():
     inp = W.make_inputs(SMALL["w2-fp32"])
     t = W.to_torch(inp, "cuda")
