@@ -183,7 +183,7 @@ def parse():
     ap.add_argument("--kernel", default="auto")
     ap.add_argument("--warps-per-block", type=int, default=0)
     ap.add_argument("--states-per-lane", type=int, default=0)
-    ap.add_argument("--time-split", type=int, default=0)
+    ap.add_argument("--channels-per-lane", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -293,7 +293,7 @@ def main():
     kernel, grid = S.plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
                           mask=w.mask is not None, chunk_len=w.chunk_len, kernel=args.kernel,
                           warps_per_block=args.warps_per_block,
-                          states_per_lane=args.states_per_lane, time_split=args.time_split)
+                          states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane)
     stream = torch.cuda.Stream(dev)
     y = torch.empty_like(t["x"])
     nch = (w.seqlen + w.chunk_len - 1) // w.chunk_len if w.chunk_len else 0
@@ -305,7 +305,7 @@ def main():
         S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
                    chunk_len=w.chunk_len, out=y, out_states=states, kernel=args.kernel,
                    warps_per_block=args.warps_per_block,
-                   states_per_lane=args.states_per_lane, time_split=args.time_split,
+                   states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane,
                    stream=stream)
 
     with torch.cuda.stream(stream):
@@ -398,7 +398,7 @@ def main():
                        f"{FP32_PER_SM_CLK} fp32 lanes/clk/SM x {sms} SMs x {sm_mhz_peak:.0f} MHz",
         "kernel": S.kernel_name(kernel), "grid": grid,
         "warps_per_block": args.warps_per_block, "states_per_lane": args.states_per_lane,
-        "time_split": args.time_split,
+        "channels_per_lane": args.channels_per_lane,
         "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
                     "fp32": r["t_fp32"] * 1e6},
         "frac_of_roof": r["t_roof"] / t_meas,

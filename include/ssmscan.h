@@ -84,18 +84,19 @@ typedef enum {
   SSM_KERNEL_WARPSCAN = 2, /* [P1] s3.1 hierarchy: thread-serial run of k steps,
                               5-round shuffle scan across the warp, serial carry
                               between windows; one warp per (b, d) */
-  SSM_KERNEL_STREAM = 3    /* state-split register sweep with TMA-staged tiles and
-                              paired fp32 math; needs batch*dim*dstate to fill the GPU */
+  SSM_KERNEL_STREAM = 3    /* register sweep over channels x states per thread, TMA-staged
+                              tiles, f32x2 math over channel pairs; needs
+                              batch*dim*dstate to fill the GPU */
 } ssm_kernel;
 
 typedef struct {
   ssm_kernel kernel;       /* SSM_KERNEL_AUTO unless forcing a tier (tests, benchmarks) */
-  int32_t warps_per_block; /* 0 = the tier's default; STREAM accepts 1, 2 or 4 */
-  int32_t states_per_lane; /* 0 = the tier's default; STREAM: 2, 4, 8 or 16 states of one
-                              channel per thread (fewer = more threads, more reduction) */
-  int32_t time_split;      /* 0 = the tier's default; STREAM: 1, or 2 = the two half-warps
-                              take consecutive runs of each 16-step sub-tile and join them
-                              with a one-round scan ([P1] s3.1), doubling the threads */
+  int32_t warps_per_block;   /* 0 = the tier's default; STREAM accepts 1, 2 or 4 */
+  int32_t states_per_lane;   /* 0 = the tier's default; STREAM: 4, 8 or 16 consecutive
+                                states of a channel per thread (instances exist for some
+                                (dstate, states, channels) combinations only) */
+  int32_t channels_per_lane; /* 0 = the tier's default; STREAM: 2 or 4 consecutive
+                                channels per thread, paired in f32x2 instructions */
 } ssm_options;
 
 /*

@@ -53,7 +53,7 @@ class Shapes(ctypes.Structure):
 
 class Options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("warps_per_block", ctypes.c_int32),
-                ("states_per_lane", ctypes.c_int32), ("time_split", ctypes.c_int32)]
+                ("states_per_lane", ctypes.c_int32), ("channels_per_lane", ctypes.c_int32)]
 
 
 _lib = None
@@ -135,11 +135,11 @@ def check_device_errors() -> None:
 
 def plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False, mask=False, chunk_len=0,
          kernel: Kernel | str = Kernel.AUTO, warps_per_block: int = 0,
-         states_per_lane: int = 0, time_split: int = 0) -> tuple[Kernel, int]:
+         states_per_lane: int = 0, channels_per_lane: int = 0) -> tuple[Kernel, int]:
     """The tier and grid the library would launch for this call (no GPU needed)."""
     s = _shapes(batch, seqlen, dim, dstate, chunk_len)
     o = Options(int(_kernel(kernel)), int(warps_per_block), int(states_per_lane),
-                int(time_split))
+                int(channels_per_lane))
     k, g = ctypes.c_int32(), ctypes.c_int64()
     st = load().ssm_scan_plan(ctypes.byref(s), int(_dtype_code(dtype)), int(gate), int(mask),
                               int(chunk_len > 0), ctypes.byref(o), ctypes.byref(k),
@@ -182,7 +182,7 @@ def _check(t, name, shape, dtype, device):
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
              out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO,
-             warps_per_block: int = 0, states_per_lane: int = 0, time_split: int = 0,
+             warps_per_block: int = 0, states_per_lane: int = 0, channels_per_lane: int = 0,
              stream=None, h0=None, want_final: bool = False, out_final=None):
     """The fused selective-scan forward on CUDA tensors.
 
@@ -231,7 +231,7 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
         _check(final, "out_final", (batch, dim, dstate), torch.float32, dev)
     s = _shapes(batch, L, dim, dstate, chunk_len)
     o = Options(int(_kernel(kernel)), int(warps_per_block), int(states_per_lane),
-                int(time_split))
+                int(channels_per_lane))
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)

@@ -63,7 +63,8 @@ ssm_status check_options(const ssm_options* o) {
   if (o->states_per_lane != 0 && o->states_per_lane != 2 && o->states_per_lane != 4 &&
       o->states_per_lane != 8 && o->states_per_lane != 16)
     return SSM_ERR_UNSUPPORTED;
-  if (o->time_split != 0 && o->time_split != 1 && o->time_split != 2) return SSM_ERR_UNSUPPORTED;
+  if (o->channels_per_lane != 0 && o->channels_per_lane != 2 && o->channels_per_lane != 4)
+    return SSM_ERR_UNSUPPORTED;
   return SSM_OK;
 }
 
@@ -78,8 +79,8 @@ ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o,
   const bool bf16 = dtype == SSM_BF16;
   const ssm_kernel forced = o ? o->kernel : SSM_KERNEL_AUTO;
   const ssm::StreamShape shape =
-      ssm::stream_shape(p, o ? o->warps_per_block : 0, o ? o->states_per_lane : 0,
-                        o ? o->time_split : 0);
+      ssm::stream_shape(p, bf16, o ? o->warps_per_block : 0, o ? o->states_per_lane : 0,
+                        o ? o->channels_per_lane : 0);
   ssm_kernel k = forced;
   if (k == SSM_KERNEL_AUTO)
     k = ssm::stream_eligible(p, bf16, shape) ? SSM_KERNEL_STREAM : SSM_KERNEL_SERIAL;

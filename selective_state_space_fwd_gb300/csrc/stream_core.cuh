@@ -1,0 +1,728 @@
+// stream_core.cuh -- the STREAM tier's kernel template: a channel-pair register sweep.
+//
+// Work split.  Every (b, d, n) recurrence h_t = Abar_t h_{t-1} + b_t is
+// independent across channels and states ([P1] s1.1 "channel parallelism");
+// when batch * dim * dstate fills the GPU, the cheapest schedule runs each
+// recurrence serially in time in registers and spends no instructions on
+// combining partial scans.  A lane owns R consecutive channels times G
+// consecutive states; NG = N / G lanes share a channel group and a warp covers
+// CW = (32 / NG) * R channels.  Per step and (channel, state) the work is one
+// MUFU ex2 and four fp32 operations (delta*A, delta*x*B, the state update, the
+// C contraction), issued as f32x2 instructions over PAIRS OF CHANNELS: the
+// per-channel operands (delta, delta*x, the state) come straight from the
+// vector loads and the per-state operands (B_n, C_n) are shared by the pair.
+// Holding R channels makes every B/C value a lane loads serve R channels and
+// every delta/x value serve G states, which is what bounds the shared-memory
+// to register traffic per (channel, state).  The C contraction is a sum over
+// the NG lanes of a channel group: a shuffle reduce-scatter once per NG steps
+// leaves each lane with one step's outputs for its R channels, to which the
+// D residual (added once, by the group's state-0 lane) and the silu(z) gate
+// apply ([P1] s3.3: everything between the loads of x, delta, B, C and the
+// store of y is fused; h never leaves registers).
+//
+// Data movement.  A CTA covers W warps (chosen at launch) of CW consecutive
+// channels of one batch row.  Time is cut into tiles of T steps; per tile TMA
+// copies each warp's x, delta (and z) slab [T x CW] and the B, C rows [T x N]
+// into one slot of a ring ([P1] s3.2: time is the slowest dimension, channels
+// and states contiguous, so every copy is a dense box).  mbarriers with
+// bounded waits order the copies and their reuse.  Boxes that run past L or D
+// are zero-filled by the copy engine, and a zero delta is the identity step
+// (a = 2^0 = 1, b = 0), so ragged tails need no branch ([P1] s2.3); steps of a
+// loaded tile past valid_len get delta = 0 the same way.  Tiles that lie
+// entirely past valid_len[b] are never loaded: y there is written as exact
+// zeros and the state stays frozen.
+#pragma once
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "tiers.h"
+
+namespace ssm {
+namespace stream {
+
+typedef unsigned long long u64;
+constexpr unsigned kWaitLimit = 1u << 24;  // try_wait polls before a wait gives up
+constexpr unsigned kErrWait = 1u;
+
+// ---- paired fp32: two channels per instruction ---------------------------------
+__device__ __forceinline__ u64 pk2(float lo, float hi) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(u64 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+  u64 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ---- shared memory, mbarriers, TMA ---------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kWaitLimit unsuccessful polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (unsigned i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---- tile element access ---------------------------------------------------------
+// pairs<PR>: 2 PR consecutive activations (R channels of one step) as fp32 pairs.
+// row<G>:    G consecutive values of a B or C row, widened to fp32.
+// put<R>:    R consecutive outputs to global memory (rounded for bf16).
+template <typename IO> struct Tile;
+template <> struct Tile<float> {
+  static constexpr int kBytes = 4;
+  template <int PR>
+  static __device__ __forceinline__ void pairs(const float* p, u64 (&o)[PR]) {
+    if constexpr (PR == 2) {
+      const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
+      o[0] = v.x;
+      o[1] = v.y;
+    } else {
+      static_assert(PR == 1, "one or two channel pairs per lane");
+      o[0] = *reinterpret_cast<const u64*>(p);
+    }
+  }
+  template <int G>
+  static __device__ __forceinline__ void row(const float* p, float (&o)[G]) {
+    if constexpr (G % 4 == 0) {
+#pragma unroll
+      for (int k = 0; k < G / 4; ++k) {
+        const float4 v = reinterpret_cast<const float4*>(p)[k];
+        o[4 * k] = v.x;
+        o[4 * k + 1] = v.y;
+        o[4 * k + 2] = v.z;
+        o[4 * k + 3] = v.w;
+      }
+    } else {
+      static_assert(G == 2, "2, 4, 8 or 16 states per lane");
+      const float2 v = *reinterpret_cast<const float2*>(p);
+      o[0] = v.x;
+      o[1] = v.y;
+    }
+  }
+  // Predicated vector store (no branch: the steps around it stay in one block
+  // for the scheduler).
+  template <int R>
+  static __device__ __forceinline__ void put(float* p, const float (&v)[R], bool on) {
+    if constexpr (R == 4)
+      asm volatile(
+          "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
+          " @q st.global.v4.f32 [%0], {%1, %2, %3, %4};\n}\n" ::"l"(p),
+          "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "r"(int(on)));
+    else
+      asm volatile(
+          "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n"
+          " @q st.global.v2.f32 [%0], {%1, %2};\n}\n" ::"l"(p),
+          "f"(v[0]), "f"(v[1]), "r"(int(on)));
+  }
+  static __device__ __forceinline__ void put_zero(float* p, int64_t i) { p[i] = 0.f; }
+};
+template <> struct Tile<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __uint_as_float(w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ u64 widen(uint32_t w) { return pk2(lo(w), hi(w)); }
+  template <int PR>
+  static __device__ __forceinline__ void pairs(const __nv_bfloat16* p, u64 (&o)[PR]) {
+    if constexpr (PR == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      o[0] = widen(v.x);
+      o[1] = widen(v.y);
+    } else {
+      static_assert(PR == 1, "one or two channel pairs per lane");
+      o[0] = widen(*reinterpret_cast<const uint32_t*>(p));
+    }
+  }
+  template <int G>
+  static __device__ __forceinline__ void row(const __nv_bfloat16* p, float (&o)[G]) {
+    if constexpr (G % 8 == 0) {
+#pragma unroll
+      for (int k = 0; k < G / 8; ++k) {
+        const uint4 v = reinterpret_cast<const uint4*>(p)[k];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          o[8 * k + 2 * j] = lo(w[j]);
+          o[8 * k + 2 * j + 1] = hi(w[j]);
+        }
+      }
+    } else if constexpr (G == 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      o[0] = lo(v.x);
+      o[1] = hi(v.x);
+      o[2] = lo(v.y);
+      o[3] = hi(v.y);
+    } else {
+      static_assert(G == 2, "2, 4, 8 or 16 states per lane");
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      o[0] = lo(w);
+      o[1] = hi(w);
+    }
+  }
+  template <int R>
+  static __device__ __forceinline__ void put(__nv_bfloat16* p, const float (&v)[R], bool on) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    const uint32_t wa = *reinterpret_cast<const uint32_t*>(&a);
+    if constexpr (R == 4) {
+      const __nv_bfloat162 c = __floats2bfloat162_rn(v[2], v[3]);
+      const uint32_t wc = *reinterpret_cast<const uint32_t*>(&c);
+      asm volatile(
+          "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n"
+          " @q st.global.v2.b32 [%0], {%1, %2};\n}\n" ::"l"(p),
+          "r"(wa), "r"(wc), "r"(int(on)));
+    } else {
+      asm volatile(
+          "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n"
+          " @q st.global.b32 [%0], %1;\n}\n" ::"l"(p), "r"(wa), "r"(int(on)));
+    }
+  }
+  static __device__ __forceinline__ void put_zero(__nv_bfloat16* p, int64_t i) {
+    p[i] = __float2bfloat16_rn(0.f);
+  }
+};
+
+// Compile-time shape of one STREAM instance.
+template <int N_, int G_, int R_, typename IO_, bool GATE_>
+struct Cfg {
+  static constexpr int N = N_, G = G_, R = R_;
+  static constexpr bool GATE = GATE_;
+  using IO = IO_;
+  static constexpr int PR = R / 2;           // channel pairs per lane
+  static constexpr int NG = N / G;           // lanes per channel group
+  static constexpr int CG = 32 / NG;         // channel groups per warp
+  static constexpr int CW = CG * R;          // channels per warp
+  static constexpr int T = 64;               // steps per tile
+  static constexpr int ES = Tile<IO>::kBytes;
+  static constexpr int RAW = 2 * R + 2 * G;  // fp32 registers of one step's inputs
+  // steps per input batch: the loads of the next batch are in flight while one
+  // batch computes
+  static constexpr int U = RAW <= 12 ? 4 : (RAW <= 24 ? 2 : 1);
+  static constexpr int SG = U > NG ? U : NG;   // steps per output group
+  static constexpr int M = 16;                 // steps per block of the tile loop
+  // per-warp buffer of the C h partial sums of one block: [M][NG][CW] floats,
+  // rows padded by 16 floats so that the epilogue's reads spread over the banks
+  static constexpr int PROW = NG * CW + 16;
+  static constexpr int PBYTES = M * PROW * 4;
+  static constexpr int NACT = GATE ? 3 : 2;    // activation tensors per tile
+  static constexpr int SLAB = T * CW * ES;     // one warp's [T x CW] tile of one tensor
+  static constexpr int ROWT = T * N * ES;      // [T x N] tile of B or C
+  static_assert(R == 2 || R == 4, "two or four channels per lane");
+  static_assert(G >= 2 && N % G == 0 && NG <= 16 && (NG & (NG - 1)) == 0, "state groups");
+  static_assert((CW * ES) % 16 == 0 && (N * ES) % 16 == 0, "TMA box rows are 16-byte multiples");
+  static_assert(T % M == 0 && M % (2 * U) == 0 && M % NG == 0, "tile steps");
+  static_assert(PBYTES == 64 * (32 * R + 16), "partial buffer size (host mirror)");
+  static_assert(SLAB % 128 == 0 && ROWT % 128 == 0, "slot alignment");
+};
+
+// One batch of U steps' inputs for this lane, as loaded from the tile.
+template <class K>
+struct Raw {
+  u64 dt[K::U][K::PR], x[K::U][K::PR];
+  float b[K::U][K::G], c[K::U][K::G];
+};
+
+template <class K>
+__device__ __forceinline__ void load_batch(Raw<K>& r, const typename K::IO* ds,
+                                           const typename K::IO* xs, const typename K::IO* bs,
+                                           const typename K::IO* cs, int s) {
+  using TL = Tile<typename K::IO>;
+#pragma unroll
+  for (int u = 0; u < K::U; ++u) {
+    TL::template pairs<K::PR>(ds + (s + u) * K::CW, r.dt[u]);
+    TL::template pairs<K::PR>(xs + (s + u) * K::CW, r.x[u]);
+    TL::template row<K::G>(bs + (s + u) * K::N, r.b[u]);
+    TL::template row<K::G>(cs + (s + u) * K::N, r.c[u]);
+  }
+}
+
+// Sum over the NG lanes of a channel group, scattered: the lane with state
+// group sg returns the full sums of step sg of the NG steps' partials it was
+// given, for its R channels.  Each round halves the values a lane holds: it
+// keeps the half selected by its lane bit and adds the half its partner sends.
+template <int NG, int R>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NG][R], int sg, float (&out)[R]) {
+#pragma unroll
+  for (int m = NG / 2; m >= 1; m /= 2) {
+    const bool upper = (sg & m) != 0;
+#pragma unroll
+    for (int k = 0; k < m; ++k) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float keep = upper ? v[k + m][r] : v[k][r];
+        const float send = upper ? v[k][r] : v[k + m][r];
+        v[k][r] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) out[r] = v[0][r];
+}
+
+// Kernel arguments besides the tensor maps.
+struct LaunchArgs {
+  int warps;       // W, warps per CTA
+  int stages;      // slots in the ring
+  int stage_bytes;
+  unsigned int* err;  // sticky error word
+};
+
+template <class K>
+__global__ void __launch_bounds__(128, 1)
+    stream_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dt,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_b,
+                  const __grid_constant__ CUtensorMap tm_c, const ScanParams p,
+                  const LaunchArgs la) {
+  using IO = typename K::IO;
+  using TL = Tile<IO>;
+  constexpr int N = K::N, G = K::G, R = K::R, PR = K::PR, NG = K::NG, CW = K::CW;
+  constexpr int T = K::T, U = K::U, M = K::M, CG = K::CG;
+  extern __shared__ __align__(128) char smem[];
+  const int W = la.warps, STAGES = la.stages, SB = la.stage_bytes;
+  // this warp's partial-sum buffer, after the ring
+  float* pbuf = reinterpret_cast<float*>(smem + STAGES * SB + (threadIdx.x >> 5) * K::PBYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * SB + W * K::PBYTES);
+  uint64_t* empty = full + STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cpc = W * CW;
+  const int64_t n_cb = (p.dim + cpc - 1) / cpc;
+  const int64_t b = blockIdx.x / n_cb;
+  const int d0 = static_cast<int>((blockIdx.x % n_cb) * cpc);
+  const int cg = lane / NG, sg = lane % NG;
+  const int dw = d0 + warp * CW;       // the warp's first channel
+  const int64_t dl = dw + cg * R;      // the lane's first channel
+  const bool d_ok = dl < p.dim;        // all R channels valid (dim is a multiple of R)
+  const int64_t L = p.seqlen;
+  const int64_t lv = valid_steps(p, b);
+  const int n_tiles = static_cast<int>((lv + T - 1) / T);  // tiles with a valid step
+  const bool producer = threadIdx.x == 0;
+
+  auto issue = [&](int tile, int slot) {
+    char* st = smem + slot * SB;
+    const int t0 = tile * T;
+    mbar_expect_tx(&full[slot], SB);
+    for (int w = 0; w < W; ++w) {
+      tma_load_3d(st + (0 * W + w) * K::SLAB, &tm_x, d0 + w * CW, t0, static_cast<int>(b),
+                  &full[slot]);
+      tma_load_3d(st + (1 * W + w) * K::SLAB, &tm_dt, d0 + w * CW, t0, static_cast<int>(b),
+                  &full[slot]);
+      if constexpr (K::GATE)
+        tma_load_3d(st + (2 * W + w) * K::SLAB, &tm_z, d0 + w * CW, t0, static_cast<int>(b),
+                    &full[slot]);
+    }
+    char* rows = st + K::NACT * W * K::SLAB;
+    tma_load_3d(rows, &tm_b, 0, t0, static_cast<int>(b), &full[slot]);
+    tma_load_3d(rows + K::ROWT, &tm_c, 0, t0, static_cast<int>(b), &full[slot]);
+  };
+
+  if (producer) {
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], W);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (producer)
+    for (int st = 0; st < STAGES && st < n_tiles; ++st) issue(st, st);
+
+  // Per-lane constants: log2(e)-scaled A for (channel pair, state), the D
+  // residual (on the state-0 lane of the group only), the initial state.
+  u64 a2[PR][G], h2[PR][G];
+#pragma unroll
+  for (int q = 0; q < PR; ++q) {
+    const int64_t d_lo = dl + 2 * q, d_hi = d_lo + 1;
+#pragma unroll
+    for (int n = 0; n < G; ++n) {
+      float lo = 0.f, hi = 0.f;
+      if (d_ok) {
+        lo = __ldg(p.A + d_lo * N + sg * G + n) * kLog2e;
+        hi = __ldg(p.A + d_hi * N + sg * G + n) * kLog2e;
+      }
+      a2[q][n] = pk2(lo, hi);
+      float h_lo = 0.f, h_hi = 0.f;  // [P1] s4.1: h_0 = 0 unless given
+      if (d_ok && p.h0) {
+        h_lo = __ldg(p.h0 + (b * p.dim + d_lo) * N + sg * G + n);
+        h_hi = __ldg(p.h0 + (b * p.dim + d_hi) * N + sg * G + n);
+      }
+      h2[q][n] = pk2(h_lo, h_hi);
+    }
+  }
+
+  // The epilogue's view of the warp: lane (cp, sl) finishes the outputs of
+  // channels dw + cp R .. + R at steps sl, sl + NG, ... of each block.
+  const int cp = lane % CG, sl = lane / CG;
+  const int64_t de = dw + cp * R;
+  const bool de_ok = de < p.dim;
+  u64 dsk[PR];  // D residual of the epilogue's channels
+#pragma unroll
+  for (int q = 0; q < PR; ++q)
+    dsk[q] = (de_ok && p.D) ? pk2(__ldg(p.D + de + 2 * q), __ldg(p.D + de + 2 * q + 1)) : 0;
+  IO* __restrict__ yout = static_cast<IO*>(p.y);
+  const bool want_states = p.states != nullptr;
+  // Chunk c ends at step min((c+1) chunk_len, L) - 1 ([P1] s3.4).
+  auto chunk_end = [&](int64_t c) { return min((c + 1) * p.chunk_len, L) - 1; };
+  int64_t next_c = 0;
+  int64_t next_ce = want_states ? chunk_end(0) : INT64_MAX;
+  // the lane's G states of each of its R channels, as rows of `dst`
+  auto put_state = [&](float* dst) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float v[G];
+#pragma unroll
+      for (int n = 0; n < G; ++n) {
+        const float2 hv = upk2(h2[r / 2][n]);
+        v[n] = (r & 1) ? hv.y : hv.x;
+      }
+      float* row = dst + (dl + r) * N + sg * G;
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < G / 4; ++k)
+          reinterpret_cast<float4*>(row)[k] =
+              make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      } else {
+        reinterpret_cast<float2*>(row)[0] = make_float2(v[0], v[1]);
+      }
+    }
+  };
+  auto store_state = [&](int64_t t) {
+    if (d_ok) put_state(p.states + (b * p.n_chunks + t / p.chunk_len) * p.dim * N);
+  };
+
+  bool ok = true;
+  for (int i = 0; i < n_tiles && ok; ++i) {
+    const int slot = i % STAGES;
+    char* st = smem + slot * SB;
+    ok = mbar_wait(&full[slot], (i / STAGES) & 1);
+    if (!ok) break;
+    // refill the slot freed by the previous tile (every warp is done with it)
+    if (producer && i >= 1 && i - 1 + STAGES < n_tiles) {
+      const int ps = (i - 1) % STAGES;
+      ok = mbar_wait(&empty[ps], ((i - 1) / STAGES) & 1);
+      if (ok) issue(i - 1 + STAGES, ps);
+    }
+    const IO* xw = reinterpret_cast<const IO*>(st + (0 * W + warp) * K::SLAB);  // warp's slabs
+    const IO* zw = reinterpret_cast<const IO*>(st + (2 * W + warp) * K::SLAB);
+    const IO* xs = xw + cg * R;  // this lane's channels
+    const IO* ds = reinterpret_cast<const IO*>(st + (1 * W + warp) * K::SLAB) + cg * R;
+    const IO* bs = reinterpret_cast<const IO*>(st + K::NACT * W * K::SLAB) + sg * G;
+    const IO* cs = bs + T * N;
+    const int64_t t0 = static_cast<int64_t>(i) * T;
+    const int steps = static_cast<int>(lv - t0 < T ? lv - t0 : T);  // valid steps in tile
+    IO* ybase = yout + (b * L + t0) * p.dim + de;                    // y[b, t0, de]
+
+    // Epilogue of the block starting at step s0 of the tile: sum the NG
+    // partials of each (step, channel), add D x, gate, store.  Every lane's
+    // items are independent, so their shared-memory latencies overlap.
+    auto epilogue = [&](int s0) {
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < M / NG; ++i) {
+        const int j = sl + NG * i;  // step within the block
+        const int so = s0 + j;      // step within the tile
+        const float* pr = pbuf + j * K::PROW + cp * R;
+        u64 sum[PR];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          u64 part[PR];
+          Tile<float>::template pairs<PR>(pr + g * CW, part);
+#pragma unroll
+          for (int q = 0; q < PR; ++q) sum[q] = g == 0 ? part[q] : add2(sum[q], part[q]);
+        }
+        u64 xq[PR];
+        TL::template pairs<PR>(xw + so * CW + cp * R, xq);
+        float o[R];
+#pragma unroll
+        for (int q = 0; q < PR; ++q) {
+          const float2 yv = upk2(fma2(dsk[q], xq[q], sum[q]));  // + D x
+          o[2 * q] = yv.x;
+          o[2 * q + 1] = yv.y;
+        }
+        if constexpr (K::GATE) {
+          u64 zq[PR];
+          TL::template pairs<PR>(zw + so * CW + cp * R, zq);
+#pragma unroll
+          for (int q = 0; q < PR; ++q) {
+            const float2 zz = upk2(zq[q]);
+            o[2 * q] *= silu(zz.x);  // * silu(z)
+            o[2 * q + 1] *= silu(zz.y);
+          }
+        }
+        TL::template put<R>(ybase + static_cast<int64_t>(so) * p.dim, o, de_ok && so < steps);
+      }
+      __syncwarp();
+    };
+
+    // Two input buffers in turn: while the steps of one batch compute, the
+    // loads of the next are in flight.  A block of M steps holds an even
+    // number of batches, so the buffers' roles are fixed at compile time.
+    Raw<K> buf[2];
+    load_batch<K>(buf[0], ds, xs, bs, cs, 0);
+    for (int s0 = 0; s0 < steps; s0 += M) {
+      const int64_t b_last = t0 + s0 + M - 1;  // the block's last step
+      // CHECK: a chunk ends strictly inside the block, test every step (a
+      // branch per step would keep the compiler from overlapping steps).
+      // PARTIAL: the block runs past the last valid step of the tile.
+      auto run_block = [&](auto check, auto partial) {
+        constexpr bool CHECK = decltype(check)::value;
+        constexpr bool PARTIAL = decltype(partial)::value;
+#pragma unroll
+        for (int k = 0; k < M / U; ++k) {
+          const int s = s0 + k * U;
+          Raw<K>& cur = buf[k & 1];
+          // next batch; after the tile's last batch this wraps to its start (unused)
+          load_batch<K>(buf[(k + 1) & 1], ds, xs, bs, cs, (s + U) & (T - 1));
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int j = k * U + u;  // step within the block
+            u64 dt[PR], ux[PR];
+#pragma unroll
+            for (int q = 0; q < PR; ++q) {
+              dt[q] = cur.dt[u][q];
+              if constexpr (PARTIAL)
+                if (s + u >= steps) dt[q] = 0;  // past valid_len: identity (1, 0), [P1] s2.3
+              ux[q] = mul2(dt[q], cur.x[u][q]);  // delta x
+            }
+            // C h accumulates in NA independent chains (short dependency
+            // chains: one warp per scheduler has little else to overlap)
+            constexpr int NA = G >= 8 ? 4 : (G >= 4 ? 2 : 1);
+            u64 acc[NA][PR];
+#pragma unroll
+            for (int n = 0; n < G; ++n) {
+              const u64 bb = pk2(cur.b[u][n], cur.b[u][n]);
+              const u64 cc = pk2(cur.c[u][n], cur.c[u][n]);
+#pragma unroll
+              for (int q = 0; q < PR; ++q) {
+                const float2 arg = upk2(mul2(dt[q], a2[q][n]));
+                const u64 ab = pk2(ex2(arg.x), ex2(arg.y));     // Abar = exp(delta A)
+                h2[q][n] = fma2(ab, h2[q][n], mul2(ux[q], bb));  // h = Abar h + delta B x
+                if (n < NA)
+                  acc[n][q] = mul2(cc, h2[q][n]);
+                else
+                  acc[n % NA][q] = fma2(cc, h2[q][n], acc[n % NA][q]);  // C h
+              }
+            }
+            // this lane's partial of sum_n C_n h_n, to the block's buffer
+            u64 part[PR];
+#pragma unroll
+            for (int q = 0; q < PR; ++q) {
+#pragma unroll
+              for (int a = NA / 2; a >= 1; a /= 2)
+#pragma unroll
+                for (int i = 0; i < a; ++i) acc[i][q] = add2(acc[i][q], acc[i + a][q]);
+              part[q] = acc[0][q];
+            }
+            float* pw = pbuf + j * K::PROW + sg * CW + cg * R;
+            if constexpr (PR == 2)
+              *reinterpret_cast<ulonglong2*>(pw) = make_ulonglong2(part[0], part[1]);
+            else
+              *reinterpret_cast<u64*>(pw) = part[0];
+            if constexpr (CHECK) {
+              if (t0 + s + u == next_ce) {  // [P1] s3.4 chunk boundary state
+                store_state(next_ce);
+                ++next_c;
+                next_ce = next_c < p.n_chunks ? chunk_end(next_c) : INT64_MAX;
+              }
+            }
+          }
+        }
+      };
+      const bool partial = s0 + M > steps;
+      if (next_ce < b_last) {
+        if (partial) run_block(std::true_type{}, std::true_type{});
+        else run_block(std::true_type{}, std::false_type{});
+      } else {
+        if (partial) run_block(std::false_type{}, std::true_type{});
+        else run_block(std::false_type{}, std::false_type{});
+      }
+      if (next_ce == b_last) {  // a chunk ends with the block
+        store_state(next_ce);
+        ++next_c;
+        next_ce = next_c < p.n_chunks ? chunk_end(next_c) : INT64_MAX;
+      }
+      epilogue(s0);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+  if (!ok) {
+    if (lane == 0) atomicOr(la.err, kErrWait);
+    return;
+  }
+
+  // Steps past valid_len: exact zeros, frozen state for the remaining chunk ends.
+  if (lv < L) {
+    const int64_t total = (L - lv) * CW;
+    for (int64_t e = lane; e < total; e += 32) {
+      const int64_t t = lv + e / CW;
+      const int c = static_cast<int>(e % CW);
+      if (dw + c < p.dim) TL::put_zero(yout, (b * L + t) * p.dim + dw + c);
+    }
+  }
+  if (want_states)
+    for (; next_c < p.n_chunks; ++next_c) store_state(chunk_end(next_c));  // frozen state
+  if (p.h_final && d_ok) put_state(p.h_final + b * p.dim * N);  // state after the last step
+}
+
+// Host side, defined in kernel_stream.cu.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_t L, int64_t batch,
+              int box_inner, int box_t);
+unsigned int* error_word();
+int max_dynamic_smem();
+
+template <class K>
+int stage_bytes(int warps) {
+  return K::NACT * warps * K::SLAB + 2 * K::ROWT;
+}
+
+template <class K>
+cudaError_t launch_k(const ScanParams& p, cudaStream_t s, int warps, int stages) {
+  const bool bf16 = sizeof(typename K::IO) == 2;
+  CUtensorMap mx, mdt, mz, mb, mc;
+  if (!make_map(&mx, p.x, bf16, p.dim, p.seqlen, p.batch, K::CW, K::T) ||
+      !make_map(&mdt, p.delta, bf16, p.dim, p.seqlen, p.batch, K::CW, K::T) ||
+      !make_map(&mb, p.B, bf16, K::N, p.seqlen, p.batch, K::N, K::T) ||
+      !make_map(&mc, p.C, bf16, K::N, p.seqlen, p.batch, K::N, K::T))
+    return cudaErrorInvalidValue;
+  if constexpr (K::GATE) {
+    if (!make_map(&mz, p.z, bf16, p.dim, p.seqlen, p.batch, K::CW, K::T))
+      return cudaErrorInvalidValue;
+  } else {
+    mz = mx;  // unused
+  }
+  LaunchArgs la;
+  la.warps = warps;
+  la.stages = stages;
+  la.stage_bytes = stage_bytes<K>(warps);
+  la.err = error_word();
+  if (la.err == nullptr) return cudaErrorInvalidValue;
+  const int smem = stages * la.stage_bytes + warps * K::PBYTES + 2 * stages * 8;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel<K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         max_dynamic_smem());
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  if (smem > max_dynamic_smem()) return cudaErrorInvalidValue;
+  const int64_t n_cb = (p.dim + warps * K::CW - 1) / (warps * K::CW);
+  const int64_t grid = n_cb * p.batch;
+  stream_kernel<K><<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(mx, mdt, mz, mb, mc, p,
+                                                                        la);
+  return cudaGetLastError();
+}
+
+// Every launcher of one (N, G, R) instance: fp32 / bf16, with / without gate.
+template <int N, int G, int R>
+cudaError_t launch_ngr(const ScanParams& p, bool bf16, cudaStream_t s, int warps, int stages);
+
+// Per-stage bytes of an instance, for the host's ring sizing.
+template <int N, int G, int R>
+int stage_bytes_ngr(bool bf16, bool gate, int warps);
+
+template <int N, int G, int R>
+cudaError_t launch_ngr_impl(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
+  if (bf16) {
+    if constexpr (N * 2 >= 16)  // bf16 B/C rows of at least 16 bytes (TMA)
+      return p.z ? launch_k<Cfg<N, G, R, __nv_bfloat16, true>>(p, s, w, st)
+                 : launch_k<Cfg<N, G, R, __nv_bfloat16, false>>(p, s, w, st);
+    else
+      return cudaErrorInvalidValue;
+  }
+  return p.z ? launch_k<Cfg<N, G, R, float, true>>(p, s, w, st)
+             : launch_k<Cfg<N, G, R, float, false>>(p, s, w, st);
+}
+
+template <int N, int G, int R>
+int stage_bytes_impl(bool bf16, bool gate, int w) {
+  if (bf16) {
+    if constexpr (N * 2 >= 16)
+      return gate ? stage_bytes<Cfg<N, G, R, __nv_bfloat16, true>>(w)
+                  : stage_bytes<Cfg<N, G, R, __nv_bfloat16, false>>(w);
+    else
+      return 0;
+  }
+  return gate ? stage_bytes<Cfg<N, G, R, float, true>>(w)
+              : stage_bytes<Cfg<N, G, R, float, false>>(w);
+}
+
+#define SSM_STREAM_DEFINE(N_, G_, R_)                                                        \
+  template <>                                                                                \
+  cudaError_t launch_ngr<N_, G_, R_>(const ScanParams& p, bool bf16, cudaStream_t s, int w, \
+                                     int st) {                                               \
+    return launch_ngr_impl<N_, G_, R_>(p, bf16, s, w, st);                                   \
+  }                                                                                          \
+  template <>                                                                                \
+  int stage_bytes_ngr<N_, G_, R_>(bool bf16, bool gate, int w) {                             \
+    return stage_bytes_impl<N_, G_, R_>(bf16, gate, w);                                      \
+  }
+
+// Instances (N, G, R): states per lane G, channels per lane R.
+#define SSM_STREAM_INSTANCES(X)                              \
+  X(4, 4, 2) X(4, 4, 4)                                      \
+  X(8, 4, 2) X(8, 4, 4) X(8, 8, 2)                           \
+  X(16, 4, 2) X(16, 4, 4) X(16, 8, 2) X(16, 8, 4) X(16, 16, 2) \
+  X(32, 4, 4) X(32, 8, 2) X(32, 8, 4)                        \
+  X(64, 8, 2) X(64, 8, 4) X(64, 16, 2)
+
+#define SSM_STREAM_DECLARE(N_, G_, R_)                                                      \
+  template <>                                                                               \
+  cudaError_t launch_ngr<N_, G_, R_>(const ScanParams&, bool, cudaStream_t, int, int);     \
+  template <>                                                                               \
+  int stage_bytes_ngr<N_, G_, R_>(bool, bool, int);
+
+}  // namespace stream
+}  // namespace ssm

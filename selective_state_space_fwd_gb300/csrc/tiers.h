@@ -12,15 +12,16 @@ namespace ssm {
 cudaError_t launch_serial(const ScanParams& p, bool bf16, cudaStream_t s);
 int64_t serial_grid(const ScanParams& p);
 
-// STREAM tier: state-split register sweep with TMA-staged tiles.
+// STREAM tier: channel-pair register sweep with TMA-staged tiles.
 struct StreamShape {
-  int wpc;  // warps per thread block
-  int g;    // states per lane
-  int ts;   // time split: 1, or 2 half-warps on consecutive runs of a sub-tile
+  int wpc;     // warps per thread block
+  int g;       // states per lane
+  int r;       // channels per lane
+  int stages;  // slots in the shared-memory ring
 };
 // The launch shape for a request (0 = default); all zero when no instance exists.
-StreamShape stream_shape(const ScanParams& p, int warps_per_block, int states_per_lane,
-                         int time_split);
+StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, int states_per_lane,
+                         int channels_per_lane);
 bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
 int64_t stream_grid(const ScanParams& p, StreamShape sh);
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);

@@ -39,10 +39,10 @@ FAKE = 0x10000  # never dereferenced: validation returns before any device work
 
 
 def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None, y=FAKE,
-          states=None, shapes=(2, 8, 4, 16, 0), dtype=0, kernel=0, wpb=0, spl=0, ts=0, shapes_ptr=True):
+          states=None, shapes=(2, 8, 4, 16, 0), dtype=0, kernel=0, wpb=0, spl=0, cpl=0, shapes_ptr=True):
     lib = Bd.load()
     s = Bd.Shapes(*shapes)
-    o = Bd.Options(kernel, wpb, spl, ts)
+    o = Bd.Options(kernel, wpb, spl, cpl)
     P = ctypes.c_void_p
     return lib.ssm_scan_fwd_ex(P(x), P(delta), P(A), P(B), P(C), P(D), P(z), P(valid), P(y),
                                P(states), ctypes.byref(s) if shapes_ptr else None, dtype, None,
@@ -72,7 +72,9 @@ def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None
     (dict(wpb=-1), Bd.Status.ERR_UNSUPPORTED),
     (dict(spl=3), Bd.Status.ERR_UNSUPPORTED),
     (dict(spl=32), Bd.Status.ERR_UNSUPPORTED),
-    (dict(ts=3), Bd.Status.ERR_UNSUPPORTED),
+    (dict(cpl=3), Bd.Status.ERR_UNSUPPORTED),
+    (dict(cpl=1), Bd.Status.ERR_UNSUPPORTED),
+    (dict(cpl=8), Bd.Status.ERR_UNSUPPORTED),
     (dict(x=FAKE + 2), Bd.Status.ERR_ALIGN),
     (dict(y=FAKE + 1, dtype=1), Bd.Status.ERR_ALIGN),
     (dict(A=FAKE + 2, dtype=1), Bd.Status.ERR_ALIGN),

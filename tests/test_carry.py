@@ -33,11 +33,11 @@ def _h0(batch, dim, n, seed=3):
 
 def _gpu(inp, kernel, h0):
     t = W.to_torch(inp, "cuda")
-    k, ts = _tier(kernel)
+    k, shape = _tier(kernel)
     h = None if h0 is None else torch.from_numpy(h0).cuda()
     y, s, f = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
-                         t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, time_split=ts,
-                         h0=h, want_final=True)
+                         t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, h0=h,
+                         want_final=True, **shape)
     torch.cuda.synchronize()
     return to_f64(y), (to_f64(s) if s is not None else None), to_f64(f)
 

@@ -15,13 +15,19 @@ from selective_state_space_fwd_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-# (tier, time_split): "stream2t" is the STREAM tier with its two half-warps on
-# consecutive runs of each sub-tile
-TIERS = ["serial", "warpscan", "stream", "stream2t", "auto"]
+# Tiers and STREAM launch shapes: "stream" takes the library's default shape,
+# "stream-r4" four channels per thread, "stream-g8" eight states per thread,
+# "stream-w4" four warps per CTA.
+TIERS = ["serial", "warpscan", "stream", "stream-r4", "stream-g8", "stream-w4", "auto"]
+_SHAPES = {"stream-r4": dict(channels_per_lane=4), "stream-g8": dict(states_per_lane=8),
+           "stream-w4": dict(warps_per_block=4)}
 
 
 def _tier(kernel):
-    return ("stream", 2) if kernel == "stream2t" else (kernel, 0)
+    """(tier, launch-shape keyword arguments) of a TIERS entry."""
+    if kernel in _SHAPES:
+        return "stream", _SHAPES[kernel]
+    return kernel, {}
 
 
 TOL_Y = {"f32": 1e-5, "bf16": 1e-2}
@@ -40,9 +46,9 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 
 def run_gpu(inp: dict, kernel="auto"):
     t = W.to_torch(inp, "cuda")
-    k, ts = _tier(kernel)
+    k, shape = _tier(kernel)
     y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
-                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, time_split=ts)
+                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, **shape)
     torch.cuda.synchronize()
     return to_f64(y), (to_f64(s) if s is not None else None)
 
@@ -77,11 +83,10 @@ def tier_supported(inp, kernel):
     if kernel == "auto":
         return True
     Bt, L, Dm = inp["x"].shape
-    k, ts = _tier(kernel)
+    k, shape = _tier(kernel)
     try:
         S.plan(Bt, L, Dm, inp["B"].shape[-1], dtype=inp["dtype"], gate=inp["z"] is not None,
-               mask=inp["valid_len"] is not None, chunk_len=inp["chunk_len"], kernel=k,
-               time_split=ts)
+               mask=inp["valid_len"] is not None, chunk_len=inp["chunk_len"], kernel=k, **shape)
         return True
     except S.SsmError as e:
         assert e.status == S.Status.ERR_UNSUPPORTED
