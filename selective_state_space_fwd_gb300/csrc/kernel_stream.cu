@@ -102,38 +102,27 @@ int sm_count() {
 
 int channels_per_warp(int n, int g, int r) { return (32 / (n / g)) * r; }
 
-// Bytes of a warp's partial-sum buffer (mirrors Cfg::PBYTES).
-int partial_bytes(int r) { return 64 * (32 * r + 16); }
+// Bytes of a warp's partial-sum buffer.
+int partial_bytes(int n, int g, int r) {
+#define SSM_PB(n_, g_, r_) \
+  if (n == n_ && g == g_ && r == r_) return Cfg<n_, g_, r_, float, false>::PBYTES;
+  SSM_STREAM_INSTANCES(SSM_PB)
+#undef SSM_PB
+  return 0;
+}
 
-// Default (G, R) for a problem: enough lanes for about four warps per SM,
-// then as many (channel, state) pairs per lane as that allows (each lane's
-// loads then serve more work).  Choices measured on GB300 for the workloads
-// of the benchmark.
+// Default (G, R): two channels per lane, four states (eight from 32 states
+// up).  Measured on GB300 over the benchmark's workloads (8192 to 49152
+// channels of 16 or 64 states): more (channel, state) pairs per lane cut the
+// shared-memory traffic per pair but leave fewer warps to hide latency, and
+// these problems have at most a few warps per scheduler to begin with.
 void default_gr(const ScanParams& p, int* g, int* r) {
-  const double lanes_per_sm = 4.0 * 32.0;
-  const double per_lane = double(p.batch) * p.dim * p.dstate / (lanes_per_sm * sm_count());
-  struct GR { int g, r; };
-  // candidates per N, from the fewest to the most (channel, state) pairs per lane
-  static const GR c4[] = {{4, 2}, {4, 4}};
-  static const GR c8[] = {{4, 2}, {4, 4}, {8, 2}};
-  static const GR c16[] = {{4, 2}, {4, 4}, {8, 4}};
-  static const GR c32[] = {{8, 2}, {8, 4}};
-  static const GR c64[] = {{8, 2}, {8, 4}};
-  const GR* c = nullptr;
-  int nc = 0;
+  *r = 2;
   switch (p.dstate) {
-    case 4: c = c4; nc = 2; break;
-    case 8: c = c8; nc = 3; break;
-    case 16: c = c16; nc = 3; break;
-    case 32: c = c32; nc = 2; break;
-    case 64: c = c64; nc = 2; break;
-    default: *g = 0; *r = 0; return;
+    case 4: case 8: case 16: *g = 4; break;
+    case 32: case 64: *g = 8; break;
+    default: *g = 0; *r = 0; break;
   }
-  int pick = 0;
-  for (int i = 1; i < nc; ++i)
-    if (c[i].g * c[i].r <= per_lane) pick = i;
-  *g = c[pick].g;
-  *r = c[pick].r;
 }
 
 }  // namespace
@@ -164,7 +153,7 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
     const int64_t cap = 16 / w;  // about 16 warps per SM by registers
     if (per_sm > cap) per_sm = cap;
     *per_sm_out = per_sm;
-    const int fixed = w * partial_bytes(r) + 64;  // partial-sum buffers, barriers
+    const int fixed = w * partial_bytes(p.dstate, g, r) + 64;  // partial-sum buffers, barriers
     int st = static_cast<int>((smem_sm / per_sm - 1024 - fixed) / sb);
     if (st > 4) st = 4;
     if (st * sb + fixed > max_dynamic_smem()) st = (max_dynamic_smem() - fixed) / sb;
@@ -176,7 +165,7 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
     stages = stages_for(w, &per_sm);
     if (stages == 0) {  // the caller's W: two slots, even if not every CTA is resident
       const int sb = stage_bytes_of(p.dstate, g, r, bf16, p.z != nullptr, w);
-      if (sb <= 0 || 2 * sb + w * partial_bytes(r) + 64 > max_dynamic_smem()) return sh;
+      if (sb <= 0 || 2 * sb + w * partial_bytes(p.dstate, g, r) + 64 > max_dynamic_smem()) return sh;
       stages = 2;
     }
   } else {  // the fewest warps per CTA for which all CTAs are resident at once
@@ -188,7 +177,7 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
       w = 4;
       stages = 2;
       const int sb = stage_bytes_of(p.dstate, g, r, bf16, p.z != nullptr, w);
-      if (sb <= 0 || 2 * sb + w * partial_bytes(r) + 64 > max_dynamic_smem()) return sh;
+      if (sb <= 0 || 2 * sb + w * partial_bytes(p.dstate, g, r) + 64 > max_dynamic_smem()) return sh;
     }
   }
   sh.wpc = w;

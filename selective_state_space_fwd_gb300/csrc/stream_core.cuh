@@ -116,7 +116,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 
 // ---- tile element access ---------------------------------------------------------
 // pairs<PR>: 2 PR consecutive activations (R channels of one step) as fp32 pairs.
-// row<G>:    G consecutive values of a B or C row, widened to fp32.
+// row<G>:    G values of a B or C row (16-byte chunks in a per-lane order), widened to fp32.
 // put<R>:    R consecutive outputs to global memory (rounded for bf16).
 template <typename IO> struct Tile;
 template <> struct Tile<float> {
@@ -132,12 +132,13 @@ template <> struct Tile<float> {
       o[0] = *reinterpret_cast<const u64*>(p);
     }
   }
+  // row<G>: 16-byte chunk k of the registers comes from p + coff[k] (elements)
   template <int G>
-  static __device__ __forceinline__ void row(const float* p, float (&o)[G]) {
+  static __device__ __forceinline__ void row(const float* p, float (&o)[G], const int* coff) {
     if constexpr (G % 4 == 0) {
 #pragma unroll
       for (int k = 0; k < G / 4; ++k) {
-        const float4 v = reinterpret_cast<const float4*>(p)[k];
+        const float4 v = *reinterpret_cast<const float4*>(p + coff[k]);
         o[4 * k] = v.x;
         o[4 * k + 1] = v.y;
         o[4 * k + 2] = v.z;
@@ -186,11 +187,12 @@ template <> struct Tile<__nv_bfloat16> {
     }
   }
   template <int G>
-  static __device__ __forceinline__ void row(const __nv_bfloat16* p, float (&o)[G]) {
+  static __device__ __forceinline__ void row(const __nv_bfloat16* p, float (&o)[G],
+                                             const int* coff) {
     if constexpr (G % 8 == 0) {
 #pragma unroll
       for (int k = 0; k < G / 8; ++k) {
-        const uint4 v = reinterpret_cast<const uint4*>(p)[k];
+        const uint4 v = *reinterpret_cast<const uint4*>(p + coff[k]);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -233,6 +235,47 @@ template <> struct Tile<__nv_bfloat16> {
   }
 };
 
+// Shared-memory bank check for one access phase of a warp: lanes [l0, l0 + n)
+// each touching R consecutive floats at offset(lane); true if no two lanes
+// share a bank (32 banks of 4 bytes).  An access of R floats per lane is
+// served in phases of 32 / R lanes.
+template <class F>
+constexpr bool phase_ok(int l0, int n, int R, F offset) {
+  bool used[32] = {};
+  for (int l = l0; l < l0 + n; ++l)
+    for (int i = 0; i < R; ++i) {
+      const int bank = (offset(l) + i) % 32;
+      if (used[bank]) return false;
+      used[bank] = true;
+    }
+  return true;
+}
+// Stride (floats) between the state groups of a partial row: compute lane
+// (cg = lane / NG, sg = lane % NG) writes R floats at sg * PS + cg * R.
+constexpr int pad_ps(int NG, int CW, int R) {
+  for (int pad = 0; pad < 32; pad += 4) {
+    const int ps = CW + pad;
+    bool ok = true;
+    for (int l0 = 0; l0 < 32; l0 += 32 / R)
+      ok = ok && phase_ok(l0, 32 / R, R, [&](int l) { return (l % NG) * ps + (l / NG) * R; });
+    if (ok) return ps;
+  }
+  return CW;
+}
+// Stride (floats) between the steps of the partial buffer: epilogue lane
+// (cp = lane % CG, sl = lane / CG) reads R floats at sl * PROW + g * PS + cp * R.
+constexpr int pad_prow(int NG, int CW, int R, int PS) {
+  const int CG = 32 / NG;
+  for (int pad = 0; pad < 64; pad += 4) {
+    const int pr = NG * PS + pad;
+    bool ok = true;
+    for (int l0 = 0; l0 < 32; l0 += 32 / R)
+      ok = ok && phase_ok(l0, 32 / R, R, [&](int l) { return (l / CG) * pr + (l % CG) * R; });
+    if (ok) return pr;
+  }
+  return NG * PS;
+}
+
 // Compile-time shape of one STREAM instance.
 template <int N_, int G_, int R_, typename IO_, bool GATE_>
 struct Cfg {
@@ -245,24 +288,31 @@ struct Cfg {
   static constexpr int CW = CG * R;          // channels per warp
   static constexpr int T = 64;               // steps per tile
   static constexpr int ES = Tile<IO>::kBytes;
-  static constexpr int RAW = 2 * R + 2 * G;  // fp32 registers of one step's inputs
-  // steps per input batch: the loads of the next batch are in flight while one
-  // batch computes
-  static constexpr int U = RAW <= 12 ? 4 : (RAW <= 24 ? 2 : 1);
-  static constexpr int SG = U > NG ? U : NG;   // steps per output group
+  // steps per batch: a batch's inputs are loaded two batches ahead and its
+  // decays and input terms formed one batch ahead of its recurrence
+  static constexpr int U = R * G <= 8 ? 2 : 1;
   static constexpr int M = 16;                 // steps per block of the tile loop
-  // per-warp buffer of the C h partial sums of one block: [M][NG][CW] floats,
-  // rows padded by 16 floats so that the epilogue's reads spread over the banks
-  static constexpr int PROW = NG * CW + 16;
+  // per-warp buffer of the C h partial sums of one block: [M][NG][PS] floats
+  // (row j: step j of the block, then state group, then channel), with the
+  // paddings PS - CW and PROW - NG PS chosen so that the compute lanes'
+  // writes and the epilogue lanes' reads hit distinct banks
+  static constexpr int PS = pad_ps(NG, CW, R);
+  static constexpr int PROW = pad_prow(NG, CW, R, PS);
   static constexpr int PBYTES = M * PROW * 4;
   static constexpr int NACT = GATE ? 3 : 2;    // activation tensors per tile
+  // A lane's slice of a B or C row is MCH 16-byte chunks of CHUNK elements.
+  // The lanes of one access phase start their slices 16 * MCH bytes apart, so
+  // for MCH > 1 they would collide in the banks; each lane therefore visits
+  // its chunks rotated by ROT(sg) and keeps its states in that order.
+  static constexpr int CHUNK = 16 / ES;
+  static constexpr int MCH = G * ES >= 16 ? G * ES / 16 : 1;
   static constexpr int SLAB = T * CW * ES;     // one warp's [T x CW] tile of one tensor
   static constexpr int ROWT = T * N * ES;      // [T x N] tile of B or C
   static_assert(R == 2 || R == 4, "two or four channels per lane");
   static_assert(G >= 2 && N % G == 0 && NG <= 16 && (NG & (NG - 1)) == 0, "state groups");
   static_assert((CW * ES) % 16 == 0 && (N * ES) % 16 == 0, "TMA box rows are 16-byte multiples");
   static_assert(T % M == 0 && M % (2 * U) == 0 && M % NG == 0, "tile steps");
-  static_assert(PBYTES == 64 * (32 * R + 16), "partial buffer size (host mirror)");
+  static_assert(PROW % 4 == 0 && PS % 4 == 0 && PBYTES <= 12 * 1024, "partial buffer");
   static_assert(SLAB % 128 == 0 && ROWT % 128 == 0, "slot alignment");
 };
 
@@ -276,38 +326,47 @@ struct Raw {
 template <class K>
 __device__ __forceinline__ void load_batch(Raw<K>& r, const typename K::IO* ds,
                                            const typename K::IO* xs, const typename K::IO* bs,
-                                           const typename K::IO* cs, int s) {
+                                           const typename K::IO* cs, int s, const int* coff) {
   using TL = Tile<typename K::IO>;
 #pragma unroll
   for (int u = 0; u < K::U; ++u) {
     TL::template pairs<K::PR>(ds + (s + u) * K::CW, r.dt[u]);
     TL::template pairs<K::PR>(xs + (s + u) * K::CW, r.x[u]);
-    TL::template row<K::G>(bs + (s + u) * K::N, r.b[u]);
-    TL::template row<K::G>(cs + (s + u) * K::N, r.c[u]);
+    TL::template row<K::G>(bs + (s + u) * K::N, r.b[u], coff);
+    TL::template row<K::G>(cs + (s + u) * K::N, r.c[u], coff);
   }
 }
 
-// Sum over the NG lanes of a channel group, scattered: the lane with state
-// group sg returns the full sums of step sg of the NG steps' partials it was
-// given, for its R channels.  Each round halves the values a lane holds: it
-// keeps the half selected by its lane bit and adds the half its partner sends.
-template <int NG, int R>
-__device__ __forceinline__ void reduce_scatter(float (&v)[NG][R], int sg, float (&out)[R]) {
+// One batch of U steps, ready for the recurrence: the decays Abar = exp(delta A)
+// ([P1] s2.4: 2^(delta * A log2 e), one MUFU ex2 each), the input terms
+// b = delta B x ([P1] s3.3), per channel pair and state; the C values.
+template <class K>
+struct Prep {
+  u64 ab[K::U][K::PR][K::G], bi[K::U][K::PR][K::G];
+  float c[K::U][K::G];
+};
+
+// Steps at or past `steps` (the tile's valid steps) become the identity
+// (a = 1, b = 0) through delta = 0 ([P1] s2.3).
+template <class K>
+__device__ __forceinline__ void prepare(Prep<K>& o, const Raw<K>& r, const u64 (&a2)[K::PR][K::G],
+                                        int s, int steps) {
 #pragma unroll
-  for (int m = NG / 2; m >= 1; m /= 2) {
-    const bool upper = (sg & m) != 0;
+  for (int u = 0; u < K::U; ++u) {
 #pragma unroll
-    for (int k = 0; k < m; ++k) {
+    for (int q = 0; q < K::PR; ++q) {
+      const u64 dt = s + u < steps ? r.dt[u][q] : 0;
+      const u64 ux = mul2(dt, r.x[u][q]);  // delta x
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float keep = upper ? v[k + m][r] : v[k][r];
-        const float send = upper ? v[k][r] : v[k + m][r];
-        v[k][r] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      for (int n = 0; n < K::G; ++n) {
+        const float2 arg = upk2(mul2(dt, a2[q][n]));
+        o.ab[u][q][n] = pk2(ex2(arg.x), ex2(arg.y));
+        o.bi[u][q][n] = mul2(ux, pk2(r.b[u][n], r.b[u][n]));
       }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) out[r] = v[0][r];
+    for (int n = 0; n < K::G; ++n) o.c[u][n] = r.c[u][n];
+  }
 }
 
 // Kernel arguments besides the tensor maps.
@@ -378,8 +437,18 @@ __global__ void __launch_bounds__(128, 1)
   if (producer)
     for (int st = 0; st < STAGES && st < n_tiles; ++st) issue(st, st);
 
-  // Per-lane constants: log2(e)-scaled A for (channel pair, state), the D
-  // residual (on the state-0 lane of the group only), the initial state.
+  // Register n of a lane holds state gsn(n) of its channels (chunk rotation,
+  // see Cfg::MCH); coff[k] is the row offset of the lane's k-th loaded chunk.
+  constexpr int CHK = K::CHUNK, MCH = K::MCH;
+  const int rot = MCH > 1 ? (sg / (8 / MCH)) % MCH : 0;
+  int coff[MCH];
+#pragma unroll
+  for (int k = 0; k < MCH; ++k) coff[k] = ((k + rot) % MCH) * CHK;
+  auto gsn = [&](int n) {
+    return MCH > 1 ? sg * G + ((n / CHK + rot) % MCH) * CHK + n % CHK : sg * G + n;
+  };
+  // Per-lane constants: log2(e)-scaled A for (channel pair, state), the
+  // initial state.
   u64 a2[PR][G], h2[PR][G];
 #pragma unroll
   for (int q = 0; q < PR; ++q) {
@@ -388,14 +457,14 @@ __global__ void __launch_bounds__(128, 1)
     for (int n = 0; n < G; ++n) {
       float lo = 0.f, hi = 0.f;
       if (d_ok) {
-        lo = __ldg(p.A + d_lo * N + sg * G + n) * kLog2e;
-        hi = __ldg(p.A + d_hi * N + sg * G + n) * kLog2e;
+        lo = __ldg(p.A + d_lo * N + gsn(n)) * kLog2e;
+        hi = __ldg(p.A + d_hi * N + gsn(n)) * kLog2e;
       }
       a2[q][n] = pk2(lo, hi);
       float h_lo = 0.f, h_hi = 0.f;  // [P1] s4.1: h_0 = 0 unless given
       if (d_ok && p.h0) {
-        h_lo = __ldg(p.h0 + (b * p.dim + d_lo) * N + sg * G + n);
-        h_hi = __ldg(p.h0 + (b * p.dim + d_hi) * N + sg * G + n);
+        h_lo = __ldg(p.h0 + (b * p.dim + d_lo) * N + gsn(n));
+        h_hi = __ldg(p.h0 + (b * p.dim + d_hi) * N + gsn(n));
       }
       h2[q][n] = pk2(h_lo, h_hi);
     }
@@ -426,14 +495,14 @@ __global__ void __launch_bounds__(128, 1)
         const float2 hv = upk2(h2[r / 2][n]);
         v[n] = (r & 1) ? hv.y : hv.x;
       }
-      float* row = dst + (dl + r) * N + sg * G;
-      if constexpr (G % 4 == 0) {
+      float* row = dst + (dl + r) * N;
+      if constexpr (G % 4 == 0) {  // 4 consecutive registers are 4 consecutive states
 #pragma unroll
         for (int k = 0; k < G / 4; ++k)
-          reinterpret_cast<float4*>(row)[k] =
+          *reinterpret_cast<float4*>(row + gsn(4 * k)) =
               make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
       } else {
-        reinterpret_cast<float2*>(row)[0] = make_float2(v[0], v[1]);
+        reinterpret_cast<float2*>(row + sg * G)[0] = make_float2(v[0], v[1]);
       }
     }
   };
@@ -477,7 +546,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           u64 part[PR];
-          Tile<float>::template pairs<PR>(pr + g * CW, part);
+          Tile<float>::template pairs<PR>(pr + g * K::PS, part);
 #pragma unroll
           for (int q = 0; q < PR; ++q) sum[q] = g == 0 ? part[q] : add2(sum[q], part[q]);
         }
@@ -505,49 +574,42 @@ __global__ void __launch_bounds__(128, 1)
       __syncwarp();
     };
 
-    // Two input buffers in turn: while the steps of one batch compute, the
-    // loads of the next are in flight.  A block of M steps holds an even
-    // number of batches, so the buffers' roles are fixed at compile time.
-    Raw<K> buf[2];
-    load_batch<K>(buf[0], ds, xs, bs, cs, 0);
+    // Software pipeline over batches of U steps: while batch k runs its
+    // recurrence (the fp32 pipe), the decays and input terms of batch k+1 are
+    // formed (the MUFU pipe) and the loads of batch k+2 are in flight.  A
+    // block of M steps holds an even number of batches, so the roles of the
+    // two raw and two prepared buffers are fixed at compile time.
+    Raw<K> raw[2];
+    Prep<K> prep[2];
+    load_batch<K>(raw[0], ds, xs, bs, cs, 0, coff);
+    load_batch<K>(raw[1], ds, xs, bs, cs, U & (T - 1), coff);
+    prepare<K>(prep[0], raw[0], a2, 0, steps);
     for (int s0 = 0; s0 < steps; s0 += M) {
       const int64_t b_last = t0 + s0 + M - 1;  // the block's last step
       // CHECK: a chunk ends strictly inside the block, test every step (a
       // branch per step would keep the compiler from overlapping steps).
-      // PARTIAL: the block runs past the last valid step of the tile.
-      auto run_block = [&](auto check, auto partial) {
+      auto run_block = [&](auto check) {
         constexpr bool CHECK = decltype(check)::value;
-        constexpr bool PARTIAL = decltype(partial)::value;
 #pragma unroll
         for (int k = 0; k < M / U; ++k) {
           const int s = s0 + k * U;
-          Raw<K>& cur = buf[k & 1];
-          // next batch; after the tile's last batch this wraps to its start (unused)
-          load_batch<K>(buf[(k + 1) & 1], ds, xs, bs, cs, (s + U) & (T - 1));
+          prepare<K>(prep[(k + 1) & 1], raw[(k + 1) & 1], a2, s + U, steps);  // batch k+1
+          // batch k+2; near the tile's end this wraps to its start (unused)
+          load_batch<K>(raw[k & 1], ds, xs, bs, cs, (s + 2 * U) & (T - 1), coff);
+          const Prep<K>& cur = prep[k & 1];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int j = k * U + u;  // step within the block
-            u64 dt[PR], ux[PR];
-#pragma unroll
-            for (int q = 0; q < PR; ++q) {
-              dt[q] = cur.dt[u][q];
-              if constexpr (PARTIAL)
-                if (s + u >= steps) dt[q] = 0;  // past valid_len: identity (1, 0), [P1] s2.3
-              ux[q] = mul2(dt[q], cur.x[u][q]);  // delta x
-            }
             // C h accumulates in NA independent chains (short dependency
             // chains: one warp per scheduler has little else to overlap)
             constexpr int NA = G >= 8 ? 4 : (G >= 4 ? 2 : 1);
             u64 acc[NA][PR];
 #pragma unroll
             for (int n = 0; n < G; ++n) {
-              const u64 bb = pk2(cur.b[u][n], cur.b[u][n]);
               const u64 cc = pk2(cur.c[u][n], cur.c[u][n]);
 #pragma unroll
               for (int q = 0; q < PR; ++q) {
-                const float2 arg = upk2(mul2(dt[q], a2[q][n]));
-                const u64 ab = pk2(ex2(arg.x), ex2(arg.y));     // Abar = exp(delta A)
-                h2[q][n] = fma2(ab, h2[q][n], mul2(ux[q], bb));  // h = Abar h + delta B x
+                h2[q][n] = fma2(cur.ab[u][q][n], h2[q][n], cur.bi[u][q][n]);  // h = Abar h + b
                 if (n < NA)
                   acc[n][q] = mul2(cc, h2[q][n]);
                 else
@@ -564,7 +626,7 @@ __global__ void __launch_bounds__(128, 1)
                 for (int i = 0; i < a; ++i) acc[i][q] = add2(acc[i][q], acc[i + a][q]);
               part[q] = acc[0][q];
             }
-            float* pw = pbuf + j * K::PROW + sg * CW + cg * R;
+            float* pw = pbuf + j * K::PROW + sg * K::PS + cg * R;
             if constexpr (PR == 2)
               *reinterpret_cast<ulonglong2*>(pw) = make_ulonglong2(part[0], part[1]);
             else
@@ -579,14 +641,10 @@ __global__ void __launch_bounds__(128, 1)
           }
         }
       };
-      const bool partial = s0 + M > steps;
-      if (next_ce < b_last) {
-        if (partial) run_block(std::true_type{}, std::true_type{});
-        else run_block(std::true_type{}, std::false_type{});
-      } else {
-        if (partial) run_block(std::false_type{}, std::true_type{});
-        else run_block(std::false_type{}, std::false_type{});
-      }
+      if (next_ce < b_last)
+        run_block(std::true_type{});
+      else
+        run_block(std::false_type{});
       if (next_ce == b_last) {  // a chunk ends with the block
         store_state(next_ce);
         ++next_c;
