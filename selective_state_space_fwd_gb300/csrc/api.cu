@@ -181,7 +181,7 @@ HostLayout host_layout(const ssm_shapes* s, ssm_dtype dtype, int has_D, int has_
 // one strided 2-D copy.
 
 #ifndef SSM_HOST_PIECES
-#define SSM_HOST_PIECES 16  // pieces per call when the sequence is long enough
+#define SSM_HOST_PIECES 8  // pieces per call when the sequence is long enough
 #endif
 
 // Library-owned copy streams and the events that chain them, one set per device.
