@@ -28,7 +28,7 @@
 // bounded waits order the copies and their reuse.  Boxes that run past L or D
 // are zero-filled by the copy engine, and a zero delta is the identity step
 // (a = 2^0 = 1, b = 0), so ragged tails need no branch ([P1] s2.3); steps of a
-// loaded tile past valid_len get delta = 0 the same way.  Tiles that lie
+// loaded tile past valid_len are zeroed in shared memory the same way.  Tiles that lie
 // entirely past valid_len[b] are never loaded: y there is written as exact
 // zeros and the state stays frozen.
 #pragma once
@@ -346,16 +346,13 @@ struct Prep {
   float c[K::U][K::G];
 };
 
-// Steps at or past `steps` (the tile's valid steps) become the identity
-// (a = 1, b = 0) through delta = 0 ([P1] s2.3).
 template <class K>
-__device__ __forceinline__ void prepare(Prep<K>& o, const Raw<K>& r, const u64 (&a2)[K::PR][K::G],
-                                        int s, int steps) {
+__device__ __forceinline__ void prepare(Prep<K>& o, const Raw<K>& r, const u64 (&a2)[K::PR][K::G]) {
 #pragma unroll
   for (int u = 0; u < K::U; ++u) {
 #pragma unroll
     for (int q = 0; q < K::PR; ++q) {
-      const u64 dt = s + u < steps ? r.dt[u][q] : 0;
+      const u64 dt = r.dt[u][q];
       const u64 ux = mul2(dt, r.x[u][q]);  // delta x
 #pragma unroll
       for (int n = 0; n < K::G; ++n) {
@@ -531,6 +528,26 @@ __global__ void __launch_bounds__(128, 1)
     const int64_t t0 = static_cast<int64_t>(i) * T;
     const int steps = static_cast<int>(lv - t0 < T ? lv - t0 : T);  // valid steps in tile
     IO* ybase = yout + (b * L + t0) * p.dim + de;                    // y[b, t0, de]
+    if (steps < T) {
+      // Steps of the tile past valid_len become the identity (a = 1, b = 0,
+      // [P1] s2.3): their delta, x, B and C are set to zero in the tile, so
+      // no per-step test is needed and padded values never reach the state.
+      // The B and C rows are shared by the CTA's warps: each warp zeroes them
+      // itself (every writer stores the same zeros, and a warp reads them only
+      // after its own pass), so no CTA-wide barrier is needed.
+      IO* dsw = const_cast<IO*>(reinterpret_cast<const IO*>(st + (1 * W + warp) * K::SLAB));
+      IO* xsw = const_cast<IO*>(xw);
+      for (int e = steps * CW + lane; e < T * CW; e += 32) {
+        dsw[e] = IO(0.f);
+        xsw[e] = IO(0.f);
+      }
+      IO* rows = reinterpret_cast<IO*>(st + K::NACT * W * K::SLAB);
+      for (int e = steps * N + lane; e < T * N; e += 32) {
+        rows[e] = IO(0.f);          // B
+        rows[T * N + e] = IO(0.f);  // C
+      }
+      __syncwarp();
+    }
 
     // Epilogue of the block starting at step s0 of the tile: sum the NG
     // partials of each (step, channel), add D x, gate, store.  Every lane's
@@ -583,7 +600,7 @@ __global__ void __launch_bounds__(128, 1)
     Prep<K> prep[2];
     load_batch<K>(raw[0], ds, xs, bs, cs, 0, coff);
     load_batch<K>(raw[1], ds, xs, bs, cs, U & (T - 1), coff);
-    prepare<K>(prep[0], raw[0], a2, 0, steps);
+    prepare<K>(prep[0], raw[0], a2);
     for (int s0 = 0; s0 < steps; s0 += M) {
       const int64_t b_last = t0 + s0 + M - 1;  // the block's last step
       // CHECK: a chunk ends strictly inside the block, test every step (a
@@ -593,7 +610,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int k = 0; k < M / U; ++k) {
           const int s = s0 + k * U;
-          prepare<K>(prep[(k + 1) & 1], raw[(k + 1) & 1], a2, s + U, steps);  // batch k+1
+          prepare<K>(prep[(k + 1) & 1], raw[(k + 1) & 1], a2);  // batch k+1
           // batch k+2; near the tile's end this wraps to its start (unused)
           load_batch<K>(raw[k & 1], ds, xs, bs, cs, (s + 2 * U) & (T - 1), coff);
           const Prep<K>& cur = prep[k & 1];
