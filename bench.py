@@ -189,6 +189,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--op", default="scan", choices=["scan", "decode"],
+                    help="scan: the forward (default); decode: one recurrence step on a "
+                         "carried state (--workload picks a decode workload)")
     return ap.parse_args()
 
 
@@ -266,8 +269,170 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+DECODE_METRIC = "decode step: B*D (batch row, channel) updates/s and achieved % of HBM roofline, 1xGB300"
+
+
+def decode_counts(w) -> dict:
+    """Algorithmic bytes of one decode step: the state read and written once,
+    the step's inputs read, y written."""
+    es = 2 if w.dtype == "bf16" else 4
+    B_, D_, N_ = w.batch, w.dim, w.dstate
+    act = (3 if w.gate else 2) * B_ * D_ * es
+    return {"elements": B_ * D_,
+            "bytes": 2 * B_ * D_ * N_ * 4 + act + 2 * B_ * N_ * es + D_ * N_ * 4 + D_ * 4
+                     + B_ * D_ * es}
+
+
+def decode_main(args):
+    """One decode step per timed step, on device buffers; the state stays resident."""
+    import torch
+    import selective_state_space_fwd_gb300 as S
+    from selective_state_space_fwd_gb300 import build as B
+    from selective_state_space_fwd_gb300 import workloads as W
+    rank, world, local = dist_env()
+    w = W.DECODE_WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            decode_reference(args, w)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    S.load()
+    inp = W.make_inputs(w)
+    t = W.to_torch(inp, dev)
+    flat = {k: (t[k].reshape(w.batch, -1) if t[k] is not None else None)
+            for k in ("x", "delta", "B", "C", "z")}
+    state = torch.from_numpy(W.make_state(w)).to(dev)
+    y = torch.empty_like(flat["x"])
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        S.decode_step(flat["x"], flat["delta"], t["A"], flat["B"], flat["C"], t["D"], flat["z"],
+                      state=state, out=y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = sum(per_step) / K
+    c = decode_counts(w)
+    # end to end: the step's inputs from pinned host memory, y back, every step
+    th = {k: (v.reshape(w.batch, -1).cpu().pin_memory() if v is not None else None)
+          for k, v in flat.items()}
+    y_h = torch.empty(tuple(y.shape), dtype=y.dtype, pin_memory=True)
+    dbuf = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in th.items()}
+
+    def step_host():
+        with torch.cuda.stream(stream):
+            for k, v in th.items():
+                if v is not None:
+                    dbuf[k].copy_(v, non_blocking=True)
+            S.decode_step(dbuf["x"], dbuf["delta"], t["A"], dbuf["B"], dbuf["C"], t["D"],
+                          dbuf["z"], state=state, out=y, stream=stream)
+            y_h.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        step_host()
+    torch.cuda.synchronize(dev)
+    KE = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        step_host()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / KE
+    peaks, peaks_src = load_peaks()
+    achieved = c["bytes"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": c["elements"] / (ms * 1e-3), "unit": "updates/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "dim": w.dim, "dstate": w.dstate,
+                   "gate": w.gate, "state_bytes": w.batch * w.dim * w.dstate * 4,
+                   "l2": "flushed between steps (256 MiB memset outside the timed events)"
+                         if not args.no_flush else "not flushed"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks_src, "kernel": "decode",
+                     "algorithmic": {"bytes": c["bytes"]}},
+        "cpu_baseline": None if args.no_cpu_baseline else decode_cpu(w, args.cpu_seconds),
+        "e2e": {"value": c["elements"] / (ms_e2e * 1e-3), "unit": "updates/s",
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in th.values()
+                                          if v is not None),
+                "d2h_bytes_per_step": y_h.numel() * y_h.element_size(), "ms_per_step": ms_e2e},
+        "gpu_launches": K, "clocks": clk,
+        "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
+                        "max": max(per_step)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _decode_sample(w, rows):
+    """The first `rows` batch rows of a decode workload, as oracle inputs (seqlen 1)."""
+    from selective_state_space_fwd_gb300 import workloads as W
+    inp = W.make_inputs(w)
+    st = W.make_state(w)
+    cut = {k: (np.ascontiguousarray(inp[k][:rows]) if inp[k] is not None else None)
+           for k in ("x", "delta", "B", "C", "z")}
+    return cut, inp["A"], inp["D"], np.ascontiguousarray(st[:rows])
+
+
+def decode_cpu(w, seconds: float) -> dict:
+    """The oracle (one-step scan from the state) on a bounded row sample."""
+    from oracle import ref_scan
+    threads = os.cpu_count() or 1
+    rows = max(1, min(w.batch, 64))
+    s, A, D, st = _decode_sample(w, rows)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        ref_scan.scan_fwd(s["x"], s["delta"], A, s["B"], s["C"], D, s["z"], None, h0=st,
+                          want_final=True, threads=threads)
+        n += 1
+        if time.perf_counter() - t0 > min(seconds, 5.0):
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": rows * w.dim / dt, "unit": "updates/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of {w.batch} batch rows x {w.dim} channels, one step"}
+
+
+def decode_reference(args, w):
+    """The oracle as the reference arm of the decode measurement."""
+    cpu = decode_cpu(w, 150.0 / max(1, args.steps + args.warmup))
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": cpu["value"],
+            "unit": "updates/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name}, "cpu_baseline": cpu,
+            "e2e": {"value": cpu["value"], "unit": "updates/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.op == "decode":
+        decode_main(args)
+        return
     from selective_state_space_fwd_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -145,6 +145,28 @@ ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, 
                               const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                               const ssm_options* opts);
 
+/*
+ * ssm_decode_step -- advance the recurrence by one step on a carried state
+ * (token-by-token generation).  For every (b, d, n):
+ *   h[b,d,n] <- exp(delta[b,d] A[d,n]) h[b,d,n] + delta[b,d] B[b,n] x[b,d]
+ *   y[b,d]    = (sum_n C[b,n] h[b,d,n] + D[d] x[b,d]) * silu(z[b,d])
+ * ([P1] s1.1, s2.4, s3.3): the scan of one step starting from `state`, with
+ * the same fp32 arithmetic as ssm_scan_fwd, so that decoding a sequence step
+ * by step follows its scan (SSM chunk carry [P1] s3.1, [P2] s2.4).
+ *   x, delta, z : device, dtype `dtype`, [batch, dim] (z nullable: no gate).
+ *   B, C        : device, dtype `dtype`, [batch, dstate].
+ *   A           : device fp32 [dim, dstate], 16-byte aligned.  D: fp32 [dim] or NULL.
+ *   state       : device fp32 [batch, dim, dstate], 16-byte aligned; read and
+ *                 overwritten in place (typically the final state of a scan,
+ *                 ssm_scan_fwd_carry).
+ *   out_y       : device, dtype `dtype`, [batch, dim].
+ * Asynchronous on `stream`; argument errors return a status before launch.
+ */
+ssm_status ssm_decode_step(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, float* state,
+                           void* out_y, int64_t batch, int64_t dim, int64_t dstate,
+                           ssm_dtype dtype, cudaStream_t stream);
+
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional
  * tensors the call passes.  Writes the tier to *kernel and the launch grid

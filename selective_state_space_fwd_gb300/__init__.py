@@ -5,10 +5,11 @@ sm_103a kernels under csrc/).  This package is its Python binding plus the
 seeded synthetic workloads used by the benchmark and tests.
 """
 from ._binding import (Kernel, SsmError, Status, check_device_errors, chunk_count,
-                       declared_functions,
+                       decode_step, declared_functions,
                        host_workspace_bytes, kernel_name, load, plan, scan_fwd, scan_fwd_host,
                        status_string, version)
 
-__all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "declared_functions",
+__all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "decode_step",
+           "declared_functions",
            "host_workspace_bytes", "kernel_name", "load", "plan", "scan_fwd", "scan_fwd_host",
            "status_string", "version"]

@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
     lib.ssm_scan_fwd_carry.restype = I32
     lib.ssm_scan_fwd_carry.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
+    lib.ssm_decode_step.restype = I32
+    lib.ssm_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
     lib.ssm_scan_plan.restype = I32
     lib.ssm_scan_plan.argtypes = [SP, I32, I32, I32, I32, OP, ctypes.POINTER(I32),
                                   ctypes.POINTER(I64)]
@@ -311,3 +313,41 @@ def scan_fwd_host(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_le
     if st != 0:
         raise SsmError(st, "ssm_scan_fwd_host")
     return y, states
+
+
+def decode_step(x, delta, A, B, C, D=None, z=None, *, state, out=None, stream=None):
+    """One step of the recurrence on a carried state, in place (decode).
+
+    x, delta, z: [batch, dim]; B, C: [batch, dstate] (fp32 or bf16, all the
+    same dtype); A: fp32 [dim, dstate]; D: fp32 [dim]; state: fp32
+    [batch, dim, dstate], updated in place.  Returns y [batch, dim]."""
+    import torch
+    lib = load()
+    if x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev, dt = x.device, x.dtype
+    code = _dtype_code(dt)
+    batch, dim = x.shape
+    dstate = B.shape[-1]
+    _check(x, "x", (batch, dim), dt, dev)
+    _check(delta, "delta", (batch, dim), dt, dev)
+    _check(B, "B", (batch, dstate), dt, dev)
+    _check(C, "C", (batch, dstate), dt, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(state, "state", (batch, dim, dstate), torch.float32, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, dim), dt, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", (batch, dim), dt, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        st = lib.ssm_decode_step(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                 _ptr(z), _ptr(state), _ptr(y), batch, dim, dstate, int(code),
+                                 ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_decode_step")
+    return y

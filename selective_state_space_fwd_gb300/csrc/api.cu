@@ -439,4 +439,29 @@ ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, c
                            dtype, static_cast<char*>(workspace), l, stream);
 }
 
+ssm_status ssm_decode_step(const void* x, const void* delta, const float* A, const void* B,
+                           const void* C, const float* D, const void* z, float* state,
+                           void* out_y, int64_t batch, int64_t dim, int64_t dstate,
+                           ssm_dtype dtype, cudaStream_t stream) {
+  if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+  if (batch < 1 || dim < 1 || dstate < 1) return SSM_ERR_SHAPE;
+  if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
+  int64_t bd, bdn, dn;
+  const int64_t lim = int64_t(1) << 60;
+  if (!mul_ok(batch, dim, &bd) || !mul_ok(bd, dstate, &bdn) || !mul_ok(dim, dstate, &dn) ||
+      bdn > lim || dn > lim || bd * 16 > lim)
+    return SSM_ERR_SHAPE;
+  if (!x || !delta || !A || !B || !C || !state || !out_y) return SSM_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+      !aligned(out_y, es) || (z && !aligned(z, es)) || (D && !aligned(D, 4)) ||
+      !aligned(A, 16) || !aligned(state, 16))
+    return SSM_ERR_ALIGN;
+  ssm::DecodeParams p;
+  p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.state = state; p.y = out_y;
+  p.batch = batch; p.dim = dim; p.dstate = static_cast<int>(dstate);
+  return ssm::launch_decode(p, dtype == SSM_BF16, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 }  // extern "C"

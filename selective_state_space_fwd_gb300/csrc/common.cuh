@@ -37,6 +37,21 @@ struct ScanParams {
   int64_t len_offset;         // this call's first step within the caller's sequence
 };
 
+// Arguments of one decode step (the recurrence advanced by one step in place).
+struct DecodeParams {
+  const void* x;      // [B, D]
+  const void* delta;  // [B, D]
+  const float* A;     // [D, N]
+  const void* B;      // [B, N]
+  const void* C;      // [B, N]
+  const float* D;     // nullable, [D]
+  const void* z;      // nullable, [B, D]
+  float* state;       // [B, D, N], read and written
+  void* y;            // [B, D]
+  int64_t batch, dim;
+  int dstate;
+};
+
 // 2^v with the MUFU unit (PTX ex2.approx.ftz.f32: results below 2^-126 flush
 // to zero, which the method tolerates: a product of decays that underflows
 // only removes contributions already below fp32 resolution, [P1] s2.4).

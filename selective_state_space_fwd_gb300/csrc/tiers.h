@@ -31,6 +31,9 @@ bool warpscan_eligible(const ScanParams& p);
 int64_t warpscan_grid(const ScanParams& p);
 cudaError_t launch_warpscan(const ScanParams& p, bool bf16, cudaStream_t s);
 
+// Decode step: one step of the recurrence on a carried state, in place.
+cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
+
 // Sticky device error word of the tiers with bounded waits: read and clear.
 bool read_and_clear_device_errors(unsigned int* word);
 

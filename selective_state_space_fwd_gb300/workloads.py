@@ -38,7 +38,7 @@ import dataclasses
 import numpy as np
 
 # tensor ids of the per-tensor streams
-_X, _DELTA, _DTBIAS, _B, _C, _D, _Z, _VALID = range(8)
+_X, _DELTA, _DTBIAS, _B, _C, _D, _Z, _VALID, _STATE = range(9)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -78,6 +78,22 @@ WORKLOADS: dict[int, Workload] = {
     5: Workload(5, "long-fp32-b2-l32768-d2048-n64", 2, 32768, 2048, 64, "f32", "loguniform", "s4d",
                 "ones", False, None, 0, 4),
 }
+
+# Decode steps (one step of the recurrence on a carried state): the inputs of
+# one time step for every (batch row, channel), drawn like the scan workloads'
+# (seqlen 1), plus a state [batch, dim, dstate] ~ N(0, 1) in fp32.  The state
+# is larger than L2, as for a serving batch of 1024 sequences.
+DECODE_WORKLOADS = {
+    1: Workload(101, "decode-fp32-b1024-d2048-n16", 1024, 1, 2048, 16, "f32", "softplus",
+                "s4d_exp", "normal", False, None, 0, 11),
+    2: Workload(102, "decode-bf16-gated-b1024-d2048-n16", 1024, 1, 2048, 16, "bf16",
+                "softplus", "s4d_exp", "normal", True, None, 0, 12),
+}
+
+
+def make_state(w: Workload) -> np.ndarray:
+    """A carried state for decode workloads: fp32 [batch, dim, dstate] ~ N(0, 1)."""
+    return _normal(_rng(w.seed, _STATE), (w.batch, w.dim, w.dstate)).astype(np.float32)
 
 
 def _rng(seed: int, tensor: int) -> np.random.Generator:

@@ -7,7 +7,7 @@ import pytest
 
 from selective_state_space_fwd_gb300 import _binding as Bd
 
-EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_plan", "ssm_scan_fwd_host",
+EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_decode_step", "ssm_scan_plan", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
@@ -103,6 +103,31 @@ def _carry(h0=None, final=None, **kw):
 ])
 def test_carry_argument_errors_return_status(ssmlib, kw, status):
     assert _carry(**kw) == status
+
+
+def _decode(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, state=FAKE, y=FAKE,
+            batch=2, dim=4, dstate=16, dtype=0):
+    P = ctypes.c_void_p
+    return Bd.load().ssm_decode_step(P(x), P(delta), P(A), P(B), P(C), P(D), P(z), P(state),
+                                     P(y), batch, dim, dstate, dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), Bd.Status.ERR_NULL),
+    (dict(state=None), Bd.Status.ERR_NULL),
+    (dict(y=None), Bd.Status.ERR_NULL),
+    (dict(batch=0), Bd.Status.ERR_SHAPE),
+    (dict(dim=-3), Bd.Status.ERR_SHAPE),
+    (dict(dstate=3), Bd.Status.ERR_UNSUPPORTED),
+    (dict(dstate=128), Bd.Status.ERR_UNSUPPORTED),
+    (dict(dtype=5), Bd.Status.ERR_UNSUPPORTED),
+    (dict(state=FAKE + 8), Bd.Status.ERR_ALIGN),
+    (dict(A=FAKE + 4), Bd.Status.ERR_ALIGN),
+    (dict(x=FAKE + 1, dtype=1), Bd.Status.ERR_ALIGN),
+    (dict(batch=1 << 40, dim=1 << 30), Bd.Status.ERR_SHAPE),
+])
+def test_decode_argument_errors_return_status(ssmlib, kw, status):
+    assert _decode(**kw) == status
 
 
 def test_plan_serial_always_available(ssmlib):
