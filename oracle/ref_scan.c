@@ -26,7 +26,11 @@
  *   - The transition is diagonal: one scalar decay per (channel d, state n).
  *   - Bbar x is taken as delta * B * x (the pages name zero-order hold but
  *     write no formula for Bbar; delta * B is its first-order form).
- *   - delta arrives already positive (after softplus); it is not transformed.
+ *   - delta is used as given, unless the call asks for the fused step-size
+ *     preparation: then the step size is softplus(delta + dt_bias[d]) with
+ *     softplus(v) = ln(1 + e^v), optionally clipped to [delta_min, delta_max]
+ *     (the pages list softplus and lower/upper clipping of delta among the
+ *     fused steps and name a bias on delta; each part is optional).
  *   - The optional gate multiplies the whole output by silu(z) = z / (1+e^-z),
  *     after the D residual is added.
  *   - The state before the first step is h0 when given, else 0.  Steps
@@ -90,6 +94,16 @@ void ref_linear_recurrence(const double* a, const double* b, int64_t L, double h
 /* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
 static double ref_silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* softplus(v) = ln(1 + e^v), written as max(v, 0) + ln(1 + e^-|v|) so that
+ * e^v never overflows. */
+static double ref_softplus(double v) {
+#if REF_PLANT == 9
+  return exp(v); /* planted: exp in place of softplus */
+#else
+  return (v > 0.0 ? v : 0.0) + log1p(exp(-fabs(v)));
+#endif
+}
+
 /*
  * The selective-scan forward over all (b, d) channels.
  *
@@ -101,16 +115,19 @@ static double ref_silu(double z) { return z / (1.0 + exp(-z)); }
  * [batch, seqlen, dim] doubles.  states_out (NULL = not wanted, also when
  * chunk_len <= 0) receives [batch, ceil(seqlen/chunk_len), dim, dstate] doubles;
  * final_out (NULL = not wanted) receives the state after the last step,
- * [batch, dim, dstate] doubles.
+ * [batch, dim, dstate] doubles.  The fused step-size preparation: dt_bias
+ * ([dim] fp32, NULL = none) is added to delta, delta_softplus != 0 applies
+ * softplus to the sum, and delta_clamp != 0 then clips it to
+ * [delta_min, delta_max], before delta is used.
  * nthreads <= 0 lets OpenMP choose.  The (b, d) loop is parallel only for
  * speed: each channel is computed by exactly one thread, in program order.
  * Returns 0, or -1 on bad sizes or a failed allocation.
  */
-int ref_scan_fwd_h0(const void* x, const void* delta, const float* A, const void* B,
-                    const void* C, const float* D, const void* z, const int32_t* valid_len,
-                    const float* h0, double* y_out, double* states_out, double* final_out,
-                    int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t chunk_len,
-                    int dtype, int nthreads) {
+int ref_scan_fwd_full(const void* x, const void* delta, const float* dt_bias, int delta_softplus,
+                      int delta_clamp, double delta_min, double delta_max, const float* A, const void* B, const void* C, const float* D,
+                      const void* z, const int32_t* valid_len, const float* h0, double* y_out,
+                      double* states_out, double* final_out, int64_t batch, int64_t seqlen,
+                      int64_t dim, int64_t dstate, int64_t chunk_len, int dtype, int nthreads) {
   if (batch < 0 || seqlen < 0 || dim < 0 || dstate < 1) return -1;
   if (dtype != REF_F32 && dtype != REF_BF16) return -1;
   const int want_states = (states_out != NULL && chunk_len > 0);
@@ -141,7 +158,12 @@ int ref_scan_fwd_h0(const void* x, const void* delta, const float* A, const void
       const int64_t r = (b * seqlen + t) * dstate;  /* row (b, t, :) of B and C */
       double y = 0.0;
       if (t < Lv) {
-        const double dt = ref_load(delta, dtype, e);
+        double dt = ref_load(delta, dtype, e);
+#if REF_PLANT != 8
+        if (dt_bias) dt += (double)dt_bias[d]; /* delta + dt_bias[d] */
+#endif
+        if (delta_softplus) dt = ref_softplus(dt); /* the step size, > 0 */
+        if (delta_clamp) dt = dt < delta_min ? delta_min : (dt > delta_max ? delta_max : dt);
         const double xv = ref_load(x, dtype, e);
         double acc = 0.0;
         for (int64_t n = 0; n < dstate; ++n) {
@@ -189,6 +211,17 @@ int ref_scan_fwd_h0(const void* x, const void* delta, const float* A, const void
     free(h);
   }
   return failed ? -1 : 0;
+}
+
+/* The forward with delta used as given. */
+int ref_scan_fwd_h0(const void* x, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const int32_t* valid_len,
+                    const float* h0, double* y_out, double* states_out, double* final_out,
+                    int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate, int64_t chunk_len,
+                    int dtype, int nthreads) {
+  return ref_scan_fwd_full(x, delta, NULL, 0, 0, 0.0, 0.0, A, B, C, D, z, valid_len, h0, y_out,
+                           states_out,
+                           final_out, batch, seqlen, dim, dstate, chunk_len, dtype, nthreads);
 }
 
 /* The forward from a zero initial state (the call without h0). */

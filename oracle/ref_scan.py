@@ -48,6 +48,9 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ref_scan_fwd.restype = I32
     lib.ref_scan_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I32, I32]
+    lib.ref_scan_fwd_full.restype = I32
+    lib.ref_scan_fwd_full.argtypes = [P, P, P, I32, I32, ctypes.c_double, ctypes.c_double, P, P,
+                                      P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I32, I32]
     lib.ref_scan_fwd_h0.restype = I32
     lib.ref_scan_fwd_h0.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
                                     I32, I32]
@@ -83,12 +86,15 @@ def linear_recurrence(a, b, h0: float = 0.0, plant: int = 0) -> np.ndarray:
 
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int = 0,
-             threads: int = 0, plant: int = 0, h0=None, want_final: bool = False):
+             threads: int = 0, plant: int = 0, h0=None, want_final: bool = False,
+             dt_bias=None, delta_softplus: bool = False, delta_clamp=None):
     """Run the oracle.  Returns ``(y, states)``: y is float64 [batch, L, dim];
     states is float64 [batch, ceil(L/chunk_len), dim, dstate], or None when
     ``chunk_len`` is 0.  With ``h0`` (float32 [batch, dim, dstate]) the state
     starts there instead of at 0; with ``want_final`` the result is
-    ``(y, states, final)`` with the state after the last step."""
+    ``(y, states, final)`` with the state after the last step.  ``dt_bias``
+    (float32 [dim]) is added to delta, ``delta_softplus`` applies softplus to
+    the sum and ``delta_clamp`` = (lo, hi) clips it, before delta is used."""
     if x.dtype == np.float32:
         dtype = 0
     elif x.dtype == np.uint16:
@@ -111,6 +117,9 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int =
         raise ValueError("valid_len must be int32 [batch]")
     if h0 is not None and (h0.shape != (batch, dim, dstate) or h0.dtype != np.float32):
         raise ValueError("h0 must be float32 [batch, dim, dstate]")
+    if dt_bias is not None and (dt_bias.shape != (dim,) or dt_bias.dtype != np.float32):
+        raise ValueError("dt_bias must be float32 [dim]")
+    dt_bias = None if dt_bias is None else np.ascontiguousarray(dt_bias)
     arrs = [np.ascontiguousarray(t) if t is not None else None
             for t in (x, delta, A, B, C, D, z, valid_len, h0)]
     y = np.empty((batch, L, dim), dtype=np.float64)
@@ -118,9 +127,13 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int =
     if chunk_len > 0:
         states = np.empty((batch, (L + chunk_len - 1) // chunk_len, dim, dstate), dtype=np.float64)
     final = np.empty((batch, dim, dstate), dtype=np.float64) if want_final else None
-    rc = _load(plant).ref_scan_fwd_h0(*[_ptr(t) for t in arrs], _ptr(y), _ptr(states),
-                                      _ptr(final), batch, L, dim, dstate, int(chunk_len), dtype,
-                                      int(threads))
+    xa, da, Aa, Ba, Ca, Da, za, va, ha = arrs
+    lo, hi = delta_clamp if delta_clamp is not None else (0.0, 0.0)
+    rc = _load(plant).ref_scan_fwd_full(_ptr(xa), _ptr(da), _ptr(dt_bias), int(bool(delta_softplus)),
+                                        int(delta_clamp is not None), float(lo), float(hi),
+                                        _ptr(Aa), _ptr(Ba), _ptr(Ca), _ptr(Da), _ptr(za), _ptr(va),
+                                        _ptr(ha), _ptr(y), _ptr(states), _ptr(final), batch, L, dim,
+                                        dstate, int(chunk_len), dtype, int(threads))
     if rc != 0:
         raise RuntimeError("ref_scan_fwd failed")
     return (y, states, final) if want_final else (y, states)

@@ -354,8 +354,70 @@ def pin_initial_state_split(plant=0):
     assert abs(fs[0, 0, 0] - want) < 1e-12 and abs(ys[0, 0, 0] - want) < 1e-12
 
 
+def pin_softplus_closed_form(plant=0):
+    """Fused step-size preparation, closed form: raw delta = 0 and no bias give
+    the step softplus(0) = ln 2; with A = -1 the decay is exactly 1/2 and
+    b = ln 2, so h_t = 2 ln 2 (1 - 2^-t) (the a = 1/2 closed form scaled by
+    ln 2) and y_t = h_t with B = C = x = 1, D = 0."""
+    L = 8
+    one = np.ones((1, L, 1), np.float32)
+    y, _ = R.scan_fwd(one, np.zeros((1, L, 1), np.float32), -np.ones((1, 1), np.float32), one,
+                      one, np.zeros(1, np.float32), delta_softplus=True, plant=plant)
+    want = 2.0 * math.log(2.0) * (1.0 - 0.5 ** np.arange(1, L + 1))
+    np.testing.assert_allclose(y[0, :, 0], want, rtol=1e-12, atol=0)
+
+
+def pin_softplus_and_bias_library(plant=0):
+    """softplus(delta + dt_bias[d]) inside the oracle equals passing the step
+    size computed beforehand with numpy's logaddexp(0, v) = ln(e^0 + e^v) (a
+    library routine); the bias alone equals adding it beforehand.  The
+    precomputed steps are rounded to fp32 once: compared within 1e-6."""
+    rng = np.random.default_rng(31)
+    batch, L, dim, N = 2, 40, 5, 4
+    x, _, A, B, C, D, z = _rand_inputs(rng, batch, L, dim, N, gate=True)
+    raw = (0.5 * rng.standard_normal((batch, L, dim))).astype(np.float32)
+    bias = np.log(np.expm1(rng.uniform(1e-3, 1e-1, dim))).astype(np.float32)
+    y, _ = R.scan_fwd(x, raw, A, B, C, D, z, dt_bias=bias, delta_softplus=True, plant=plant)
+    pre = np.logaddexp(0.0, raw.astype(np.float64) + bias.astype(np.float64)).astype(np.float32)
+    y_pre, _ = R.scan_fwd(x, pre, A, B, C, D, z, plant=plant)
+    np.testing.assert_allclose(y, y_pre, rtol=1e-6, atol=1e-6 * np.max(np.abs(y_pre)))
+    pos = np.exp(rng.uniform(np.log(1e-2), np.log(0.5), (batch, L, dim))).astype(np.float32)
+    small = (0.1 * rng.uniform(0.0, 1.0, dim)).astype(np.float32)
+    y_b, _ = R.scan_fwd(x, pos, A, B, C, D, z, dt_bias=small, plant=plant)
+    y_b2, _ = R.scan_fwd(x, (pos.astype(np.float64) + small).astype(np.float32), A, B, C, D, z,
+                         plant=plant)
+    np.testing.assert_allclose(y_b, y_b2, rtol=1e-6, atol=1e-6 * np.max(np.abs(y_b2)))
+
+
+def pin_delta_clamp(plant=0):
+    """Clipping after softplus: with [lo, hi] = [c, c] every step size is c, so
+    the run equals one with delta = c given directly; with a wide interval the
+    clip changes nothing; a clip inside the range moves only the steps outside
+    it (compared with the steps clipped beforehand by numpy)."""
+    rng = np.random.default_rng(37)
+    batch, L, dim, N = 2, 30, 4, 4
+    x, _, A, B, C, D, z = _rand_inputs(rng, batch, L, dim, N, gate=True)
+    raw = rng.standard_normal((batch, L, dim)).astype(np.float32)
+    c = np.float32(0.125)
+    y_c, _ = R.scan_fwd(x, raw, A, B, C, D, z, delta_softplus=True,
+                        delta_clamp=(float(c), float(c)), plant=plant)
+    y_k, _ = R.scan_fwd(x, np.full_like(raw, c), A, B, C, D, z, plant=plant)
+    np.testing.assert_allclose(y_c, y_k, rtol=1e-12, atol=1e-12)
+    y_w, _ = R.scan_fwd(x, raw, A, B, C, D, z, delta_softplus=True, delta_clamp=(0.0, 1e30),
+                        plant=plant)
+    y_n, _ = R.scan_fwd(x, raw, A, B, C, D, z, delta_softplus=True, plant=plant)
+    np.testing.assert_array_equal(y_w, y_n)
+    lo, hi = 0.3, 0.9
+    y_m, _ = R.scan_fwd(x, raw, A, B, C, D, z, delta_softplus=True, delta_clamp=(lo, hi),
+                        plant=plant)
+    pre = np.clip(np.logaddexp(0.0, raw.astype(np.float64)), lo, hi).astype(np.float32)
+    y_p, _ = R.scan_fwd(x, pre, A, B, C, D, z, plant=plant)
+    np.testing.assert_allclose(y_m, y_p, rtol=1e-6, atol=1e-6 * np.max(np.abs(y_p)))
+
+
 ALL_PINS = [pin_closed_form_recurrence, pin_closed_form_forward, pin_combine_is_composition,
             pin_associativity_bruteforce, pin_recurrence_is_prefix_of_combines,
             pin_reverse_identity, pin_lti_convolution, pin_unrolled_sum_bruteforce,
             pin_d_residual, pin_gate, pin_masking, pin_chunk_states_and_carry,
-            pin_bf16_widening, pin_long_sequence_sane, pin_initial_state_split]
+            pin_bf16_widening, pin_long_sequence_sane, pin_initial_state_split,
+            pin_softplus_closed_form, pin_softplus_and_bias_library, pin_delta_clamp]
