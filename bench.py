@@ -189,6 +189,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--fused-delta", action="store_true",
+                    help="softplus workloads: pass the raw step inputs and dt_bias and let the "
+                         "kernel apply softplus(raw + dt_bias)")
     ap.add_argument("--op", default="scan", choices=["scan", "decode"],
                     help="scan: the forward (default); decode: one recurrence step on a "
                          "carried state (--workload picks a decode workload)")
@@ -453,8 +456,16 @@ def main():
     S.load()
 
     inp = W.make_inputs(w)
+    prep = {}
+    if args.fused_delta:
+        raw, bias = W.make_raw_delta(w)
+        inp["delta"] = raw
+        prep = {"dt_bias": torch.from_numpy(bias).to(dev), "delta_softplus": True}
     t = W.to_torch(inp, dev)
     counts = algorithmic_counts(w, inp)
+    if args.fused_delta:  # one exp and one log per valid (b, t, d)
+        counts["exps"] += 2 * counts["valid_elements"]
+        counts["bytes"] += w.dim * 4
     kernel, grid = S.plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
                           mask=w.mask is not None, chunk_len=w.chunk_len, kernel=args.kernel,
                           warps_per_block=args.warps_per_block,
@@ -471,7 +482,7 @@ def main():
                    chunk_len=w.chunk_len, out=y, out_states=states, kernel=args.kernel,
                    warps_per_block=args.warps_per_block,
                    states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane,
-                   stream=stream)
+                   stream=stream, **prep)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -581,6 +592,8 @@ def main():
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
                    "dstate": w.dstate, "gate": w.gate, "chunk_len": w.chunk_len,
                    "masked": w.mask is not None,
+                   "delta": "fused: softplus(raw + dt_bias) in the kernel" if args.fused_delta
+                            else "given (already positive)",
                    "l2": "flushed between steps (256 MiB memset outside the timed events)"
                          if not args.no_flush else "not flushed",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -130,6 +130,22 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A, con
                            const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                            const ssm_options* opts);
 
+/* The fused step-size preparation ([P1] s3.3: the fused kernel applies a bias,
+ * softplus and lower/upper clipping to delta before the discretisation).  For
+ * every (b, t, d), before delta is used:
+ *   v = delta[b,t,d] + (dt_bias ? dt_bias[d] : 0)
+ *   v = softplus ? ln(1 + e^v) : v
+ *   v = clamp ? min(max(v, lo), hi) : v
+ * Steps past valid_len stay the identity whatever the preparation gives.
+ * dt_bias: device fp32 [dim] or NULL.  softplus, clamp: 0 or 1; with clamp,
+ * lo <= hi is required. */
+typedef struct {
+  const float* dt_bias;
+  int32_t softplus;
+  int32_t clamp;
+  float lo, hi;
+} ssm_delta_prep;
+
 /* As ssm_scan_fwd_ex, continuing from a given state and returning the final one.
  *   h0              : device fp32 [batch, dim, dstate], the state before the first
  *                     step (NULL = zeros, [P1] s4.1).
@@ -144,6 +160,17 @@ ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, 
                               float* out_chunk_states, float* out_final_state,
                               const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                               const ssm_options* opts);
+
+/* The most general forward: ssm_scan_fwd_carry with the fused step-size
+ * preparation `prep` (NULL = delta used as given).  Under SSM_KERNEL_AUTO the
+ * STREAM tier runs it in its default launch shapes; forcing another STREAM
+ * shape with a preparation returns SSM_ERR_UNSUPPORTED. */
+ssm_status ssm_scan_fwd_prep(const void* x, const void* delta, const ssm_delta_prep* prep,
+                             const float* A, const void* B, const void* C, const float* D,
+                             const void* z, const int32_t* valid_len, const float* h0,
+                             void* out_y, float* out_chunk_states, float* out_final_state,
+                             const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
+                             const ssm_options* opts);
 
 /*
  * ssm_decode_step -- advance the recurrence by one step on a carried state
@@ -166,6 +193,13 @@ ssm_status ssm_decode_step(const void* x, const void* delta, const float* A, con
                            const void* C, const float* D, const void* z, float* state,
                            void* out_y, int64_t batch, int64_t dim, int64_t dstate,
                            ssm_dtype dtype, cudaStream_t stream);
+
+/* ssm_decode_step with the fused step-size preparation `prep` (NULL = none). */
+ssm_status ssm_decode_step_prep(const void* x, const void* delta, const ssm_delta_prep* prep,
+                                const float* A, const void* B, const void* C, const float* D,
+                                const void* z, float* state, void* out_y, int64_t batch,
+                                int64_t dim, int64_t dstate, ssm_dtype dtype,
+                                cudaStream_t stream);
 
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional

@@ -59,6 +59,24 @@ class Options(ctypes.Structure):
 _lib = None
 
 
+class DeltaPrep(ctypes.Structure):
+    """ssm_delta_prep: the fused step-size preparation."""
+    _fields_ = [("dt_bias", ctypes.c_void_p), ("softplus", ctypes.c_int32),
+                ("clamp", ctypes.c_int32), ("lo", ctypes.c_float), ("hi", ctypes.c_float)]
+
+
+def _prep(dt_bias, delta_softplus, delta_clamp, dim, dev):
+    """A DeltaPrep for the keyword arguments, or None when nothing is asked."""
+    if dt_bias is None and not delta_softplus and delta_clamp is None:
+        return None
+    import torch
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", (dim,), torch.float32, dev)
+    lo, hi = delta_clamp if delta_clamp is not None else (0.0, 0.0)
+    return DeltaPrep(_ptr(dt_bias).value if dt_bias is not None else None,
+                     int(bool(delta_softplus)), int(delta_clamp is not None), float(lo), float(hi))
+
+
 def load() -> ctypes.CDLL:
     """Load libssmscan.so (built in-tree by ``selective_state_space_fwd_gb300.build``)."""
     global _lib
@@ -76,6 +94,11 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
     lib.ssm_scan_fwd_carry.restype = I32
     lib.ssm_scan_fwd_carry.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
+    DP = ctypes.POINTER(DeltaPrep)
+    lib.ssm_scan_fwd_prep.restype = I32
+    lib.ssm_scan_fwd_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
+    lib.ssm_decode_step_prep.restype = I32
+    lib.ssm_decode_step_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
     lib.ssm_decode_step.restype = I32
     lib.ssm_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
     lib.ssm_scan_plan.restype = I32
@@ -185,7 +208,8 @@ def _check(t, name, shape, dtype, device):
 def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
              out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO,
              warps_per_block: int = 0, states_per_lane: int = 0, channels_per_lane: int = 0,
-             stream=None, h0=None, want_final: bool = False, out_final=None):
+             stream=None, h0=None, want_final: bool = False, out_final=None, dt_bias=None,
+             delta_softplus: bool = False, delta_clamp=None):
     """The fused selective-scan forward on CUDA tensors.
 
     x, delta, z: [batch, L, dim]; B, C: [batch, L, dstate] (fp32 or bf16, all the
@@ -194,7 +218,9 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
     [batch, ceil(L/chunk_len), dim, dstate] (None when chunk_len == 0).
     ``h0`` (fp32 [batch, dim, dstate]) is the state before the first step
     (zeros when None); with ``want_final`` the result is ``(y, states, final)``,
-    final being the fp32 state after the last step.
+    final being the fp32 state after the last step.  ``dt_bias`` (fp32 [dim]),
+    ``delta_softplus`` and ``delta_clamp`` = (lo, hi) ask for the fused
+    step-size preparation of delta.
     Runs on ``stream`` (default: the current PyTorch stream of x's device).
     """
     import torch
@@ -237,8 +263,14 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    prep = _prep(dt_bias, delta_softplus, delta_clamp, dim, dev)
     with torch.cuda.device(dev):
-        if h0 is None and final is None:
+        if prep is not None:
+            st = lib.ssm_scan_fwd_prep(_ptr(x), _ptr(delta), ctypes.byref(prep), _ptr(A), _ptr(B),
+                                       _ptr(C), _ptr(D), _ptr(z), _ptr(valid_len), _ptr(h0),
+                                       _ptr(y), _ptr(states), _ptr(final), ctypes.byref(s),
+                                       int(code), ctypes.c_void_p(handle), ctypes.byref(o))
+        elif h0 is None and final is None:
             st = lib.ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
                                      _ptr(z), _ptr(valid_len), _ptr(y), _ptr(states),
                                      ctypes.byref(s), int(code), ctypes.c_void_p(handle),
@@ -249,7 +281,8 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
                                         _ptr(states), _ptr(final), ctypes.byref(s), int(code),
                                         ctypes.c_void_p(handle), ctypes.byref(o))
     if st != 0:
-        raise SsmError(st, "ssm_scan_fwd_carry" if final is not None or h0 is not None
+        raise SsmError(st, "ssm_scan_fwd_prep" if prep is not None else
+                       "ssm_scan_fwd_carry" if final is not None or h0 is not None
                        else "ssm_scan_fwd")
     if want_final or out_final is not None:
         return y, states, final
@@ -315,12 +348,14 @@ def scan_fwd_host(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_le
     return y, states
 
 
-def decode_step(x, delta, A, B, C, D=None, z=None, *, state, out=None, stream=None):
+def decode_step(x, delta, A, B, C, D=None, z=None, *, state, out=None, stream=None,
+                dt_bias=None, delta_softplus: bool = False, delta_clamp=None):
     """One step of the recurrence on a carried state, in place (decode).
 
     x, delta, z: [batch, dim]; B, C: [batch, dstate] (fp32 or bf16, all the
     same dtype); A: fp32 [dim, dstate]; D: fp32 [dim]; state: fp32
-    [batch, dim, dstate], updated in place.  Returns y [batch, dim]."""
+    [batch, dim, dstate], updated in place.  Returns y [batch, dim].  The
+    step-size preparation arguments are those of scan_fwd."""
     import torch
     lib = load()
     if x.device.type != "cuda":
@@ -344,10 +379,12 @@ def decode_step(x, delta, A, B, C, D=None, z=None, *, state, out=None, stream=No
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    prep = _prep(dt_bias, delta_softplus, delta_clamp, dim, dev)
     with torch.cuda.device(dev):
-        st = lib.ssm_decode_step(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                 _ptr(z), _ptr(state), _ptr(y), batch, dim, dstate, int(code),
-                                 ctypes.c_void_p(handle))
+        st = lib.ssm_decode_step_prep(_ptr(x), _ptr(delta),
+                                      ctypes.byref(prep) if prep is not None else None, _ptr(A),
+                                      _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(state), _ptr(y),
+                                      batch, dim, dstate, int(code), ctypes.c_void_p(handle))
     if st != 0:
         raise SsmError(st, "ssm_decode_step")
     return y

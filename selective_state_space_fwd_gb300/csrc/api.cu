@@ -117,7 +117,28 @@ ScanParams make_params(const void* x, const void* delta, const float* A, const v
   p.chunk_len = st ? s->chunk_len : 1;
   p.n_chunks = st ? (s->seqlen + s->chunk_len - 1) / s->chunk_len : 0;
   p.len_offset = 0;
+  p.dt_bias = nullptr;
+  p.delta_softplus = 0;
+  p.delta_clamp = 0;
+  p.delta_lo = 0.f;
+  p.delta_hi = 0.f;
   return p;
+}
+
+// Validates and applies the fused step-size preparation to the kernel parameters.
+template <class P>
+ssm_status apply_prep(const ssm_delta_prep* prep, P* p) {
+  if (prep == nullptr) return SSM_OK;
+  if (prep->dt_bias && !aligned(prep->dt_bias, 4)) return SSM_ERR_ALIGN;
+  if ((prep->softplus != 0 && prep->softplus != 1) || (prep->clamp != 0 && prep->clamp != 1))
+    return SSM_ERR_UNSUPPORTED;
+  if (prep->clamp && !(prep->lo <= prep->hi)) return SSM_ERR_SHAPE;  // also rejects NaN
+  p->dt_bias = prep->dt_bias;
+  p->delta_softplus = prep->softplus;
+  p->delta_clamp = prep->clamp;
+  p->delta_lo = prep->lo;
+  p->delta_hi = prep->hi;
+  return SSM_OK;
 }
 
 // Launch the planned tier.
@@ -392,6 +413,16 @@ ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, 
                               float* out_chunk_states, float* out_final_state,
                               const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
                               const ssm_options* opts) {
+  return ssm_scan_fwd_prep(x, delta, nullptr, A, B, C, D, z, valid_len, h0, out_y,
+                           out_chunk_states, out_final_state, shapes, dtype, stream, opts);
+}
+
+ssm_status ssm_scan_fwd_prep(const void* x, const void* delta, const ssm_delta_prep* prep,
+                             const float* A, const void* B, const void* C, const float* D,
+                             const void* z, const int32_t* valid_len, const float* h0,
+                             void* out_y, float* out_chunk_states, float* out_final_state,
+                             const ssm_shapes* shapes, ssm_dtype dtype, cudaStream_t stream,
+                             const ssm_options* opts) {
   ssm_status st = check_shapes(shapes, dtype, out_chunk_states != nullptr);
   if (st != SSM_OK) return st;
   if ((st = check_options(opts)) != SSM_OK) return st;
@@ -403,8 +434,9 @@ ssm_status ssm_scan_fwd_carry(const void* x, const void* delta, const float* A, 
       (h0 && !aligned(h0, 4)) || (out_final_state && !aligned(out_final_state, 4)))
     return SSM_ERR_ALIGN;
 
-  const ScanParams p = make_params(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states,
-                                   shapes, h0, out_final_state);
+  ScanParams p = make_params(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states, shapes,
+                             h0, out_final_state);
+  if ((st = apply_prep(prep, &p)) != SSM_OK) return st;
   return launch(p, dtype, opts, stream);
 }
 
@@ -443,6 +475,15 @@ ssm_status ssm_decode_step(const void* x, const void* delta, const float* A, con
                            const void* C, const float* D, const void* z, float* state,
                            void* out_y, int64_t batch, int64_t dim, int64_t dstate,
                            ssm_dtype dtype, cudaStream_t stream) {
+  return ssm_decode_step_prep(x, delta, nullptr, A, B, C, D, z, state, out_y, batch, dim, dstate,
+                              dtype, stream);
+}
+
+ssm_status ssm_decode_step_prep(const void* x, const void* delta, const ssm_delta_prep* prep,
+                                const float* A, const void* B, const void* C, const float* D,
+                                const void* z, float* state, void* out_y, int64_t batch,
+                                int64_t dim, int64_t dstate, ssm_dtype dtype,
+                                cudaStream_t stream) {
   if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
   if (batch < 1 || dim < 1 || dstate < 1) return SSM_ERR_SHAPE;
   if (!supported_dstate(dstate)) return SSM_ERR_UNSUPPORTED;
@@ -461,6 +502,9 @@ ssm_status ssm_decode_step(const void* x, const void* delta, const float* A, con
   p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
   p.state = state; p.y = out_y;
   p.batch = batch; p.dim = dim; p.dstate = static_cast<int>(dstate);
+  p.dt_bias = nullptr; p.delta_softplus = 0; p.delta_clamp = 0; p.delta_lo = 0.f; p.delta_hi = 0.f;
+  const ssm_status st = apply_prep(prep, &p);
+  if (st != SSM_OK) return st;
   return ssm::launch_decode(p, dtype == SSM_BF16, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

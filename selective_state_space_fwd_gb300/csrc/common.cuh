@@ -35,7 +35,16 @@ struct ScanParams {
   int64_t chunk_len;          // > 0 when states != nullptr
   int64_t n_chunks;
   int64_t len_offset;         // this call's first step within the caller's sequence
+  // fused step-size preparation: delta <- clip(softplus(delta + dt_bias[d]))
+  const float* dt_bias;       // nullable, [D]
+  int delta_softplus;         // 0 / 1
+  int delta_clamp;            // 0 / 1: clip to [delta_lo, delta_hi]
+  float delta_lo, delta_hi;
 };
+
+__host__ __device__ inline bool has_delta_prep(const ScanParams& p) {
+  return p.dt_bias != nullptr || p.delta_softplus || p.delta_clamp;
+}
 
 // Arguments of one decode step (the recurrence advanced by one step in place).
 struct DecodeParams {
@@ -50,6 +59,9 @@ struct DecodeParams {
   void* y;            // [B, D]
   int64_t batch, dim;
   int dstate;
+  const float* dt_bias;  // fused step-size preparation, as in ScanParams
+  int delta_softplus, delta_clamp;
+  float delta_lo, delta_hi;
 };
 
 // 2^v with the MUFU unit (PTX ex2.approx.ftz.f32: results below 2^-126 flush
@@ -63,6 +75,45 @@ __device__ __forceinline__ float ex2(float v) {
 
 // silu(v) = v * sigmoid(v) = v / (1 + e^-v), the optional output gate.
 __device__ __forceinline__ float silu(float v) { return __fdividef(v, 1.0f + ex2(-v * kLog2e)); }
+
+// softplus(v) = ln(1 + e^v) = max(v, 0) + ln(1 + e^-|v|).  With e = e^-|v| in
+// (0, 1], ln(1 + e) = 2 atanh(s) for s = e / (2 + e) in (0, 1/3], and
+// atanh(s) = s (1 + s^2/3 + s^4/5 + ...): six terms leave a relative
+// truncation error below s^12/13 < 2e-7, and the series keeps full relative
+// precision where ln(1 + e) is small (e^v for very negative v; the method's
+// step sizes are often 1e-3 .. 1e-1), unlike a logarithm of the rounded sum
+// 1 + e.
+__device__ __forceinline__ float softplus_f(float v) {
+  const float e = ex2(-fabsf(v) * kLog2e);  // e^-|v|
+  const float sv = __fdividef(e, 2.0f + e);
+  const float s2 = sv * sv;
+  float t = 1.0f / 11.0f;
+  t = fmaf(t, s2, 1.0f / 9.0f);
+  t = fmaf(t, s2, 1.0f / 7.0f);
+  t = fmaf(t, s2, 1.0f / 5.0f);
+  t = fmaf(t, s2, 1.0f / 3.0f);
+  t = fmaf(t, s2, 1.0f);
+  return fmaxf(v, 0.0f) + 2.0f * sv * t;
+}
+
+// The fused step-size preparation of one delta value ([P1] s3.3: bias,
+// softplus, lower/upper clipping); `bias` is the value of the channel's bias
+// (0 without one), loaded once by the caller.
+__device__ __forceinline__ float prep_delta(float v, float bias, int softplus, int clamp, float lo,
+                                            float hi) {
+  v += bias;
+  const float sp = softplus_f(v);  // selects, not branches: callers run many in a row
+  v = softplus ? sp : v;
+  const float cl = fminf(fmaxf(v, lo), hi);
+  return clamp ? cl : v;
+}
+__device__ __forceinline__ float prep_delta(float v, float bias, const ScanParams& p) {
+  return prep_delta(v, bias, p.delta_softplus, p.delta_clamp, p.delta_lo, p.delta_hi);
+}
+// The bias of channel d (0 without one).
+__device__ __forceinline__ float delta_bias(const float* bias, int64_t d) {
+  return bias ? __ldg(bias + d) : 0.f;
+}
 
 // Element access for the two I/O types.  bf16 widens exactly to fp32; stores
 // round to nearest even.

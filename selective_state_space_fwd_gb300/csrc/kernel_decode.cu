@@ -55,7 +55,10 @@ __global__ void __launch_bounds__(256) decode_kernel(const DecodeParams p) {
 
   float acc = 0.f, xv = 0.f;
   if (ok) {
-    const float dt = IO<T>::load(p.delta, bd);
+    float dt = IO<T>::load(p.delta, bd);
+    if (p.dt_bias || p.delta_softplus || p.delta_clamp)  // bias, softplus, clipping
+      dt = prep_delta(dt, delta_bias(p.dt_bias, d), p.delta_softplus, p.delta_clamp, p.delta_lo,
+                      p.delta_hi);
     xv = IO<T>::load(p.x, bd);
     const float ux = dt * xv;  // delta x
     float a[G], h[G];

@@ -27,13 +27,16 @@ __global__ void __launch_bounds__(128) serial_kernel(const ScanParams p) {
     h[n] = p.h0 ? __ldg(p.h0 + bd * N + n) : 0.0f;  // [P1] s4.1: h_0 = 0 unless given
   }
   const float dskip = p.D ? __ldg(p.D + d) : 0.0f;
+  const bool prep = has_delta_prep(p);
+  const float dbias = delta_bias(p.dt_bias, d);
   const int64_t lv = valid_steps(p, b);
 
   for (int64_t t = 0; t < p.seqlen; ++t) {
     const int64_t e = (b * p.seqlen + t) * p.dim + d;
     float yv = 0.0f;  // exact zero past the valid length
     if (t < lv) {
-      const float dt = IO<T>::load(p.delta, e);
+      float dt = IO<T>::load(p.delta, e);
+      if (prep) dt = prep_delta(dt, dbias, p);  // bias, softplus, clipping
       const float xv = IO<T>::load(p.x, e);
       const float u = dt * xv;
       const int64_t r = (b * p.seqlen + t) * N;

@@ -140,6 +140,7 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
     if (r == 0) r = dr;
   }
   if (g == 0 || r == 0 || !has_instance(p.dstate, g, r)) return sh;
+  if (has_delta_prep(p) && !dtp_shape(p.dstate, g, r)) return sh;  // not compiled with it
   const int cw = channels_per_warp(p.dstate, g, r);
   const int sms = sm_count();
   const int64_t smem_sm = 228 * 1024;  // shared memory per SM
@@ -153,7 +154,9 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
     const int64_t cap = 16 / w;  // about 16 warps per SM by registers
     if (per_sm > cap) per_sm = cap;
     *per_sm_out = per_sm;
-    const int fixed = w * partial_bytes(p.dstate, g, r) + 64;  // partial-sum buffers, barriers
+    // per-warp partial-sum buffers (and fp32 delta slabs), barriers
+    const int dsf = (bf16 && has_delta_prep(p)) ? 64 * cw * 4 : 0;
+    const int fixed = w * (partial_bytes(p.dstate, g, r) + dsf) + 64;
     int st = static_cast<int>((smem_sm / per_sm - 1024 - fixed) / sb);
     if (st > 4) st = 4;
     if (st * sb + fixed > max_dynamic_smem()) st = (max_dynamic_smem() - fixed) / sb;
@@ -165,7 +168,9 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
     stages = stages_for(w, &per_sm);
     if (stages == 0) {  // the caller's W: two slots, even if not every CTA is resident
       const int sb = stage_bytes_of(p.dstate, g, r, bf16, p.z != nullptr, w);
-      if (sb <= 0 || 2 * sb + w * partial_bytes(p.dstate, g, r) + 64 > max_dynamic_smem()) return sh;
+      const int dsf = (bf16 && has_delta_prep(p)) ? 64 * cw * 4 : 0;
+      if (sb <= 0 || 2 * sb + w * (partial_bytes(p.dstate, g, r) + dsf) + 64 > max_dynamic_smem())
+        return sh;
       stages = 2;
     }
   } else {  // the fewest warps per CTA for which all CTAs are resident at once
@@ -177,7 +182,9 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
       w = 4;
       stages = 2;
       const int sb = stage_bytes_of(p.dstate, g, r, bf16, p.z != nullptr, w);
-      if (sb <= 0 || 2 * sb + w * partial_bytes(p.dstate, g, r) + 64 > max_dynamic_smem()) return sh;
+      const int dsf = (bf16 && has_delta_prep(p)) ? 64 * cw * 4 : 0;
+      if (sb <= 0 || 2 * sb + w * (partial_bytes(p.dstate, g, r) + dsf) + 64 > max_dynamic_smem())
+        return sh;
     }
   }
   sh.wpc = w;

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
   const int64_t L = p.seqlen;
   const int64_t lv = valid_steps(p, b);
   const float dskip = (d_ok && p.D) ? __ldg(p.D + d) : 0.f;
+  const float dbias = d_ok ? delta_bias(p.dt_bias, d) : 0.f;
   const bool want_states = p.states != nullptr;
   const int row0 = lane * K;
 
@@ -229,6 +230,11 @@ __global__ void __launch_bounds__(kWarps * 32) warpscan_kernel(const ScanParams 
       float dt[K], xv[K];
       load_run<K>(ds + warp * W, lane, dt);
       load_run<K>(xs + warp * W, lane, xv);
+      if (has_delta_prep(p)) {  // bias, softplus, clipping; padded steps stay 0
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+          if (row0 + j < nv) dt[j] = prep_delta(dt[j], dbias, p);
+      }
       u64 dd[K], uu[K], y2[K];
 #pragma unroll
       for (int j = 0; j < K; ++j) {

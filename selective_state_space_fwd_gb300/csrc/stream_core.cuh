@@ -277,10 +277,14 @@ constexpr int pad_prow(int NG, int CW, int R, int PS) {
 }
 
 // Compile-time shape of one STREAM instance.
-template <int N_, int G_, int R_, typename IO_, bool GATE_>
+template <int N_, int G_, int R_, typename IO_, bool GATE_, bool DTP_ = false>
 struct Cfg {
   static constexpr int N = N_, G = G_, R = R_;
   static constexpr bool GATE = GATE_;
+  // DTP: the fused step-size preparation (bias, softplus, clipping) runs once
+  // per tile over the warp's delta slab; for fp32 in place, for bf16 into an
+  // fp32 slab of the warp (the prepared step is not rounded to bf16).
+  static constexpr bool DTP = DTP_;
   using IO = IO_;
   static constexpr int PR = R / 2;           // channel pairs per lane
   static constexpr int NG = N / G;           // lanes per channel group
@@ -299,6 +303,9 @@ struct Cfg {
   static constexpr int PS = pad_ps(NG, CW, R);
   static constexpr int PROW = pad_prow(NG, CW, R, PS);
   static constexpr int PBYTES = M * PROW * 4;
+  static constexpr bool DSF = DTP && ES == 2;          // the fp32 delta slab exists
+  static constexpr int DSFBYTES = DSF ? T * CW * 4 : 0;
+  using DT = typename std::conditional<DSF, float, IO>::type;  // delta as the lanes read it
   static constexpr int NACT = GATE ? 3 : 2;    // activation tensors per tile
   // A lane's slice of a B or C row is MCH 16-byte chunks of CHUNK elements.
   // The lanes of one access phase start their slices 16 * MCH bytes apart, so
@@ -324,13 +331,13 @@ struct Raw {
 };
 
 template <class K>
-__device__ __forceinline__ void load_batch(Raw<K>& r, const typename K::IO* ds,
+__device__ __forceinline__ void load_batch(Raw<K>& r, const typename K::DT* ds,
                                            const typename K::IO* xs, const typename K::IO* bs,
                                            const typename K::IO* cs, int s, const int* coff) {
   using TL = Tile<typename K::IO>;
 #pragma unroll
   for (int u = 0; u < K::U; ++u) {
-    TL::template pairs<K::PR>(ds + (s + u) * K::CW, r.dt[u]);
+    Tile<typename K::DT>::template pairs<K::PR>(ds + (s + u) * K::CW, r.dt[u]);
     TL::template pairs<K::PR>(xs + (s + u) * K::CW, r.x[u]);
     TL::template row<K::G>(bs + (s + u) * K::N, r.b[u], coff);
     TL::template row<K::G>(cs + (s + u) * K::N, r.c[u], coff);
@@ -388,7 +395,10 @@ __global__ void __launch_bounds__(128, 1)
   const int W = la.warps, STAGES = la.stages, SB = la.stage_bytes;
   // this warp's partial-sum buffer, after the ring
   float* pbuf = reinterpret_cast<float*>(smem + STAGES * SB + (threadIdx.x >> 5) * K::PBYTES);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * SB + W * K::PBYTES);
+  float* dsf = reinterpret_cast<float*>(smem + STAGES * SB + W * K::PBYTES +
+                                        (threadIdx.x >> 5) * K::DSFBYTES);  // fp32 delta slab
+  uint64_t* full =
+      reinterpret_cast<uint64_t*>(smem + STAGES * SB + W * (K::PBYTES + K::DSFBYTES));
   uint64_t* empty = full + STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -467,6 +477,15 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
 
+  // Bias of the channels this lane prepares step sizes for (element e of the
+  // warp's slab belongs to channel e % CW; lane l visits e = l + 32 k).
+  constexpr int NBV = CW > 32 ? CW / 32 : 1;
+  float dbias[NBV];
+#pragma unroll
+  for (int i = 0; i < NBV; ++i) {
+    const int c = (lane + 32 * i) % CW;
+    dbias[i] = (K::DTP && dw + c < p.dim) ? delta_bias(p.dt_bias, dw + c) : 0.f;
+  }
   // The epilogue's view of the warp: lane (cp, sl) finishes the outputs of
   // channels dw + cp R .. + R at steps sl, sl + NG, ... of each block.
   const int cp = lane % CG, sl = lane / CG;
@@ -522,12 +541,48 @@ __global__ void __launch_bounds__(128, 1)
     const IO* xw = reinterpret_cast<const IO*>(st + (0 * W + warp) * K::SLAB);  // warp's slabs
     const IO* zw = reinterpret_cast<const IO*>(st + (2 * W + warp) * K::SLAB);
     const IO* xs = xw + cg * R;  // this lane's channels
-    const IO* ds = reinterpret_cast<const IO*>(st + (1 * W + warp) * K::SLAB) + cg * R;
+    IO* dslab = reinterpret_cast<IO*>(st + (1 * W + warp) * K::SLAB);  // warp's delta slab
+    const typename K::DT* ds;  // this lane's delta column, as the recurrence reads it
     const IO* bs = reinterpret_cast<const IO*>(st + K::NACT * W * K::SLAB) + sg * G;
     const IO* cs = bs + T * N;
     const int64_t t0 = static_cast<int64_t>(i) * T;
     const int steps = static_cast<int>(lv - t0 < T ? lv - t0 : T);  // valid steps in tile
     IO* ybase = yout + (b * L + t0) * p.dim + de;                    // y[b, t0, de]
+    if constexpr (K::DTP) {
+      // The step size of every (step, channel) of the warp, prepared once:
+      // delta + dt_bias[d], softplus, clipping ([P1] s3.3).  Rows past the
+      // valid steps and channels past dim become 0 (identity steps).
+      typename K::DT* dst;
+      if constexpr (K::DSF) dst = dsf;
+      else dst = dslab;
+      // groups of 8 elements per lane: loads, then arithmetic, then stores, so
+      // that the in-place update of fp32 slabs does not serialise the loads
+      constexpr int PER = T * CW / 32, GRP = 8;
+      static_assert(PER % GRP == 0, "delta preparation groups");
+#pragma unroll
+      for (int g0 = 0; g0 < PER; g0 += GRP) {
+        float v[GRP];
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) {
+          const int e = lane + 32 * (g0 + k);
+          if constexpr (K::ES == 2) v[k] = __bfloat162float(dslab[e]);
+          else v[k] = dslab[e];
+        }
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) {
+          const int e = lane + 32 * (g0 + k);
+          const int row = e / CW, c = e % CW;
+          const float pv = prep_delta(v[k], dbias[(g0 + k) % NBV], p);
+          v[k] = (row < steps && dw + c < p.dim) ? pv : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < GRP; ++k) dst[lane + 32 * (g0 + k)] = typename K::DT(v[k]);
+      }
+      ds = dst + cg * R;
+      __syncwarp();
+    } else {
+      ds = dslab + cg * R;
+    }
     if (steps < T) {
       // Steps of the tile past valid_len become the identity (a = 1, b = 0,
       // [P1] s2.3): their delta, x, B and C are set to zero in the tile, so
@@ -535,7 +590,7 @@ __global__ void __launch_bounds__(128, 1)
       // The B and C rows are shared by the CTA's warps: each warp zeroes them
       // itself (every writer stores the same zeros, and a warp reads them only
       // after its own pass), so no CTA-wide barrier is needed.
-      IO* dsw = const_cast<IO*>(reinterpret_cast<const IO*>(st + (1 * W + warp) * K::SLAB));
+      IO* dsw = dslab;
       IO* xsw = const_cast<IO*>(xw);
       for (int e = steps * CW + lane; e < T * CW; e += 32) {
         dsw[e] = IO(0.f);
@@ -723,7 +778,7 @@ cudaError_t launch_k(const ScanParams& p, cudaStream_t s, int warps, int stages)
   la.stage_bytes = stage_bytes<K>(warps);
   la.err = error_word();
   if (la.err == nullptr) return cudaErrorInvalidValue;
-  const int smem = stages * la.stage_bytes + warps * K::PBYTES + 2 * stages * 8;
+  const int smem = stages * la.stage_bytes + warps * (K::PBYTES + K::DSFBYTES) + 2 * stages * 8;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(stream_kernel<K>,
@@ -748,23 +803,46 @@ cudaError_t launch_ngr(const ScanParams& p, bool bf16, cudaStream_t s, int warps
 template <int N, int G, int R>
 int stage_bytes_ngr(bool bf16, bool gate, int warps);
 
+// bf16 instances exist when the B/C rows and a warp's activation rows are at
+// least 16-byte multiples (TMA boxes).
 template <int N, int G, int R>
-cudaError_t launch_ngr_impl(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
+constexpr bool bf16_ok() {
+  return N * 2 >= 16 && (32 / (N / G)) * R * 2 % 16 == 0;
+}
+
+template <int N, int G, int R, bool DTP>
+cudaError_t launch_ngr_dtp(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
   if (bf16) {
-    if constexpr (N * 2 >= 16)  // bf16 B/C rows of at least 16 bytes (TMA)
-      return p.z ? launch_k<Cfg<N, G, R, __nv_bfloat16, true>>(p, s, w, st)
-                 : launch_k<Cfg<N, G, R, __nv_bfloat16, false>>(p, s, w, st);
+    if constexpr (bf16_ok<N, G, R>())
+      return p.z ? launch_k<Cfg<N, G, R, __nv_bfloat16, true, DTP>>(p, s, w, st)
+                 : launch_k<Cfg<N, G, R, __nv_bfloat16, false, DTP>>(p, s, w, st);
     else
       return cudaErrorInvalidValue;
   }
-  return p.z ? launch_k<Cfg<N, G, R, float, true>>(p, s, w, st)
-             : launch_k<Cfg<N, G, R, float, false>>(p, s, w, st);
+  return p.z ? launch_k<Cfg<N, G, R, float, true, DTP>>(p, s, w, st)
+             : launch_k<Cfg<N, G, R, float, false, DTP>>(p, s, w, st);
+}
+
+// Shapes compiled with the fused step-size preparation: the default ones.
+constexpr bool dtp_shape(int n, int g, int r) {
+  return r == 2 && ((n <= 16 && g == 4) || (n >= 32 && g == 8));
+}
+
+template <int N, int G, int R>
+cudaError_t launch_ngr_impl(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
+  if (has_delta_prep(p)) {
+    if constexpr (dtp_shape(N, G, R))
+      return launch_ngr_dtp<N, G, R, true>(p, bf16, s, w, st);
+    else
+      return cudaErrorInvalidValue;
+  }
+  return launch_ngr_dtp<N, G, R, false>(p, bf16, s, w, st);
 }
 
 template <int N, int G, int R>
 int stage_bytes_impl(bool bf16, bool gate, int w) {
   if (bf16) {
-    if constexpr (N * 2 >= 16)
+    if constexpr (bf16_ok<N, G, R>())
       return gate ? stage_bytes<Cfg<N, G, R, __nv_bfloat16, true>>(w)
                   : stage_bytes<Cfg<N, G, R, __nv_bfloat16, false>>(w);
     else

@@ -1,4 +1,4 @@
-// STREAM instances for 32 and 64 states (kernel template in stream_core.cuh).
+// STREAM instances for 32 states (kernel template in stream_core.cuh).
 #include "stream_core.cuh"
 
 namespace ssm {
@@ -6,8 +6,5 @@ namespace stream {
 SSM_STREAM_DEFINE(32, 4, 4)
 SSM_STREAM_DEFINE(32, 8, 2)
 SSM_STREAM_DEFINE(32, 8, 4)
-SSM_STREAM_DEFINE(64, 8, 2)
-SSM_STREAM_DEFINE(64, 8, 4)
-SSM_STREAM_DEFINE(64, 16, 2)
 }  // namespace stream
 }  // namespace ssm

@@ -91,6 +91,28 @@ DECODE_WORKLOADS = {
 }
 
 
+def make_raw_delta(w: Workload):
+    """For the softplus recipe: the step inputs before the fused preparation,
+    raw = 0.5 N(0,1) [batch, L, dim] (I/O dtype) and dt_bias [dim] fp32, from
+    the same streams as make_inputs' delta, so that softplus(raw + dt_bias)
+    is that delta up to the rounding of raw and dt_bias."""
+    if w.delta != "softplus":
+        raise ValueError("only the softplus recipe has a raw form")
+    shape = (w.batch, w.seqlen, w.dim)
+    u = _rng(w.seed, _DTBIAS).uniform(1e-3, 1e-1, w.dim)
+    bias = np.log(np.expm1(u)).astype(np.float32)
+    rng = _rng(w.seed, _DELTA)
+    raw = np.empty(shape, dtype=np.float32)
+    r2 = raw.reshape(-1, w.dim)
+    rows_per_chunk = max(1, (1 << 22) // w.dim)
+    for r in range(0, r2.shape[0], rows_per_chunk):
+        n = min(rows_per_chunk, r2.shape[0] - r)
+        r2[r:r + n] = 0.5 * rng.standard_normal((n, w.dim))
+    if w.dtype == "bf16":
+        raw = f32_to_bf16_bits(raw)
+    return raw, bias
+
+
 def make_state(w: Workload) -> np.ndarray:
     """A carried state for decode workloads: fp32 [batch, dim, dstate] ~ N(0, 1)."""
     return _normal(_rng(w.seed, _STATE), (w.batch, w.dim, w.dstate)).astype(np.float32)

@@ -7,7 +7,8 @@ import pytest
 
 from selective_state_space_fwd_gb300 import _binding as Bd
 
-EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_decode_step", "ssm_scan_plan", "ssm_scan_fwd_host",
+EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_fwd_prep",
+            "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_plan", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
@@ -128,6 +129,27 @@ def _decode(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, state=FA
 ])
 def test_decode_argument_errors_return_status(ssmlib, kw, status):
     assert _decode(**kw) == status
+
+
+def _prep_call(prep):
+    lib = Bd.load()
+    s = Bd.Shapes(2, 8, 4, 16, 0)
+    o = Bd.Options(0, 0, 0, 0)
+    P = ctypes.c_void_p
+    return lib.ssm_scan_fwd_prep(P(FAKE), P(FAKE), ctypes.byref(prep), P(FAKE), P(FAKE), P(FAKE),
+                                 None, None, None, None, P(FAKE), None, None, ctypes.byref(s), 0,
+                                 None, ctypes.byref(o))
+
+
+@pytest.mark.parametrize("prep,status", [
+    (Bd.DeltaPrep(FAKE + 2, 0, 0, 0.0, 0.0), Bd.Status.ERR_ALIGN),
+    (Bd.DeltaPrep(None, 2, 0, 0.0, 0.0), Bd.Status.ERR_UNSUPPORTED),
+    (Bd.DeltaPrep(None, 1, 3, 0.0, 1.0), Bd.Status.ERR_UNSUPPORTED),
+    (Bd.DeltaPrep(None, 1, 1, 1.0, 0.5), Bd.Status.ERR_SHAPE),
+    (Bd.DeltaPrep(None, 1, 1, float("nan"), 0.5), Bd.Status.ERR_SHAPE),
+])
+def test_prep_argument_errors_return_status(ssmlib, prep, status):
+    assert _prep_call(prep) == status
 
 
 def test_plan_serial_always_available(ssmlib):
