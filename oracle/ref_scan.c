@@ -233,5 +233,147 @@ int ref_scan_fwd(const void* x, const void* delta, const float* A, const void* B
                          seqlen, dim, dstate, chunk_len, dtype, nthreads);
 }
 
+/* d silu(z) / dz = sigma(z) (1 + z (1 - sigma(z))). */
+static double ref_dsilu(double z) {
+  const double sg = 1.0 / (1.0 + exp(-z));
+  return sg * (1.0 + z * (1.0 - sg));
+}
+
+/*
+ * The backward of the forward above (delta used as given), for the loss
+ * l = sum_{b,t,d} dy[b,t,d] * y[b,t,d]: every gradient of l.  The reverse-mode
+ * derivation of the recurrence ([P1] s3.4: the backward replays the chunk
+ * boundary states; here every state of the channel is simply kept):
+ *   g_t = silu(z_t) (1 without gate), yp_t = sum_n C_tn h_tn + D x_t, y_t = yp_t g_t
+ *   dyp_t = dy_t g_t,  dz_t = dy_t yp_t silu'(z_t)
+ *   lambda_tn = C_tn dyp_t + a_{t+1,n} lambda_{t+1,n}   (the adjoint of h_t)
+ *   with a_t = exp(delta_t A_n), b_t = delta_t B_tn x_t:
+ *   d delta_t = sum_n lambda_tn (B_tn x_t + A_n a_tn h_{t-1,n})
+ *   d x_t     = sum_n lambda_tn delta_t B_tn + dyp_t D
+ *   d B_tn   += lambda_tn delta_t x_t        (summed over d)
+ *   d C_tn   += dyp_t h_tn                   (summed over d)
+ *   d A_n    += lambda_tn delta_t a_tn h_{t-1,n}   (summed over b, t)
+ *   d D      += dyp_t x_t                    (summed over b, t)
+ *   d h0_n    = a_{0,n} lambda_{0,n}
+ * Steps t >= valid_len contribute nothing (their output is the constant 0
+ * and their state update the identity).  dy is [batch, seqlen, dim] doubles;
+ * every output is doubles: dx, ddelta, dz [batch, seqlen, dim] (dz NULL
+ * without gate), dA [dim, dstate], dB, dC [batch, seqlen, dstate], dD [dim]
+ * (NULL = not wanted), dh0 [batch, dim, dstate] (NULL = not wanted).  The
+ * summed outputs are overwritten (zeroed first).  Returns 0 or -1.
+ */
+int ref_scan_bwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const int32_t* valid_len, const float* h0,
+                 const double* dy, double* dx, double* ddelta, double* dA, double* dB,
+                 double* dC, double* dD, double* dz, double* dh0, int64_t batch, int64_t seqlen,
+                 int64_t dim, int64_t dstate, int dtype, int nthreads) {
+  if (batch < 0 || seqlen < 0 || dim < 0 || dstate < 1) return -1;
+  if (dtype != REF_F32 && dtype != REF_BF16) return -1;
+  memset(dA, 0, (size_t)(dim * dstate) * sizeof(double));
+  memset(dB, 0, (size_t)(batch * seqlen * dstate) * sizeof(double));
+  memset(dC, 0, (size_t)(batch * seqlen * dstate) * sizeof(double));
+  if (dD) memset(dD, 0, (size_t)dim * sizeof(double));
+  const int64_t channels = batch * dim;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : failed)
+#endif
+  for (int64_t bd = 0; bd < channels; ++bd) {
+    const int64_t b = bd / dim, d = bd % dim;
+    /* hs[(t + 1) * dstate + n] = h_t, t = -1 .. L-1 */
+    double* hs = (double*)malloc((size_t)((seqlen + 1) * dstate) * sizeof(double));
+    double* lam = (double*)malloc((size_t)dstate * sizeof(double));
+    double* dAl = (double*)calloc((size_t)dstate, sizeof(double));
+    if (!hs || !lam || !dAl) { free(hs); free(lam); free(dAl); failed = 1; continue; }
+    int64_t Lv = seqlen;
+    if (valid_len) {
+      Lv = valid_len[b];
+      if (Lv < 0) Lv = 0;
+      if (Lv > seqlen) Lv = seqlen;
+    }
+    for (int64_t n = 0; n < dstate; ++n) {
+      hs[n] = h0 ? (double)h0[(b * dim + d) * dstate + n] : 0.0;
+      lam[n] = 0.0;
+    }
+    for (int64_t t = 0; t < Lv; ++t) { /* forward, every state kept */
+      const int64_t e = (b * seqlen + t) * dim + d, r = (b * seqlen + t) * dstate;
+      const double dt = ref_load(delta, dtype, e), xv = ref_load(x, dtype, e);
+      for (int64_t n = 0; n < dstate; ++n)
+        hs[(t + 1) * dstate + n] = exp(dt * (double)A[d * dstate + n]) * hs[t * dstate + n] +
+                                   dt * ref_load(B, dtype, r + n) * xv;
+    }
+    double dDl = 0.0;
+    for (int64_t t = seqlen - 1; t >= 0; --t) {
+      const int64_t e = (b * seqlen + t) * dim + d, r = (b * seqlen + t) * dstate;
+      if (t >= Lv) {
+        dx[e] = 0.0; ddelta[e] = 0.0;
+        if (dz) dz[e] = 0.0;
+        continue;
+      }
+      const double dt = ref_load(delta, dtype, e), xv = ref_load(x, dtype, e);
+      const double Dd = D ? (double)D[d] : 0.0;
+      double yp = Dd * xv;
+      for (int64_t n = 0; n < dstate; ++n) yp += ref_load(C, dtype, r + n) * hs[(t + 1) * dstate + n];
+      double g = 1.0;
+      if (z) {
+        const double zv = ref_load(z, dtype, e);
+        g = ref_silu(zv);
+#if REF_PLANT == 12
+        dz[e] = dy[e] * yp * g; /* planted: silu in place of its derivative */
+#else
+        dz[e] = dy[e] * yp * ref_dsilu(zv);
+#endif
+      }
+      const double dyp = dy[e] * g;
+      double ddt = 0.0, dxv = dyp * Dd;
+      dDl += dyp * xv;
+      for (int64_t n = 0; n < dstate; ++n) {
+        const double An = (double)A[d * dstate + n];
+        const double a = exp(dt * An), Bn = ref_load(B, dtype, r + n);
+        const double hp = hs[t * dstate + n]; /* h_{t-1} */
+        lam[n] += ref_load(C, dtype, r + n) * dyp;
+        ddt += lam[n] * (Bn * xv + An * a * hp);
+        dxv += lam[n] * dt * Bn;
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+        dB[r + n] += lam[n] * dt * xv;
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+        dC[r + n] += dyp * hs[(t + 1) * dstate + n];
+#if REF_PLANT == 11
+        dAl[n] += lam[n] * a * hp; /* planted: delta factor of dA lost */
+#else
+        dAl[n] += lam[n] * dt * a * hp;
+#endif
+#if REF_PLANT == 10
+        lam[n] *= exp((t + 1 < Lv ? ref_load(delta, dtype, e + dim) : dt) * An); /* planted: a_{t+1} */
+#else
+        lam[n] *= a; /* carry to step t-1: a_t lambda_t */
+#endif
+      }
+      ddelta[e] = ddt;
+      dx[e] = dxv;
+    }
+    for (int64_t n = 0; n < dstate; ++n) {
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+      dA[d * dstate + n] += dAl[n];
+      if (dh0) dh0[(b * dim + d) * dstate + n] = lam[n];
+    }
+    if (dD) {
+#ifdef _OPENMP
+#pragma omp atomic
+#endif
+      dD[d] += dDl;
+    }
+    free(hs); free(lam); free(dAl);
+  }
+  return failed ? -1 : 0;
+}
+
 /* Version tag so a loader can tell which oracle build (plain or planted) it has. */
 int ref_plant_id(void) { return REF_PLANT; }

@@ -54,6 +54,8 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     lib.ref_scan_fwd_h0.restype = I32
     lib.ref_scan_fwd_h0.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
                                     I32, I32]
+    lib.ref_scan_bwd.restype = I32
+    lib.ref_scan_bwd.argtypes = [P] * 18 + [I64, I64, I64, I64, I32, I32]
     D = ctypes.c_double
     lib.ref_combine.restype = None
     lib.ref_combine.argtypes = [D, D, D, D, ctypes.POINTER(D), ctypes.POINTER(D)]
@@ -137,6 +139,38 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, chunk_len: int =
     if rc != 0:
         raise RuntimeError("ref_scan_fwd failed")
     return (y, states, final) if want_final else (y, states)
+
+
+def scan_bwd(x, delta, A, B, C, D=None, z=None, valid_len=None, dy=None, h0=None,
+             threads: int = 0, plant: int = 0) -> dict:
+    """Gradients of l = sum(dy * y) with respect to every input of the forward
+    (delta used as given).  Returns a dict of float64 arrays: dx, ddelta, dA,
+    dB, dC, dD (None without D), dz (None without gate), dh0 (None without h0)."""
+    if x.dtype == np.float32:
+        dtype = 0
+    elif x.dtype == np.uint16:
+        dtype = 1
+    else:
+        raise TypeError("x must be float32 or uint16 (bf16 bits)")
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    dy = np.ascontiguousarray(dy, dtype=np.float64)
+    if dy.shape != (batch, L, dim):
+        raise ValueError("dy must be [batch, L, dim]")
+    arrs = [np.ascontiguousarray(t) if t is not None else None
+            for t in (x, delta, A, B, C, D, z, valid_len, h0)]
+    out = {"dx": np.empty((batch, L, dim)), "ddelta": np.empty((batch, L, dim)),
+           "dA": np.empty((dim, dstate)), "dB": np.empty((batch, L, dstate)),
+           "dC": np.empty((batch, L, dstate)), "dD": np.empty(dim) if D is not None else None,
+           "dz": np.empty((batch, L, dim)) if z is not None else None,
+           "dh0": np.empty((batch, dim, dstate)) if h0 is not None else None}
+    rc = _load(plant).ref_scan_bwd(*[_ptr(t) for t in arrs], _ptr(dy), _ptr(out["dx"]),
+                                   _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]),
+                                   _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                                   _ptr(out["dh0"]), batch, L, dim, dstate, dtype, int(threads))
+    if rc != 0:
+        raise RuntimeError("ref_scan_bwd failed")
+    return out
 
 
 def plant_id(plant: int = 0) -> int:

@@ -415,9 +415,78 @@ def pin_delta_clamp(plant=0):
     np.testing.assert_allclose(y_m, y_p, rtol=1e-6, atol=1e-6 * np.max(np.abs(y_p)))
 
 
+# ---------------------------------------------------------------------------
+# The backward
+
+
+def _bwd_problem(rng, gate=True, with_h0=True):
+    batch, L, dim, N = 2, 5, 2, 3
+    x, delta, A, B, C, D, z = _rand_inputs(rng, batch, L, dim, N, gate=gate)
+    h0 = rng.standard_normal((batch, dim, N)).astype(np.float32) if with_h0 else None
+    vl = np.array([5, 3], np.int32)
+    dy = rng.standard_normal((batch, L, dim))
+    return dict(x=x, delta=delta, A=A, B=B, C=C, D=D, z=z, valid_len=vl, h0=h0), dy
+
+
+def _loss(args, dy, plant):
+    y, _ = R.scan_fwd(args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                      args["z"], args["valid_len"], h0=args["h0"], plant=plant)
+    return float(np.sum(dy * y))
+
+
+def pin_bwd_finite_differences(plant=0):
+    """Every gradient of l = sum(dy * y) against central differences of the
+    forward (each fp32 input moved up and down by about 1e-3 of its size; the
+    difference quotient uses the moved values as stored)."""
+    rng = np.random.default_rng(51)
+    args, dy = _bwd_problem(rng)
+    g = R.scan_bwd(args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                   args["z"], args["valid_len"], dy=dy, h0=args["h0"], plant=plant)
+    names = {"x": "dx", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "h0": "dh0"}
+    for key, gname in names.items():
+        base = args[key]
+        fd = np.empty(base.shape)
+        for idx in np.ndindex(base.shape):
+            v = float(base[idx])
+            step = max(abs(v), 0.1) * 1e-3
+            up, dn = base.copy(), base.copy()
+            up[idx] = np.float32(v + step)
+            dn[idx] = np.float32(v - step)
+            lu = _loss(dict(args, **{key: up}), dy, plant)
+            ld = _loss(dict(args, **{key: dn}), dy, plant)
+            fd[idx] = (lu - ld) / (float(up[idx]) - float(dn[idx]))
+        got = g[gname]
+        scale = max(np.max(np.abs(fd)), 1e-12)
+        assert np.max(np.abs(got - fd)) <= 1e-4 * scale, (key, np.max(np.abs(got - fd)), scale)
+
+
+def pin_bwd_homogeneity(plant=0):
+    """Without gate and with h0 = 0, y is linear in x, in B and in C, so
+    <dx, x> = <dy, y>, <dB, B> = <dC, C> = <dy, y - D x> and <dD, D> = <dy, D x>
+    (Euler's identity for functions homogeneous of degree one)."""
+    rng = np.random.default_rng(53)
+    args, dy = _bwd_problem(rng, gate=False, with_h0=False)
+    y, _ = R.scan_fwd(args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                      None, args["valid_len"], plant=plant)
+    g = R.scan_bwd(args["x"], args["delta"], args["A"], args["B"], args["C"], args["D"], None,
+                   args["valid_len"], dy=dy, plant=plant)
+    L = y.shape[1]
+    mask = (np.arange(L)[None, :] < args["valid_len"][:, None])[:, :, None]
+    dxy = args["D"][None, None, :].astype(np.float64) * args["x"] * mask
+    tot = float(np.sum(dy * y))
+    assert abs(float(np.sum(g["dx"] * args["x"])) - tot) <= 1e-10 * abs(tot) + 1e-12
+    rest = float(np.sum(dy * (y - dxy)))
+    assert abs(float(np.sum(g["dB"] * args["B"])) - rest) <= 1e-10 * abs(rest) + 1e-12
+    assert abs(float(np.sum(g["dC"] * args["C"])) - rest) <= 1e-10 * abs(rest) + 1e-12
+    dpart = float(np.sum(dy * dxy))
+    assert abs(float(np.sum(g["dD"] * args["D"])) - dpart) <= 1e-10 * abs(dpart) + 1e-12
+
+
 ALL_PINS = [pin_closed_form_recurrence, pin_closed_form_forward, pin_combine_is_composition,
             pin_associativity_bruteforce, pin_recurrence_is_prefix_of_combines,
             pin_reverse_identity, pin_lti_convolution, pin_unrolled_sum_bruteforce,
             pin_d_residual, pin_gate, pin_masking, pin_chunk_states_and_carry,
             pin_bf16_widening, pin_long_sequence_sane, pin_initial_state_split,
-            pin_softplus_closed_form, pin_softplus_and_bias_library, pin_delta_clamp]
+            pin_softplus_closed_form, pin_softplus_and_bias_library, pin_delta_clamp,
+            pin_bwd_finite_differences, pin_bwd_homogeneity]
