@@ -192,9 +192,11 @@ def parse():
     ap.add_argument("--fused-delta", action="store_true",
                     help="softplus workloads: pass the raw step inputs and dt_bias and let the "
                          "kernel apply softplus(raw + dt_bias)")
-    ap.add_argument("--op", default="scan", choices=["scan", "decode"],
+    ap.add_argument("--op", default="scan", choices=["scan", "decode", "bwd"],
                     help="scan: the forward (default); decode: one recurrence step on a "
-                         "carried state (--workload picks a decode workload)")
+                         "carried state (--workload picks a decode workload); bwd: the "
+                         "backward, replaying from chunk states (--bwd-chunk)")
+    ap.add_argument("--bwd-chunk", type=int, default=256)
     return ap.parse_args()
 
 
@@ -431,10 +433,159 @@ def decode_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+BWD_METRIC = "selective-scan backward: B*L*D elems/s and achieved % of roofline, 1xGB300"
+BWD_FP32_PER_NELT = 10  # lambda, d delta (2), dx, dB, dC, dA, the carry, the replayed update (2)
+
+
+def bwd_counts(w, inp, chunk: int) -> dict:
+    """Algorithmic work of the backward: one exp per valid (t, d, n) (the decay,
+    reused by the replayed update and the adjoint), about ten fp32 operations
+    per valid (t, d, n); bytes: the forward's inputs, dy and the chunk states
+    read once, every gradient written once."""
+    L, Dm, N, Bt = w.seqlen, w.dim, w.dstate, w.batch
+    vl = np.clip(inp["valid_len"], 0, L) if inp["valid_len"] is not None else np.full(Bt, L)
+    ev = int(vl.sum()) * Dm
+    es = 2 if w.dtype == "bf16" else 4
+    nact = 3 if w.gate else 2
+    nch = (L + chunk - 1) // chunk
+    rd = (nact + 1) * Bt * L * Dm * es + 2 * Bt * L * N * es + Dm * N * 4 + Dm * 4 \
+        + Bt * nch * Dm * N * 4 + Bt * 4
+    wr = nact * Bt * L * Dm * es + 2 * Bt * L * N * 4 + Dm * N * 4 + Dm * 4
+    return {"elements": Bt * L * Dm, "n_elements": ev * N, "exps": ev * N,
+            "fp32_ops": BWD_FP32_PER_NELT * ev * N, "bytes": rd + wr}
+
+
+def bwd_main(args):
+    """The backward on device buffers, after one forward that writes the chunk states."""
+    import torch
+    import selective_state_space_fwd_gb300 as S
+    from selective_state_space_fwd_gb300 import build as Bld
+    from selective_state_space_fwd_gb300 import workloads as W
+    rank, world, local = dist_env()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "metric": BWD_METRIC,
+                              "unavailable": "the reference arm times only the forward oracle"}))
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Bld.build()
+    S.load()
+    inp = W.make_inputs(w)
+    t = W.to_torch(inp, dev)
+    chunk = args.bwd_chunk
+    _, states = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                           t["valid_len"], chunk_len=chunk)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    dy = torch.randn(tuple(t["x"].shape), generator=gen, device=dev).to(t["x"].dtype)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        return S.scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                          t["valid_len"], chunk_states=states, chunk_len=chunk, dy=dy,
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = sum(per_step) / K
+    c = bwd_counts(w, inp, chunk)
+    peaks, peaks_src = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    r = roof(c, peaks, sms, mhz)
+    t_meas = ms * 1e-3
+    pk = MUFU_PER_SM_CLK * sms * mhz * 1e6 / 1e9
+    if r["t_hbm"] >= max(r["t_mufu"], r["t_fp32"]):
+        achieved = c["bytes"] / t_meas / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = r["t_roof"] / t_meas
+        roofline = {"bound": "alu", "achieved": c["fp32_ops"] / t_meas / 1e12,
+                    "peak": FP32_PER_SM_CLK * sms * mhz * 1e6 / 1e12, "unit": "TFLOP/s fp32",
+                    "frac": r["t_roof"] / t_meas}
+    roofline.update({"traffic": None, "kernel": "bwd", "peak_source": peaks_src,
+                     "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
+                                 "fp32": r["t_fp32"] * 1e6},
+                     "algorithmic": {"bytes": c["bytes"], "exps": c["exps"],
+                                     "fp32_ops": c["fp32_ops"]}})
+    # end to end: the backward's inputs in from pinned host memory, every gradient out
+    host = {k: v.cpu().pin_memory() for k, v in (("x", t["x"]), ("delta", t["delta"]),
+                                                  ("B", t["B"]), ("C", t["C"]), ("dy", dy),
+                                                  ("states", states))}
+    if t["z"] is not None:
+        host["z"] = t["z"].cpu().pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    outs = step()
+    outs_h = {k: torch.empty(tuple(v.shape), dtype=v.dtype, pin_memory=True)
+              for k, v in outs.items() if v is not None}
+
+    def step_host():
+        with torch.cuda.stream(stream):
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            g = S.scan_bwd(dbuf["x"], dbuf["delta"], t["A"], dbuf["B"], dbuf["C"], t["D"],
+                           dbuf.get("z"), t["valid_len"], chunk_states=dbuf["states"],
+                           chunk_len=chunk, dy=dbuf["dy"], stream=stream)
+            for k, v in outs_h.items():
+                v.copy_(g[k], non_blocking=True)
+
+    for _ in range(2):
+        step_host()
+    torch.cuda.synchronize(dev)
+    KE = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        step_host()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / KE
+    line = {"metric": BWD_METRIC, "value": c["elements"] / t_meas, "unit": UNIT, "n_gpus": 1,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32", "data": "synthetic",
+            "config": {"workload": w.name, "chunk_len": chunk, "gate": w.gate,
+                       "masked": w.mask is not None,
+                       "l2": "flushed between steps (256 MiB memset outside the timed events)"},
+            "roofline": roofline, "cpu_baseline": None,
+            "e2e": {"value": c["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                    "d2h_bytes_per_step": sum(v.numel() * v.element_size()
+                                              for v in outs_h.values()),
+                    "ms_per_step": ms_e2e},
+            "gpu_launches": K, "clocks": clk,
+            "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
+                            "max": max(per_step)}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.op == "decode":
         decode_main(args)
+        return
+    if args.op == "bwd":
+        bwd_main(args)
         return
     from selective_state_space_fwd_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]

@@ -201,6 +201,32 @@ ssm_status ssm_decode_step_prep(const void* x, const void* delta, const ssm_delt
                                 int64_t dim, int64_t dstate, ssm_dtype dtype,
                                 cudaStream_t stream);
 
+/*
+ * ssm_scan_bwd -- the backward: every gradient of l = sum(dy * y) for the
+ * forward ssm_scan_fwd_carry computes (delta used as given).
+ *   Forward inputs x, delta, A, B, C, D, z, valid_len, h0: as in the forward.
+ *   chunk_states : device fp32 [batch, ceil(L/chunk_len), dim, dstate], the
+ *                  boundary states the forward wrote with the same chunk_len
+ *                  (shapes->chunk_len, 1 .. 512); the backward replays the
+ *                  forward from them ([P1] s3.4).
+ *   dy           : device, dtype `dtype`, [batch, L, dim].
+ *   dx, ddelta   : device, dtype `dtype`, [batch, L, dim] (outputs).
+ *   dz           : device, dtype `dtype`, [batch, L, dim]; required with z.
+ *   dA           : device fp32 [dim, dstate]; dB, dC: fp32 [batch, L, dstate];
+ *                  dD: fp32 [dim] or NULL; all four are sums over channels,
+ *                  steps or batch rows, zeroed on `stream` by the call.
+ *   dh0          : device fp32 [batch, dim, dstate] or NULL: the gradient of
+ *                  the state before the first step.
+ * Steps past valid_len get zero gradients.  The summed outputs are added with
+ * atomics: their last bits depend on the order.  Asynchronous on `stream`.
+ */
+ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z,
+                        const int32_t* valid_len, const float* h0, const float* chunk_states,
+                        const void* dy, void* dx, void* ddelta, float* dA, float* dB, float* dC,
+                        float* dD, void* dz, float* dh0, const ssm_shapes* shapes,
+                        ssm_dtype dtype, cudaStream_t stream);
+
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional
  * tensors the call passes.  Writes the tier to *kernel and the launch grid

@@ -6,10 +6,11 @@ seeded synthetic workloads used by the benchmark and tests.
 """
 from ._binding import (Kernel, SsmError, Status, check_device_errors, chunk_count,
                        decode_step, declared_functions,
-                       host_workspace_bytes, kernel_name, load, plan, scan_fwd, scan_fwd_host,
+                       host_workspace_bytes, kernel_name, load, plan, scan_bwd, scan_fwd, scan_fwd_host,
                        status_string, version)
 
 __all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "decode_step",
            "declared_functions",
-           "host_workspace_bytes", "kernel_name", "load", "plan", "scan_fwd", "scan_fwd_host",
+           "host_workspace_bytes", "kernel_name", "load", "plan", "scan_bwd", "scan_fwd",
+           "scan_fwd_host",
            "status_string", "version"]

@@ -99,6 +99,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
     lib.ssm_decode_step_prep.restype = I32
     lib.ssm_decode_step_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
+    lib.ssm_scan_bwd.restype = I32
+    lib.ssm_scan_bwd.argtypes = [P] * 19 + [SP, I32, P]
     lib.ssm_decode_step.restype = I32
     lib.ssm_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
     lib.ssm_scan_plan.restype = I32
@@ -388,3 +390,53 @@ def decode_step(x, delta, A, B, C, D=None, z=None, *, state, out=None, stream=No
     if st != 0:
         raise SsmError(st, "ssm_decode_step")
     return y
+
+
+def scan_bwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_states, chunk_len: int,
+             dy, h0=None, want_dh0: bool = False, stream=None) -> dict:
+    """Every gradient of sum(dy * y) for the forward on these inputs (delta used
+    as given).  ``chunk_states`` are the boundary states the forward wrote with
+    the same ``chunk_len`` (1 .. 512).  Returns a dict: dx, ddelta, dz (None
+    without gate) like x; dA, dB, dC, dD (None without D), dh0 (when wanted) in fp32."""
+    import torch
+    lib = load()
+    dev, dt = x.device, x.dtype
+    code = _dtype_code(dt)
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    nch = (L + chunk_len - 1) // chunk_len
+    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, dim), dt),
+                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
+                                ("A", A, (dim, dstate), torch.float32), ("dy", dy, (batch, L, dim), dt),
+                                ("chunk_states", chunk_states, (batch, nch, dim, dstate),
+                                 torch.float32)):
+        _check(t, name, shape, tdt, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, dev)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, dstate), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+           "dz": torch.empty_like(x) if z is not None else None,
+           "dA": torch.empty((dim, dstate), **f32), "dB": torch.empty((batch, L, dstate), **f32),
+           "dC": torch.empty((batch, L, dstate), **f32),
+           "dD": torch.empty((dim,), **f32) if D is not None else None,
+           "dh0": torch.empty((batch, dim, dstate), **f32) if want_dh0 else None}
+    s = _shapes(batch, L, dim, dstate, chunk_len)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                              _ptr(valid_len), _ptr(h0), _ptr(chunk_states), _ptr(dy),
+                              _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                              _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out["dz"]),
+                              _ptr(out["dh0"]), ctypes.byref(s), int(code),
+                              ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_bwd")
+    return out

@@ -16,6 +16,8 @@ namespace {
 
 using ssm::ScanParams;
 
+constexpr int64_t kBwdMaxChunk = 512;  // longest chunk the backward replays in shared memory
+
 bool supported_dstate(int64_t n) {
   return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
 }
@@ -506,6 +508,43 @@ ssm_status ssm_decode_step_prep(const void* x, const void* delta, const ssm_delt
   const ssm_status st = apply_prep(prep, &p);
   if (st != SSM_OK) return st;
   return ssm::launch_decode(p, dtype == SSM_BF16, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z,
+                        const int32_t* valid_len, const float* h0, const float* chunk_states,
+                        const void* dy, void* dx, void* ddelta, float* dA, float* dB, float* dC,
+                        float* dD, void* dz, float* dh0, const ssm_shapes* shapes,
+                        ssm_dtype dtype, cudaStream_t stream) {
+  ssm_status st = check_shapes(shapes, dtype, true);
+  if (st != SSM_OK) return st;
+  if (shapes->chunk_len > kBwdMaxChunk) return SSM_ERR_UNSUPPORTED;
+  if (!x || !delta || !A || !B || !C || !chunk_states || !dy || !dx || !ddelta || !dA || !dB ||
+      !dC)
+    return SSM_ERR_NULL;
+  if (z && !dz) return SSM_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+      !aligned(dy, es) || !aligned(dx, es) || !aligned(ddelta, es) || (z && !aligned(z, es)) ||
+      (dz && !aligned(dz, es)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (valid_len && !aligned(valid_len, 4)) || (h0 && !aligned(h0, 4)) ||
+      !aligned(chunk_states, 4) || !aligned(dA, 4) || !aligned(dB, 4) || !aligned(dC, 4) ||
+      (dD && !aligned(dD, 4)) || (dh0 && !aligned(dh0, 4)))
+    return SSM_ERR_ALIGN;
+  ssm::BwdParams p;
+  p.fwd = make_params(x, delta, A, B, C, D, z, valid_len, nullptr,
+                      const_cast<float*>(chunk_states), shapes, h0, nullptr);
+  p.dy = dy; p.dx = dx; p.ddelta = ddelta; p.dz = z ? dz : nullptr;
+  p.dA = dA; p.dB = dB; p.dC = dC; p.dD = D ? dD : nullptr; p.dh0 = dh0;
+  const size_t bln = size_t(shapes->batch) * shapes->seqlen * shapes->dstate * sizeof(float);
+  cudaError_t e = cudaMemsetAsync(dA, 0, size_t(shapes->dim) * shapes->dstate * sizeof(float),
+                                  stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, bln, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dC, 0, bln, stream);
+  if (e == cudaSuccess && p.dD) e = cudaMemsetAsync(dD, 0, size_t(shapes->dim) * sizeof(float),
+                                                    stream);
+  if (e == cudaSuccess) e = ssm::launch_bwd(p, dtype == SSM_BF16, stream);
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // extern "C"

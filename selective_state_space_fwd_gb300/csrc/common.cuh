@@ -64,6 +64,21 @@ struct DecodeParams {
   float delta_lo, delta_hi;
 };
 
+// Arguments of the backward: the forward's inputs (and its chunk boundary
+// states, chunk_len > 0) in `fwd`, the output gradient and every gradient.
+struct BwdParams {
+  ScanParams fwd;     // y, h_final unused; states = the forward's chunk states
+  const void* dy;     // [B, L, D]
+  void* dx;           // [B, L, D]
+  void* ddelta;       // [B, L, D]
+  void* dz;           // [B, L, D], when fwd.z
+  float* dA;          // [D, N], summed (zeroed before the kernel)
+  float* dB;          // [B, L, N], summed
+  float* dC;          // [B, L, N], summed
+  float* dD;          // nullable, [D], summed
+  float* dh0;         // nullable, [B, D, N]
+};
+
 // 2^v with the MUFU unit (PTX ex2.approx.ftz.f32: results below 2^-126 flush
 // to zero, which the method tolerates: a product of decays that underflows
 // only removes contributions already below fp32 resolution, [P1] s2.4).

@@ -1,0 +1,291 @@
+// kernel_bwd.cu -- the backward of the selective-scan forward.
+//
+// For the loss l = sum dy * y, every gradient: dx, d delta, dz (per element),
+// dB, dC (per (b, t, n), summed over channels), dA (per (d, n), summed over b
+// and t), dD (per d) and the initial state's gradient dh0.  Reverse mode
+// through the recurrence: the adjoint of h_t is
+//   lambda_t = C_t dyp_t + a_{t+1} lambda_{t+1},   dyp_t = dy_t silu(z_t),
+// and each input's gradient follows from a_t = exp(delta_t A),
+// b_t = delta_t B_t x_t, the C contraction, the D residual and the gate.
+// The reverse pass needs h_{t-1} at every step: it replays the forward from
+// the chunk boundary states the forward wrote ([P1] s3.4: the boundary
+// states are kept so that the backward recomputes instead of storing every
+// state).  Inside a chunk, a first pass keeps a checkpoint every K steps in
+// shared memory and each K-step piece is then replayed once more, newest
+// first, with its states and inputs in shared memory; the global loads of a
+// half piece are issued together, so their latency is paid once per half
+// piece and not once per step.
+//
+// Work split: GB = min(4, N) consecutive states per thread, NL = N / GB
+// threads per channel, 32 / NL channels per warp, all of one batch row.  Sums
+// over a channel's states are xor-shuffles over its NL lanes; sums over the
+// warp's channels (dB, dC) are xor-shuffles over the channel lanes followed
+// by one atomic add per warp; dA and dD accumulate in registers and are
+// added once per thread.
+#include "common.cuh"
+#include "tiers.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBwdThreads = 128;
+constexpr int kBwdK = 16;  // steps per replayed piece
+
+template <int N>
+struct BwdShape {
+  static constexpr int GB = N >= 4 ? 4 : N;  // states per thread
+  static constexpr int NL = N / GB;          // threads per channel
+  static constexpr int CWB = 32 / NL;        // channels per warp
+  static constexpr int CPB = CWB * (kBwdThreads / 32);
+};
+
+// Shared-memory floats per thread for chunks of cl steps: the checkpoints,
+// the piece's K + 1 states, and the piece's inputs (delta, x, dy, z, and the
+// thread's B and C values).
+__host__ __device__ inline int bwd_floats(int64_t cl, int gb) {
+  const int nck = static_cast<int>((cl + kBwdK - 1) / kBwdK);
+  return nck * gb + (kBwdK + 1) * gb + 4 * kBwdK + 2 * kBwdK * gb;
+}
+
+template <int N, typename T, bool GATE>
+__global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
+  using S = BwdShape<N>;
+  constexpr int GB = S::GB, NL = S::NL, K = kBwdK, H = K / 2;
+  extern __shared__ __align__(16) float sm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nblk = (p.fwd.dim + S::CPB - 1) / S::CPB;
+  const int64_t b = blockIdx.x / nblk;
+  const int64_t d = (blockIdx.x % nblk) * S::CPB + warp * S::CWB + lane / NL;
+  const int sl = lane % NL, n0 = sl * GB;
+  const bool ok = d < p.fwd.dim;
+  const int64_t dd = ok ? d : 0;
+  const int64_t L = p.fwd.seqlen, CL = p.fwd.chunk_len, D_ = p.fwd.dim;
+  const int64_t lv = valid_steps(p.fwd, b);
+  const int nck = static_cast<int>((CL + K - 1) / K);
+  // this thread's float i of its shared-memory area: sm[i * blockDim + tid]
+  auto f = [&](int i) -> float& { return sm[i * kBwdThreads + tid]; };
+  const int CK = 0, HS = nck * GB, IDT = HS + (K + 1) * GB, IX = IDT + K, IDY = IX + K,
+            IZ = IDY + K, IB = IZ + K, IC = IB + K * GB;
+
+  float av[GB], al[GB];  // A of this thread's states, and scaled by log2(e)
+#pragma unroll
+  for (int g = 0; g < GB; ++g) {
+    av[g] = ok ? __ldg(p.fwd.A + dd * N + n0 + g) : 0.f;
+    al[g] = av[g] * kLog2e;
+  }
+  const float dsk = (ok && p.fwd.D) ? __ldg(p.fwd.D + dd) : 0.f;
+  float lam[GB], dacc[GB];
+#pragma unroll
+  for (int g = 0; g < GB; ++g) lam[g] = dacc[g] = 0.f;
+  float dDacc = 0.f;
+
+  const int64_t nch = (L + CL - 1) / CL;
+  for (int64_t c = nch - 1; c >= 0; --c) {
+    const int64_t t0 = c * CL, t1 = min(t0 + CL, L), tv = min(t1, lv);
+    for (int64_t t = (tv > t0 ? tv : t0); t < t1; ++t) {  // past valid_len: zero gradients
+      if (ok && sl == 0) {
+        const int64_t e = (b * L + t) * D_ + dd;
+        IO<T>::store(p.dx, e, 0.f);
+        IO<T>::store(p.ddelta, e, 0.f);
+        if (GATE) IO<T>::store(p.dz, e, 0.f);
+      }
+    }
+    if (tv <= t0) continue;
+    float h[GB];
+#pragma unroll
+    for (int g = 0; g < GB; ++g) {
+      float v = 0.f;
+      if (ok) {
+        if (c > 0)
+          v = p.fwd.states[((b * p.fwd.n_chunks + c - 1) * D_ + dd) * N + n0 + g];
+        else if (p.fwd.h0)
+          v = p.fwd.h0[(b * D_ + dd) * N + n0 + g];
+      }
+      h[g] = v;
+    }
+    // pass 1: the forward's arithmetic over the chunk, a checkpoint (the
+    // state before the piece) every K steps; the loads of a half piece are
+    // issued together
+    for (int64_t s0 = t0; s0 < tv; s0 += K) {
+#pragma unroll
+      for (int g = 0; g < GB; ++g) f(CK + static_cast<int>((s0 - t0) / K) * GB + g) = h[g];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float dt[H], ux[H], bb[H][GB];
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+          const int64_t t = s0 + hh * H + k;
+          const bool in = t < tv;
+          const int64_t tt = in ? t : s0;
+          const int64_t e = (b * L + tt) * D_ + dd;
+          dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;  // past the chunk: identity
+          ux[k] = dt[k] * IO<T>::load(p.fwd.x, e);
+#pragma unroll
+          for (int g = 0; g < GB; ++g) bb[k][g] = IO<T>::load(p.fwd.B, (b * L + tt) * N + n0 + g);
+        }
+#pragma unroll
+        for (int k = 0; k < H; ++k)
+#pragma unroll
+          for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux[k] * bb[k][g]);
+      }
+    }
+    // pass 2: the pieces, newest first
+    for (int64_t j = (tv - t0 - 1) / K; j >= 0; --j) {
+      const int64_t s0 = t0 + j * K, s1 = min(s0 + K, tv);
+#pragma unroll
+      for (int g = 0; g < GB; ++g) h[g] = f(CK + static_cast<int>(j) * GB + g);
+      // replay: the piece's inputs to shared memory, its states h_{t-1}
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float dt[H], xv[H], dyv[H], zv[H], bb[H][GB], cc[H][GB];
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+          const int64_t t = s0 + hh * H + k;
+          const bool in = t < s1;
+          const int64_t tt = in ? t : s0;
+          const int64_t e = (b * L + tt) * D_ + dd, r = (b * L + tt) * N + n0;
+          dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;
+          xv[k] = IO<T>::load(p.fwd.x, e);
+          dyv[k] = (in && ok) ? IO<T>::load(p.dy, e) : 0.f;
+          zv[k] = GATE ? IO<T>::load(p.fwd.z, e) : 0.f;
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            bb[k][g] = IO<T>::load(p.fwd.B, r + g);
+            cc[k][g] = IO<T>::load(p.fwd.C, r + g);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+          const int kk = hh * H + k;
+          f(IDT + kk) = dt[k];
+          f(IX + kk) = xv[k];
+          f(IDY + kk) = dyv[k];
+          f(IZ + kk) = zv[k];
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            f(IB + kk * GB + g) = bb[k][g];
+            f(IC + kk * GB + g) = cc[k][g];
+            f(HS + kk * GB + g) = h[g];  // h_{t-1}
+          }
+          const float ux = dt[k] * xv[k];
+#pragma unroll
+          for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * bb[k][g]);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < GB; ++g) f(HS + K * GB + g) = h[g];  // beyond s1 the steps were identities
+      // reverse over the piece
+      for (int k = static_cast<int>(s1 - s0) - 1; k >= 0; --k) {
+        const int64_t t = s0 + k;
+        const int64_t e = (b * L + t) * D_ + dd, r = (b * L + t) * N + n0;
+        const float dt = f(IDT + k), xv = f(IX + k), dyv = f(IDY + k);
+        float hp[GB], hc[GB], bb[GB], cc[GB];
+        float yp = 0.f;
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          hp[g] = f(HS + k * GB + g);
+          hc[g] = f(HS + (k + 1) * GB + g);
+          bb[g] = f(IB + k * GB + g);
+          cc[g] = f(IC + k * GB + g);
+          yp = fmaf(cc[g], hc[g], yp);
+        }
+#pragma unroll
+        for (int m = NL / 2; m >= 1; m /= 2) yp += __shfl_xor_sync(0xffffffffu, yp, m);
+        yp = fmaf(dsk, xv, yp);  // C h + D x, before the gate
+        float dyp = dyv, dzv = 0.f;
+        if (GATE) {
+          const float zz = f(IZ + k);
+          const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
+          dyp = dyv * zz * sg;                           // dy silu(z)
+          dzv = dyv * yp * sg * (1.f + zz * (1.f - sg));  // dy yp silu'(z)
+        }
+        float pdt = 0.f, pdx = 0.f, db[GB], dc[GB];
+#pragma unroll
+        for (int g = 0; g < GB; ++g) {
+          const float a = ex2(dt * al[g]);
+          lam[g] = fmaf(cc[g], dyp, lam[g]);  // + C_t dyp_t
+          pdt = fmaf(lam[g], fmaf(bb[g], xv, av[g] * a * hp[g]), pdt);
+          pdx = fmaf(lam[g] * dt, bb[g], pdx);
+          db[g] = lam[g] * dt * xv;
+          dc[g] = dyp * hc[g];
+          dacc[g] = fmaf(lam[g] * dt * a, hp[g], dacc[g]);
+          lam[g] *= a;  // carried to step t - 1
+        }
+#pragma unroll
+        for (int m = NL / 2; m >= 1; m /= 2) {
+          pdt += __shfl_xor_sync(0xffffffffu, pdt, m);
+          pdx += __shfl_xor_sync(0xffffffffu, pdx, m);
+        }
+        // sums over the warp's channels (lanes sl + NL k)
+#pragma unroll
+        for (int m = 16; m >= NL; m /= 2) {
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            db[g] += __shfl_xor_sync(0xffffffffu, db[g], m);
+            dc[g] += __shfl_xor_sync(0xffffffffu, dc[g], m);
+          }
+        }
+        if (lane < NL) {
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            atomicAdd(p.dB + r + g, db[g]);
+            atomicAdd(p.dC + r + g, dc[g]);
+          }
+        }
+        if (ok && sl == 0) {
+          IO<T>::store(p.ddelta, e, pdt);
+          IO<T>::store(p.dx, e, fmaf(dyp, dsk, pdx));
+          if (GATE) IO<T>::store(p.dz, e, dzv);
+          dDacc = fmaf(dyp, xv, dDacc);
+        }
+      }
+    }
+  }
+  if (ok) {
+#pragma unroll
+    for (int g = 0; g < GB; ++g) {
+      atomicAdd(p.dA + dd * N + n0 + g, dacc[g]);
+      if (p.dh0) p.dh0[(b * D_ + dd) * N + n0 + g] = lam[g];
+    }
+    if (sl == 0 && p.dD) atomicAdd(p.dD + dd, dDacc);
+  }
+}
+
+template <typename T, bool GATE>
+cudaError_t launch_tg(const BwdParams& p, cudaStream_t s) {
+  const int gb = p.fwd.dstate >= 4 ? 4 : p.fwd.dstate;
+  const size_t smem = size_t(bwd_floats(p.fwd.chunk_len, gb)) * kBwdThreads * sizeof(float);
+  auto go = [&](auto kern, int cpb) -> cudaError_t {
+    // set on every launch: all the kernels share one function type, so a
+    // "done once" flag here would cover only the first of them
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (p.fwd.dim + cpb - 1) / cpb * p.fwd.batch;
+    kern<<<static_cast<unsigned>(blocks), kBwdThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  };
+  switch (p.fwd.dstate) {
+    case 1: return go(bwd_kernel<1, T, GATE>, BwdShape<1>::CPB);
+    case 2: return go(bwd_kernel<2, T, GATE>, BwdShape<2>::CPB);
+    case 4: return go(bwd_kernel<4, T, GATE>, BwdShape<4>::CPB);
+    case 8: return go(bwd_kernel<8, T, GATE>, BwdShape<8>::CPB);
+    case 16: return go(bwd_kernel<16, T, GATE>, BwdShape<16>::CPB);
+    case 32: return go(bwd_kernel<32, T, GATE>, BwdShape<32>::CPB);
+    case 64: return go(bwd_kernel<64, T, GATE>, BwdShape<64>::CPB);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int64_t chunk_len, int dstate) {
+  return size_t(bwd_floats(chunk_len, dstate >= 4 ? 4 : dstate)) * kBwdThreads * sizeof(float);
+}
+
+cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s) {
+  if (bf16) return p.fwd.z ? launch_tg<__nv_bfloat16, true>(p, s) : launch_tg<__nv_bfloat16, false>(p, s);
+  return p.fwd.z ? launch_tg<float, true>(p, s) : launch_tg<float, false>(p, s);
+}
+
+}  // namespace ssm

@@ -34,6 +34,11 @@ cudaError_t launch_warpscan(const ScanParams& p, bool bf16, cudaStream_t s);
 // Decode step: one step of the recurrence on a carried state, in place.
 cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 
+// Backward: every gradient of sum(dy * y), replaying the forward from its
+// chunk boundary states.
+cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s);
+size_t bwd_smem_bytes(int64_t chunk_len, int dstate);
+
 // Sticky device error word of the tiers with bounded waits: read and clear.
 bool read_and_clear_device_errors(unsigned int* word);
 

@@ -8,7 +8,7 @@ import pytest
 from selective_state_space_fwd_gb300 import _binding as Bd
 
 EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_fwd_prep",
-            "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_plan", "ssm_scan_fwd_host",
+            "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_bwd", "ssm_scan_plan", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
@@ -150,6 +150,27 @@ def _prep_call(prep):
 ])
 def test_prep_argument_errors_return_status(ssmlib, prep, status):
     assert _prep_call(prep) == status
+
+
+def _bwd(shapes=(2, 8, 4, 16, 4), z=None, dz=None, states=FAKE, dA=FAKE, x=FAKE, dtype=0):
+    P = ctypes.c_void_p
+    s = Bd.Shapes(*shapes)
+    return Bd.load().ssm_scan_bwd(P(x), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(z), None,
+                                  None, P(states), P(FAKE), P(FAKE), P(FAKE), P(dA), P(FAKE),
+                                  P(FAKE), None, P(dz), None, ctypes.byref(s), dtype, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(shapes=(2, 8, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 8, 4, 16, 513)), Bd.Status.ERR_UNSUPPORTED),
+    (dict(states=None), Bd.Status.ERR_NULL),
+    (dict(dA=None), Bd.Status.ERR_NULL),
+    (dict(z=FAKE, dz=None), Bd.Status.ERR_NULL),
+    (dict(x=FAKE + 2), Bd.Status.ERR_ALIGN),
+    (dict(dA=FAKE + 2), Bd.Status.ERR_ALIGN),
+])
+def test_bwd_argument_errors_return_status(ssmlib, kw, status):
+    assert _bwd(**kw) == status
 
 
 def test_plan_serial_always_available(ssmlib):
