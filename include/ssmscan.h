@@ -262,6 +262,32 @@ ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, c
                              const ssm_shapes* shapes, ssm_dtype dtype, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * ssm_scan_fwd_host_static -- ssm_scan_fwd_host without any allocation.  The
+ * pages have no counterpart: this is a deployment form of the end-to-end call
+ * for callers that may not allocate device memory (fixed-memory services).
+ * The device workspace is a fixed array inside the library of
+ * ssm_scan_host_static_capacity() bytes (64 MiB); calls whose workspace
+ * (ssm_scan_host_workspace_bytes) is larger return SSM_ERR_SHAPE.  Every copy
+ * and kernel runs on `stream` in order (no pipelining, no library streams or
+ * events); the call allocates nothing, neither with cudaMalloc nor through
+ * any other library.  Nothing in the array has to start at zero.
+ *   - The array is shared by all calls on a device: calls that overlap in
+ *     time (on different streams, or from several threads) race on it and
+ *     must be serialised by the caller.
+ *   - The first call on a device looks the array's address up (one runtime
+ *     query); make it before capturing `stream` into a CUDA graph.
+ * Arguments, layouts and the result are those of ssm_scan_fwd_host.
+ */
+ssm_status ssm_scan_fwd_host_static(const void* x, const void* delta, const float* A,
+                                    const void* B, const void* C, const float* D, const void* z,
+                                    const int32_t* valid_len, void* out_y, float* out_chunk_states,
+                                    const ssm_shapes* shapes, ssm_dtype dtype,
+                                    cudaStream_t stream);
+
+/* Bytes of the fixed workspace of ssm_scan_fwd_host_static. */
+size_t ssm_scan_host_static_capacity(void);
+
 /* Device bytes ssm_scan_fwd_host needs for these shapes and optional tensors;
  * 0 on invalid shapes. */
 size_t ssm_scan_host_workspace_bytes(const ssm_shapes* shapes, ssm_dtype dtype, int has_D,

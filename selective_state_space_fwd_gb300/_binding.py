@@ -99,6 +99,10 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, P, P, P, SP, I32, P, OP]
     lib.ssm_decode_step_prep.restype = I32
     lib.ssm_decode_step_prep.argtypes = [P, P, DP, P, P, P, P, P, P, P, I64, I64, I64, I32, P]
+    lib.ssm_scan_fwd_host_static.restype = I32
+    lib.ssm_scan_fwd_host_static.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P]
+    lib.ssm_scan_host_static_capacity.restype = SZ
+    lib.ssm_scan_host_static_capacity.argtypes = []
     lib.ssm_scan_bwd.restype = I32
     lib.ssm_scan_bwd.argtypes = [P] * 19 + [SP, I32, P]
     lib.ssm_decode_step.restype = I32
@@ -440,3 +444,37 @@ def scan_bwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_states,
     if st != 0:
         raise SsmError(st, "ssm_scan_bwd")
     return out
+
+
+def static_capacity() -> int:
+    """Bytes of the fixed workspace of scan_fwd_host_static."""
+    return int(load().ssm_scan_host_static_capacity())
+
+
+def scan_fwd_host_static(x, delta, A, B, C, D=None, z=None, valid_len=None, *, out, chunk_len=0,
+                         out_states=None, stream=None):
+    """scan_fwd_host without any allocation: the library's fixed device
+    workspace, every step on ``stream``.  ``out`` (and ``out_states`` when
+    chunk_len > 0) are caller-owned host tensors; nothing is allocated here.
+    Calls that overlap in time race on the workspace."""
+    import torch
+    lib = load()
+    dt = x.dtype
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    cpu = torch.device("cpu")
+    _check(out, "out", (batch, L, dim), dt, cpu)
+    if chunk_len > 0:
+        nch = (L + chunk_len - 1) // chunk_len
+        _check(out_states, "out_states", (batch, nch, dim, dstate), torch.float32, cpu)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    s = _shapes(batch, L, dim, dstate, chunk_len)
+    st = lib.ssm_scan_fwd_host_static(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                      _ptr(z), _ptr(valid_len), _ptr(out), _ptr(out_states),
+                                      ctypes.byref(s), int(_dtype_code(dt)),
+                                      ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd_host_static")
+    return out, out_states

@@ -548,3 +548,115 @@ ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const 
 }
 
 }  // extern "C"
+
+// ---- the end-to-end form without any allocation ------------------------------------
+//
+// The same computation as ssm_scan_fwd_host (pieces chained by the carried
+// state), with its device workspace in a fixed file-scope array instead of a
+// caller-owned buffer, and every copy and kernel on the caller's stream (no
+// library streams or events are created).
+
+namespace {
+
+constexpr size_t kStaticWsBytes = size_t(64) << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+// Address of g_static_ws on each device, looked up once with that device current.
+char* static_ws(int dev) {
+  static char* addr[64] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_static_ws) != cudaSuccess || a == nullptr) return nullptr;
+    addr[dev] = static_cast<char*>(a);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_host_static_capacity(void) { return kStaticWsBytes; }
+
+ssm_status ssm_scan_fwd_host_static(const void* x, const void* delta, const float* A,
+                                    const void* B, const void* C, const float* D, const void* z,
+                                    const int32_t* valid_len, void* out_y, float* out_chunk_states,
+                                    const ssm_shapes* shapes, ssm_dtype dtype,
+                                    cudaStream_t stream) {
+  const bool want_states = out_chunk_states != nullptr;
+  ssm_status st = check_shapes(shapes, dtype, want_states);
+  if (st != SSM_OK) return st;
+  if (!x || !delta || !A || !B || !C || !out_y) return SSM_ERR_NULL;
+  const HostLayout l = host_layout(shapes, dtype, D != nullptr, z != nullptr,
+                                   valid_len != nullptr, want_states);
+  if (l.total > kStaticWsBytes) return SSM_ERR_SHAPE;  // larger than the fixed workspace
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  char* ws = static_ws(dev);
+  if (ws == nullptr) return SSM_ERR_CUDA;
+
+  const ssm_shapes& s = *shapes;
+  const size_t es = elem_size(dtype);
+  const int64_t L = s.seqlen, Bt = s.batch, N = s.dstate;
+  const size_t dn4 = size_t(s.dim) * N * 4;
+  const int64_t nch = want_states ? (L + s.chunk_len - 1) / s.chunk_len : 0;
+  const int64_t piece = host_piece_steps(s, dtype, z != nullptr, want_states);
+  float* carry[2] = {reinterpret_cast<float*>(ws + l.carry),
+                     reinterpret_cast<float*>(ws + l.carry + size_t(Bt) * dn4)};
+  cudaError_t e = cudaSuccess;
+  auto ok = [&](cudaError_t r) { if (e == cudaSuccess) e = r; return e == cudaSuccess; };
+  auto copy_in = [&](size_t region, const void* src, int64_t w, int64_t t0, int64_t n) {
+    const size_t row = size_t(w) * es;
+    return ok(cudaMemcpy2DAsync(ws + region + size_t(Bt) * t0 * row, n * row,
+                                static_cast<const char*>(src) + t0 * row, L * row, n * row, Bt,
+                                cudaMemcpyHostToDevice, stream));
+  };
+  // Nothing in the workspace has to start at zero: every piece's carried state
+  // is written by the piece before it is read, and the first piece starts
+  // from h0 = 0 without reading the workspace.
+  ok(cudaMemcpyAsync(ws + l.A, A, dn4, cudaMemcpyHostToDevice, stream));
+  if (D) ok(cudaMemcpyAsync(ws + l.D, D, size_t(s.dim) * 4, cudaMemcpyHostToDevice, stream));
+  if (valid_len)
+    ok(cudaMemcpyAsync(ws + l.valid, valid_len, size_t(Bt) * 4, cudaMemcpyHostToDevice, stream));
+  int i = 0;
+  for (int64_t t0 = 0; t0 < L && e == cudaSuccess; t0 += piece, ++i) {
+    const int64_t n = L - t0 < piece ? L - t0 : piece;
+    const size_t act_off = size_t(Bt) * t0 * s.dim * es, bc_off = size_t(Bt) * t0 * N * es;
+    copy_in(l.x, x, s.dim, t0, n);
+    copy_in(l.delta, delta, s.dim, t0, n);
+    if (z) copy_in(l.z, z, s.dim, t0, n);
+    copy_in(l.B, B, N, t0, n);
+    copy_in(l.C, C, N, t0, n);
+    if (e != cudaSuccess) break;
+    const int64_t c0 = want_states ? t0 / s.chunk_len : 0;
+    const int64_t pch = want_states ? (n + s.chunk_len - 1) / s.chunk_len : 0;
+    float* pstates = want_states ? reinterpret_cast<float*>(ws + l.states) + size_t(Bt) * c0 *
+                                       (dn4 / 4)
+                                 : nullptr;
+    const ssm_shapes ps = {Bt, n, s.dim, N, want_states ? s.chunk_len : 0};
+    ScanParams p = make_params(ws + l.x + act_off, ws + l.delta + act_off,
+                               reinterpret_cast<const float*>(ws + l.A), ws + l.B + bc_off,
+                               ws + l.C + bc_off,
+                               D ? reinterpret_cast<const float*>(ws + l.D) : nullptr,
+                               z ? ws + l.z + act_off : nullptr,
+                               valid_len ? reinterpret_cast<const int32_t*>(ws + l.valid) : nullptr,
+                               ws + l.y + act_off, pstates, &ps,
+                               t0 == 0 ? nullptr : carry[i % 2],
+                               t0 + n < L ? carry[(i + 1) % 2] : nullptr);
+    p.len_offset = t0;
+    st = launch(p, dtype, nullptr, stream);
+    if (st != SSM_OK) return st;
+    const size_t row = size_t(s.dim) * es;
+    ok(cudaMemcpy2DAsync(static_cast<char*>(out_y) + t0 * row, L * row, ws + l.y + act_off,
+                         n * row, n * row, Bt, cudaMemcpyDeviceToHost, stream));
+    if (want_states)
+      ok(cudaMemcpy2DAsync(out_chunk_states + size_t(c0) * (dn4 / 4), nch * dn4, pstates,
+                           pch * dn4, pch * dn4, Bt, cudaMemcpyDeviceToHost, stream));
+  }
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"

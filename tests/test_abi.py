@@ -8,7 +8,8 @@ import pytest
 from selective_state_space_fwd_gb300 import _binding as Bd
 
 EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_fwd_prep",
-            "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_bwd", "ssm_scan_plan", "ssm_scan_fwd_host",
+            "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_bwd", "ssm_scan_plan",
+            "ssm_scan_fwd_host_static", "ssm_scan_host_static_capacity", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
 
