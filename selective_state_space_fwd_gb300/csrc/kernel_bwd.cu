@@ -12,9 +12,9 @@
 // states are kept so that the backward recomputes instead of storing every
 // state).  Inside a chunk, a first pass keeps a checkpoint every K steps in
 // shared memory and each K-step piece is then replayed once more, newest
-// first, with its states and inputs in shared memory; the global loads of a
-// half piece are issued together, so their latency is paid once per half
-// piece and not once per step.
+// first, with its states and inputs in shared memory (the B and C rows once
+// per CTA); the global loads of a half piece are issued together, so their
+// latency is paid once per half piece and not once per step.
 //
 // Work split: GB = min(4, N) consecutive states per thread, NL = N / GB
 // threads per channel, 32 / NL channels per warp, all of one batch row.  Sums
@@ -40,11 +40,15 @@ struct BwdShape {
 };
 
 // Shared-memory floats per thread for chunks of cl steps: the checkpoints,
-// the piece's K + 1 states, and the piece's inputs (delta, x, dy, z, and the
-// thread's B and C values).
+// the piece's K + 1 states, and the piece's per-channel inputs (delta, x, dy,
+// z).  The piece's B and C rows are shared by the CTA (one batch row).
 __host__ __device__ inline int bwd_floats(int64_t cl, int gb) {
   const int nck = static_cast<int>((cl + kBwdK - 1) / kBwdK);
-  return nck * gb + (kBwdK + 1) * gb + 4 * kBwdK + 2 * kBwdK * gb;
+  return nck * gb + (kBwdK + 1) * gb + 4 * kBwdK;
+}
+__host__ __device__ inline size_t bwd_smem(int64_t cl, int n) {
+  const int gb = n >= 4 ? 4 : n;
+  return (size_t(bwd_floats(cl, gb)) * kBwdThreads + 2 * kBwdK * n) * sizeof(float);
 }
 
 template <int N, typename T, bool GATE>
@@ -65,7 +69,10 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
   // this thread's float i of its shared-memory area: sm[i * blockDim + tid]
   auto f = [&](int i) -> float& { return sm[i * kBwdThreads + tid]; };
   const int CK = 0, HS = nck * GB, IDT = HS + (K + 1) * GB, IX = IDT + K, IDY = IX + K,
-            IZ = IDY + K, IB = IZ + K, IC = IB + K * GB;
+            IZ = IDY + K;
+  // the piece's B and C rows [K][N], shared by the CTA, after the threads' areas
+  float* sB = sm + bwd_floats(CL, GB) * kBwdThreads;
+  float* sC = sB + K * N;
 
   float av[GB], al[GB];  // A of this thread's states, and scaled by log2(e)
 #pragma unroll
@@ -134,25 +141,31 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
       const int64_t s0 = t0 + j * K, s1 = min(s0 + K, tv);
 #pragma unroll
       for (int g = 0; g < GB; ++g) h[g] = f(CK + static_cast<int>(j) * GB + g);
+      // the piece's B and C rows, once per CTA (every warp of the CTA walks the
+      // same pieces: one batch row); the previous piece is done with them
+      __syncthreads();
+      for (int i = tid; i < K * N; i += kBwdThreads) {
+        const int64_t t = s0 + i / N;
+        const bool in = t < s1;
+        const int64_t r = (b * L + (in ? t : s0)) * N + i % N;
+        sB[i] = in ? IO<T>::load(p.fwd.B, r) : 0.f;
+        sC[i] = in ? IO<T>::load(p.fwd.C, r) : 0.f;
+      }
+      __syncthreads();
       // replay: the piece's inputs to shared memory, its states h_{t-1}
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float dt[H], xv[H], dyv[H], zv[H], bb[H][GB], cc[H][GB];
+        float dt[H], xv[H], dyv[H], zv[H];
 #pragma unroll
         for (int k = 0; k < H; ++k) {
           const int64_t t = s0 + hh * H + k;
           const bool in = t < s1;
           const int64_t tt = in ? t : s0;
-          const int64_t e = (b * L + tt) * D_ + dd, r = (b * L + tt) * N + n0;
+          const int64_t e = (b * L + tt) * D_ + dd;
           dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;
           xv[k] = IO<T>::load(p.fwd.x, e);
           dyv[k] = (in && ok) ? IO<T>::load(p.dy, e) : 0.f;
           zv[k] = GATE ? IO<T>::load(p.fwd.z, e) : 0.f;
-#pragma unroll
-          for (int g = 0; g < GB; ++g) {
-            bb[k][g] = IO<T>::load(p.fwd.B, r + g);
-            cc[k][g] = IO<T>::load(p.fwd.C, r + g);
-          }
         }
 #pragma unroll
         for (int k = 0; k < H; ++k) {
@@ -162,14 +175,11 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
           f(IDY + kk) = dyv[k];
           f(IZ + kk) = zv[k];
 #pragma unroll
-          for (int g = 0; g < GB; ++g) {
-            f(IB + kk * GB + g) = bb[k][g];
-            f(IC + kk * GB + g) = cc[k][g];
-            f(HS + kk * GB + g) = h[g];  // h_{t-1}
-          }
+          for (int g = 0; g < GB; ++g) f(HS + kk * GB + g) = h[g];  // h_{t-1}
           const float ux = dt[k] * xv[k];
 #pragma unroll
-          for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * bb[k][g]);
+          for (int g = 0; g < GB; ++g)
+            h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * sB[kk * N + n0 + g]);
         }
       }
 #pragma unroll
@@ -185,8 +195,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
         for (int g = 0; g < GB; ++g) {
           hp[g] = f(HS + k * GB + g);
           hc[g] = f(HS + (k + 1) * GB + g);
-          bb[g] = f(IB + k * GB + g);
-          cc[g] = f(IC + k * GB + g);
+          bb[g] = sB[k * N + n0 + g];
+          cc[g] = sC[k * N + n0 + g];
           yp = fmaf(cc[g], hc[g], yp);
         }
 #pragma unroll
@@ -253,8 +263,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
 
 template <typename T, bool GATE>
 cudaError_t launch_tg(const BwdParams& p, cudaStream_t s) {
-  const int gb = p.fwd.dstate >= 4 ? 4 : p.fwd.dstate;
-  const size_t smem = size_t(bwd_floats(p.fwd.chunk_len, gb)) * kBwdThreads * sizeof(float);
+  const size_t smem = bwd_smem(p.fwd.chunk_len, p.fwd.dstate);
   auto go = [&](auto kern, int cpb) -> cudaError_t {
     // set on every launch: all the kernels share one function type, so a
     // "done once" flag here would cover only the first of them
@@ -280,7 +289,7 @@ cudaError_t launch_tg(const BwdParams& p, cudaStream_t s) {
 }  // namespace
 
 size_t bwd_smem_bytes(int64_t chunk_len, int dstate) {
-  return size_t(bwd_floats(chunk_len, dstate >= 4 ? 4 : dstate)) * kBwdThreads * sizeof(float);
+  return bwd_smem(chunk_len, dstate);
 }
 
 cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s) {

@@ -14,11 +14,11 @@
 // Holding R channels makes every B/C value a lane loads serve R channels and
 // every delta/x value serve G states, which is what bounds the shared-memory
 // to register traffic per (channel, state).  The C contraction is a sum over
-// the NG lanes of a channel group: a shuffle reduce-scatter once per NG steps
-// leaves each lane with one step's outputs for its R channels, to which the
-// D residual (added once, by the group's state-0 lane) and the silu(z) gate
-// apply ([P1] s3.3: everything between the loads of x, delta, B, C and the
-// store of y is fused; h never leaves registers).
+// the NG lanes of a channel group: each lane stores its per-step partial sums
+// to a per-warp shared buffer, and every 16 steps an epilogue sums the NG
+// partials of each (step, channel), adds the D residual, applies the silu(z)
+// gate and stores y ([P1] s3.3: everything between the loads of x, delta, B,
+// C and the store of y is fused; h never leaves registers).
 //
 // Data movement.  A CTA covers W warps (chosen at launch) of CW consecutive
 // channels of one batch row.  Time is cut into tiles of T steps; per tile TMA
@@ -27,10 +27,10 @@
 // and states contiguous, so every copy is a dense box).  mbarriers with
 // bounded waits order the copies and their reuse.  Boxes that run past L or D
 // are zero-filled by the copy engine, and a zero delta is the identity step
-// (a = 2^0 = 1, b = 0), so ragged tails need no branch ([P1] s2.3); steps of a
-// loaded tile past valid_len are zeroed in shared memory the same way.  Tiles that lie
-// entirely past valid_len[b] are never loaded: y there is written as exact
-// zeros and the state stays frozen.
+// (a = 2^0 = 1, b = 0), so ragged tails need no branch ([P1] s2.3); steps of
+// a loaded tile past valid_len are zeroed in shared memory the same way.
+// Tiles that lie entirely past valid_len[b] are never loaded: y there is
+// written as exact zeros and the state stays frozen.
 #pragma once
 
 #include <cuda.h>
