@@ -19,7 +19,9 @@
  *   [P2] "Mamba并行扫描与硬件感知优化：从SSM递推到GPU高效实现"
  *        (bjdmk.com.cn/news/5218626):
  *        s2.2 the operator pair (A_t, b_t) and its merge rule;  s4.2 the
- *        element-wise (diagonal) state transition, states of shape (..., N).
+ *        element-wise (diagonal) state transition, states of shape (..., N);
+ *        s5.1-s5.2 the Mamba 2 duality (the recurrence as a semiseparable
+ *        matrix product, blocks by matrix products and a scan between them).
  *
  * Readings where the pages leave a step open (each is also listed in the
  * design notes of the repository):
@@ -371,6 +373,82 @@ int ref_scan_bwd(const void* x, const void* delta, const float* A, const void* B
       dD[d] += dDl;
     }
     free(hs); free(lam); free(dAl);
+  }
+  return failed ? -1 : 0;
+}
+
+/*
+ * The state-space-duality (SSD) form of the scan ([P2] s5.1-s5.2, the Mamba 2
+ * section): the same linear recurrence, with one decay per head shared by all
+ * of the head's channels and states, which is what lets the in-block work be
+ * written as matrix products.  Channels are grouped in nheads heads of
+ * headdim channels (d = h * headdim + p); per head h the step size delta is
+ * one value per (b, t, h) and A is one scalar A[h] < 0.  For every (b, h, p)
+ * and state n, from h_{-1} = h0 (else 0):
+ *   a_t = exp(delta_{b,t,h} A_h),  h_tn = a_t h_{t-1,n} + delta_{b,t,h} B_{b,t,n} x_{b,t,d}
+ *   y_{b,t,d} = (sum_n C_{b,t,n} h_tn + D_d x_{b,t,d}) * silu(z_{b,t,d})   (gate optional)
+ * Steps t >= valid_len[b] are the identity and their output is exactly 0, as
+ * in the scan above.  This is the definition; the blocked matrix form that a
+ * fast implementation uses is checked against it by the tests (the quadratic
+ * form y = M x with M[t,s] = (C_t . B_s) exp(A_h sum_{s<r<=t} delta_r) delta_s).
+ * Layouts: x, z [batch, seqlen, nheads*headdim]; delta [batch, seqlen, nheads];
+ * A [nheads] fp32; B, C [batch, seqlen, dstate]; D [nheads*headdim] fp32 or
+ * NULL; h0 and final [batch, nheads*headdim, dstate] (fp32 in, double out, NULL
+ * = zero / not wanted); y_out [batch, seqlen, nheads*headdim] doubles.
+ */
+int ref_ssd_fwd(const void* x, const void* delta, const float* A, const void* B, const void* C,
+                const float* D, const void* z, const int32_t* valid_len, const float* h0,
+                double* y_out, double* final_out, int64_t batch, int64_t seqlen, int64_t nheads,
+                int64_t headdim, int64_t dstate, int dtype, int nthreads) {
+  if (batch < 0 || seqlen < 0 || nheads < 0 || headdim < 1 || dstate < 1) return -1;
+  if (dtype != REF_F32 && dtype != REF_BF16) return -1;
+  const int64_t dim = nheads * headdim, channels = batch * dim;
+  int failed = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : failed)
+#endif
+  for (int64_t bd = 0; bd < channels; ++bd) {
+    const int64_t b = bd / dim, d = bd % dim, hd = d / headdim;
+    double* h = (double*)malloc((size_t)dstate * sizeof(double));
+    if (!h) { failed = 1; continue; }
+    for (int64_t n = 0; n < dstate; ++n) h[n] = h0 ? (double)h0[(b * dim + d) * dstate + n] : 0.0;
+    int64_t Lv = seqlen;
+    if (valid_len) {
+      Lv = valid_len[b];
+      if (Lv < 0) Lv = 0;
+      if (Lv > seqlen) Lv = seqlen;
+    }
+    const double Ah = (double)A[hd];
+    for (int64_t t = 0; t < seqlen; ++t) {
+      const int64_t e = (b * seqlen + t) * dim + d;
+      const int64_t r = (b * seqlen + t) * dstate;
+      double y = 0.0;
+      if (t < Lv) {
+        const double dt = ref_load(delta, dtype, (b * seqlen + t) * nheads + hd);
+#if REF_PLANT == 13
+        const double xv = ref_load(x, dtype, (b * seqlen + t) * dim + d % headdim); /* planted: head offset lost */
+#else
+        const double xv = ref_load(x, dtype, e);
+#endif
+        const double a = exp(dt * Ah); /* one decay for the whole head */
+        double acc = 0.0;
+        for (int64_t n = 0; n < dstate; ++n) {
+#if REF_PLANT == 14
+          h[n] = a * (h[n] + dt * ref_load(B, dtype, r + n) * xv); /* planted: input decayed too */
+#else
+          h[n] = a * h[n] + dt * ref_load(B, dtype, r + n) * xv;
+#endif
+          acc += ref_load(C, dtype, r + n) * h[n];
+        }
+        y = acc + (D ? (double)D[d] * xv : 0.0);
+        if (z) y *= ref_silu(ref_load(z, dtype, e));
+      }
+      y_out[e] = y;
+    }
+    if (final_out)
+      for (int64_t n = 0; n < dstate; ++n) final_out[(b * dim + d) * dstate + n] = h[n];
+    free(h);
   }
   return failed ? -1 : 0;
 }

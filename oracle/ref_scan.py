@@ -54,6 +54,8 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     lib.ref_scan_fwd_h0.restype = I32
     lib.ref_scan_fwd_h0.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
                                     I32, I32]
+    lib.ref_ssd_fwd.restype = I32
+    lib.ref_ssd_fwd.argtypes = [P] * 11 + [I64, I64, I64, I64, I64, I32, I32]
     lib.ref_scan_bwd.restype = I32
     lib.ref_scan_bwd.argtypes = [P] * 18 + [I64, I64, I64, I64, I32, I32]
     D = ctypes.c_double
@@ -171,6 +173,49 @@ def scan_bwd(x, delta, A, B, C, D=None, z=None, valid_len=None, dy=None, h0=None
     if rc != 0:
         raise RuntimeError("ref_scan_bwd failed")
     return out
+
+
+def ssd_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, h0=None, nheads: int = 1,
+            want_final: bool = False, threads: int = 0, plant: int = 0):
+    """The SSD form of the scan: one decay per head.  x, z [batch, L, nheads *
+    headdim]; delta [batch, L, nheads]; A float32 [nheads]; B, C [batch, L,
+    dstate]; D float32 [nheads * headdim]; h0 float32 [batch, nheads * headdim,
+    dstate].  Returns y (float64 [batch, L, dim]), and with ``want_final`` also
+    the state after the last step (float64 [batch, dim, dstate])."""
+    if x.dtype == np.float32:
+        dtype = 0
+    elif x.dtype == np.uint16:
+        dtype = 1
+    else:
+        raise TypeError("x must be float32 or uint16 (bf16 bits)")
+    batch, L, dim = x.shape
+    if dim % nheads:
+        raise ValueError("dim must be a multiple of nheads")
+    headdim = dim // nheads
+    dstate = B.shape[-1]
+    for name, t, shape in (("delta", delta, (batch, L, nheads)), ("B", B, (batch, L, dstate)),
+                           ("C", C, (batch, L, dstate))):
+        if t.shape != shape or t.dtype != x.dtype:
+            raise ValueError(f"{name}: expected {shape} {x.dtype}, got {t.shape} {t.dtype}")
+    if A.shape != (nheads,) or A.dtype != np.float32:
+        raise ValueError("A must be float32 [nheads]")
+    if D is not None and (D.shape != (dim,) or D.dtype != np.float32):
+        raise ValueError("D must be float32 [dim]")
+    if z is not None and (z.shape != (batch, L, dim) or z.dtype != x.dtype):
+        raise ValueError("z must match x")
+    if valid_len is not None and (valid_len.shape != (batch,) or valid_len.dtype != np.int32):
+        raise ValueError("valid_len must be int32 [batch]")
+    if h0 is not None and (h0.shape != (batch, dim, dstate) or h0.dtype != np.float32):
+        raise ValueError("h0 must be float32 [batch, dim, dstate]")
+    arrs = [np.ascontiguousarray(t) if t is not None else None
+            for t in (x, delta, A, B, C, D, z, valid_len, h0)]
+    y = np.empty((batch, L, dim), dtype=np.float64)
+    final = np.empty((batch, dim, dstate), dtype=np.float64) if want_final else None
+    rc = _load(plant).ref_ssd_fwd(*[_ptr(t) for t in arrs], _ptr(y), _ptr(final), batch, L,
+                                  nheads, headdim, dstate, dtype, int(threads))
+    if rc != 0:
+        raise RuntimeError("ref_ssd_fwd failed")
+    return (y, final) if want_final else y
 
 
 def plant_id(plant: int = 0) -> int:

@@ -483,10 +483,109 @@ def pin_bwd_homogeneity(plant=0):
     assert abs(float(np.sum(g["dD"] * args["D"])) - dpart) <= 1e-10 * abs(dpart) + 1e-12
 
 
+# ---------------------------------------------------------------------------
+# The SSD form ([P2] s5.1-s5.2): one decay per head
+
+
+def _ssd_problem(rng, batch=2, L=10, H=2, P=3, N=4, valid=(10, 6)):
+    dim = H * P
+    x = rng.standard_normal((batch, L, dim)).astype(np.float32)
+    delta = np.exp(rng.uniform(np.log(1e-2), np.log(0.5), (batch, L, H))).astype(np.float32)
+    A = -np.exp(rng.uniform(np.log(0.5), np.log(4.0), H)).astype(np.float32)
+    B = rng.standard_normal((batch, L, N)).astype(np.float32)
+    C = rng.standard_normal((batch, L, N)).astype(np.float32)
+    D = rng.standard_normal(dim).astype(np.float32)
+    z = rng.standard_normal((batch, L, dim)).astype(np.float32)
+    h0 = rng.standard_normal((batch, dim, N)).astype(np.float32)
+    vl = np.array(valid, np.int32)
+    return dict(x=x, delta=delta, A=A, B=B, C=C, D=D, z=z, h0=h0, valid_len=vl, H=H)
+
+
+def pin_ssd_closed_form(plant=0):
+    """The a = 1/2, b = 1 closed form through the SSD form: one head of one
+    channel, one state, delta = 1, A = -ln 2, B = C = x = 1, D = 0."""
+    L = 8
+    one = np.ones((1, L, 1), np.float32)
+    y = R.ssd_fwd(one, one, np.array([-math.log(2.0)], np.float32), one, one,
+                  D=np.zeros(1, np.float32), nheads=1, plant=plant)
+    np.testing.assert_allclose(y[0, :, 0], golden_closed_form(), rtol=1e-7, atol=0)
+
+
+def pin_ssd_quadratic_form(plant=0):
+    """[P2] s5.1: the recurrence written out is one lower-triangular
+    (semiseparable) matrix per head applied to the inputs,
+    y_t = sum_{s<=t} (C_t . B_s) exp(A_h sum_{s<r<=t} delta_r) delta_s x_s
+          + (C_t . h0) exp(A_h sum_{r<=t} delta_r) + D x_t, times silu(z_t),
+    built here by brute force as a dense matrix, with the final state as the
+    same sums taken at the last valid step."""
+    rng = np.random.default_rng(71)
+    a = _ssd_problem(rng)
+    H = a["H"]
+    y, fin = R.ssd_fwd(a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["valid_len"],
+                       a["h0"], nheads=H, want_final=True, plant=plant)
+    batch, L, dim = a["x"].shape
+    P = dim // H
+    x, dl, B, C = (a[k].astype(np.float64) for k in ("x", "delta", "B", "C"))
+    A, D, z, h0 = (a[k].astype(np.float64) for k in ("A", "D", "z", "h0"))
+    want = np.zeros((batch, L, dim))
+    want_fin = np.zeros(fin.shape)
+    for b in range(batch):
+        Lv = int(a["valid_len"][b])
+        for h in range(H):
+            cs = np.concatenate([[0.0], np.cumsum(dl[b, :Lv, h])])  # cs[t+1] = sum_{r<=t}
+            M = np.zeros((Lv, Lv))
+            for t in range(Lv):
+                for s_ in range(t + 1):
+                    M[t, s_] = (C[b, t] @ B[b, s_]) * math.exp(A[h] * (cs[t + 1] - cs[s_ + 1])) \
+                        * dl[b, s_, h]
+            ch = slice(h * P, (h + 1) * P)
+            yp = M @ x[b, :Lv, ch]
+            yp += (C[b, :Lv] @ h0[b, ch].T) * np.exp(A[h] * cs[1:])[:, None]
+            yp += D[ch][None, :] * x[b, :Lv, ch]
+            zz = z[b, :Lv, ch]
+            want[b, :Lv, ch] = yp * zz / (1.0 + np.exp(-zz))
+            w = np.exp(A[h] * (cs[Lv] - cs[1:])) * dl[b, :Lv, h]  # weight of step s in the final state
+            want_fin[b, ch] = math.exp(A[h] * cs[Lv]) * h0[b, ch] + (x[b, :Lv, ch] * w[:, None]).T @ B[b, :Lv]
+    scale = np.max(np.abs(want))
+    assert np.max(np.abs(y - want)) <= 1e-12 * scale, np.max(np.abs(y - want)) / scale
+    fscale = np.max(np.abs(want_fin))
+    assert np.max(np.abs(fin - want_fin)) <= 1e-12 * fscale
+
+
+def pin_ssd_reduces_to_scan(plant=0):
+    """With the head's step size and decay copied to each of its channels and
+    states (delta[b,t,d] = delta[b,t,h], A[d,n] = A[h]), the SSD form is the
+    diagonal scan pinned above: same y and final state, fp32 and bf16 inputs."""
+    rng = np.random.default_rng(73)
+    a = _ssd_problem(rng, batch=2, L=23, H=3, P=4, N=5, valid=(23, 9))
+    H = a["H"]
+    P = a["x"].shape[2] // H
+    N = a["B"].shape[2]
+    for bf16 in (False, True):
+        cv = (lambda t: _to_bf16_bits(t)) if bf16 else (lambda t: t)
+        x, dl, B, C, z = (cv(a[k]) for k in ("x", "delta", "B", "C", "z"))
+        y, fin = R.ssd_fwd(x, dl, a["A"], B, C, a["D"], z, a["valid_len"], a["h0"], nheads=H,
+                           want_final=True, plant=plant)
+        dfull = np.repeat(dl, P, axis=2)
+        Afull = np.repeat(a["A"], P)[:, None].repeat(N, axis=1).astype(np.float32)
+        ys, _, fs = R.scan_fwd(x, dfull, Afull, B, C, a["D"], z, a["valid_len"], h0=a["h0"],
+                               want_final=True)
+        np.testing.assert_allclose(y, ys, rtol=0, atol=1e-13 * np.max(np.abs(ys)))
+        np.testing.assert_allclose(fin, fs, rtol=0, atol=1e-13 * np.max(np.abs(fs)))
+
+
+def _to_bf16_bits(a):
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (numpy, for pins only)."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
 ALL_PINS = [pin_closed_form_recurrence, pin_closed_form_forward, pin_combine_is_composition,
             pin_associativity_bruteforce, pin_recurrence_is_prefix_of_combines,
             pin_reverse_identity, pin_lti_convolution, pin_unrolled_sum_bruteforce,
             pin_d_residual, pin_gate, pin_masking, pin_chunk_states_and_carry,
             pin_bf16_widening, pin_long_sequence_sane, pin_initial_state_split,
             pin_softplus_closed_form, pin_softplus_and_bias_library, pin_delta_clamp,
-            pin_bwd_finite_differences, pin_bwd_homogeneity]
+            pin_bwd_finite_differences, pin_bwd_homogeneity, pin_ssd_closed_form,
+            pin_ssd_quadratic_form, pin_ssd_reduces_to_scan]
