@@ -192,10 +192,11 @@ def parse():
     ap.add_argument("--fused-delta", action="store_true",
                     help="softplus workloads: pass the raw step inputs and dt_bias and let the "
                          "kernel apply softplus(raw + dt_bias)")
-    ap.add_argument("--op", default="scan", choices=["scan", "decode", "bwd"],
+    ap.add_argument("--op", default="scan", choices=["scan", "decode", "bwd", "ssd"],
                     help="scan: the forward (default); decode: one recurrence step on a "
                          "carried state (--workload picks a decode workload); bwd: the "
-                         "backward, replaying from chunk states (--bwd-chunk)")
+                         "backward, replaying from chunk states (--bwd-chunk); ssd: the "
+                         "SSD form (one decay per head) on the tensor cores")
     ap.add_argument("--bwd-chunk", type=int, default=256)
     return ap.parse_args()
 
@@ -579,6 +580,178 @@ def bwd_main(args):
     print(json.dumps(line), flush=True)
 
 
+SSD_METRIC = "SSD (one decay per head) fwd: B*L*D elems/s and achieved % of roofline, 1xGB300"
+
+
+def ssd_counts(w) -> dict:
+    """Algorithmic work of the SSD form with blocks of 128 steps.  Bytes: x, z
+    read and y written once (bf16), delta per (t, head), B and C rows once.
+    Tensor flops: C B^T once per (batch row, block) (shared by the heads),
+    then per head the block matrix times x, C times the entering state and the
+    state update (2 flops per multiply-add)."""
+    Q = 128
+    Bt, L, H, P, N = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate
+    nb = (L + Q - 1) // Q
+    act = Bt * L * H * P
+    nbytes = 2 * act * (3 if w.gate else 2) + 2 * Bt * L * H + 2 * 2 * Bt * L * N + 4 * H + 4 * H * P
+    flops = Bt * nb * 2 * Q * Q * N + Bt * H * nb * (2 * Q * Q * P + 2 * 2 * Q * N * P)
+    return {"elements": act, "bytes": nbytes, "flops": flops}
+
+
+def _ssd_sample(inp, w, pairs):
+    subs = []
+    P = w.headdim
+    for b, h in pairs:
+        ch = slice(h * P, (h + 1) * P)
+        subs.append(tuple(np.ascontiguousarray(a) for a in (
+            inp["x"][b:b + 1, :, ch], inp["delta"][b:b + 1, :, h:h + 1], inp["A"][h:h + 1],
+            inp["B"][b:b + 1], inp["C"][b:b + 1], inp["D"][ch],
+            inp["z"][b:b + 1, :, ch] if inp["z"] is not None else None)))
+    return subs
+
+
+def ssd_cpu(w, inp, seconds: float) -> dict:
+    """The oracle's SSD form on a bounded sample of (batch row, head) pairs."""
+    from oracle import ref_scan
+    threads = os.cpu_count() or 1
+    pairs = [(b % w.batch, (7 * b) % w.nheads) for b in range(16)]
+    subs = _ssd_sample(inp, w, pairs)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        for sub in subs:
+            ref_scan.ssd_fwd(*sub, nheads=1, threads=threads)
+            n += 1
+        if time.perf_counter() - t0 > min(seconds, 20.0):
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": w.seqlen * w.headdim / dt, "unit": "elements/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{len(pairs)} (batch row, head) pairs x {w.headdim} channels x "
+                      f"{w.seqlen} steps, cycled for about {min(seconds, 20.0):.0f} s"}
+
+
+def ssd_main(args):
+    """The SSD form on device buffers (inputs larger than L2), then end to end."""
+    import torch
+    import selective_state_space_fwd_gb300 as S
+    from selective_state_space_fwd_gb300 import build as Bld
+    from selective_state_space_fwd_gb300 import workloads as W
+    rank, world, local = dist_env()
+    w = W.SSD_WORKLOADS[1]
+    inp = W.make_ssd_inputs(w)
+    if args.impl == "reference":
+        if rank == 0:
+            cpu = ssd_cpu(w, inp, 150.0 / max(1, args.steps + args.warmup))
+            print(json.dumps({"impl": "reference", "metric": SSD_METRIC, "value": cpu["value"],
+                              "unit": "elements/s", "n_gpus": 1, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": None,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                              "dtype": "f64", "data": "synthetic",
+                              "config": {"workload": w.name}, "cpu_baseline": cpu,
+                              "e2e": {"value": cpu["value"], "unit": "elements/s",
+                                      "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                  flush=True)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Bld.build()
+    S.load()
+    t = W.to_torch(inp, dev)
+    y = torch.empty_like(t["x"])
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(tt, out):
+        S.ssd_fwd(tt["x"], tt["delta"], t["A"], tt["B"], tt["C"], t["D"], tt["z"], None,
+                  nheads=w.nheads, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(t, y)
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev0[i].record(stream)
+            step(t, y)
+            ev1[i].record(stream)
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    S.check_device_errors()
+    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = sum(per_step) / K
+    c = ssd_counts(w)
+    peaks, peaks_src = load_peaks()
+    t_hbm = c["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = c["flops"] / (peaks["bf16_tflops"] * 1e12)
+    sec = ms * 1e-3
+    if t_hbm >= t_tc:
+        ach = c["bytes"] / sec / 1e9
+        roofline = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"]}
+    else:
+        ach = c["flops"] / sec / 1e12
+        roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"]}
+    roofline.update({"traffic": measured_traffic("ssd", w.name), "kernel": "ssd",
+                     "peak_source": peaks_src,
+                     "roof_us": {"hbm": t_hbm * 1e6, "tensor_bf16": t_tc * 1e6},
+                     "frac_of_roof": max(t_hbm, t_tc) / sec,
+                     "tensor_tflops": c["flops"] / sec / 1e12,
+                     "algorithmic": {"bytes": c["bytes"], "flops": c["flops"]}})
+    # end to end: every input from pinned host memory, y back, every step
+    names = ("x", "delta", "B", "C", "z")
+    host = {k: t[k].cpu().pin_memory() for k in names if t[k] is not None}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    y_h = torch.empty(tuple(y.shape), dtype=y.dtype, pin_memory=True)
+
+    def step_host():
+        with torch.cuda.stream(stream):
+            for k, v in host.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            step({k: dbuf.get(k) for k in names}, y)
+            y_h.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        step_host()
+    torch.cuda.synchronize(dev)
+    KE = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        step_host()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / KE
+    line = {
+        "metric": SSD_METRIC, "value": c["elements"] / sec, "unit": "elements/s", "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16-io/bf16-mma/f32-acc",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen,
+                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
+                   "gate": w.gate, "block": 128,
+                   "l2": "flushed between steps (256 MiB memset outside the timed events)"
+                         if not args.no_flush else "not flushed"},
+        "roofline": roofline,
+        "cpu_baseline": None if args.no_cpu_baseline else ssd_cpu(w, inp, args.cpu_seconds),
+        "e2e": {"value": c["elements"] / (ms_e2e * 1e-3), "unit": "elements/s",
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                "d2h_bytes_per_step": y_h.numel() * y_h.element_size(), "ms_per_step": ms_e2e},
+        "gpu_launches": K, "clocks": clk,
+        "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
+                        "max": max(per_step)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.op == "decode":
@@ -586,6 +759,9 @@ def main():
         return
     if args.op == "bwd":
         bwd_main(args)
+        return
+    if args.op == "ssd":
+        ssd_main(args)
         return
     from selective_state_space_fwd_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]

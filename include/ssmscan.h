@@ -227,6 +227,45 @@ ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const 
                         float* dD, void* dz, float* dh0, const ssm_shapes* shapes,
                         ssm_dtype dtype, cudaStream_t stream);
 
+/*
+ * ssm_ssd_fwd -- the state-space-duality (SSD) form of the scan, computed
+ * blockwise with tensor-core matrix products ([P2] s5.1-s5.2: the recurrence
+ * expanded into a semiseparable matrix product; blocks of steps by matrix
+ * products, the state carried from block to block by the recurrence).  The
+ * decay is shared by all channels and states of a head: the channels
+ * d = h * headdim + p of head h use one step size delta[b,t,h] and one scalar
+ * A[h] < 0.  For every (b, d, n), from h = h0 (zeros when NULL):
+ *   h[b,d,n] <- exp(delta[b,t,h] A[h]) h[b,d,n] + delta[b,t,h] B[b,t,n] x[b,t,d]
+ *   y[b,t,d]  = (sum_n C[b,t,n] h[b,d,n] + D[d] x[b,t,d]) * silu(z[b,t,d])
+ * Steps t >= valid_len[b] are the identity and their output is exactly 0.
+ *   x, z      : device bf16 [batch, seqlen, nheads*headdim], 16-byte aligned
+ *               (z NULL: no gate).
+ *   delta     : device bf16 [batch, seqlen, nheads], the step size as given (> 0).
+ *   A         : device fp32 [nheads].  D: device fp32 [nheads*headdim] or NULL.
+ *   B, C      : device bf16 [batch, seqlen, dstate], 16-byte aligned.
+ *   valid_len : device int32 [batch] or NULL; clamped to [0, seqlen] on the device.
+ *   h0        : device fp32 [batch, nheads*headdim, dstate] or NULL.
+ *   out_y     : device bf16 [batch, seqlen, nheads*headdim], 16-byte aligned.
+ *   out_final_state : device fp32 [batch, nheads*headdim, dstate], the state
+ *               after the last step, or NULL.
+ * Supported: dtype SSM_BF16, headdim 64, dstate 128; other sizes or fp32 return
+ * SSM_ERR_UNSUPPORTED.  The products take bf16 operands (the inputs, the masked
+ * decay-weighted block matrix and the state entering a block, rounded to bf16)
+ * and accumulate in fp32; the state between blocks of 128 steps stays fp32.
+ * All pointers are caller-owned; nothing is allocated.  Asynchronous on
+ * `stream`; argument errors return a status before launch.  A CTA whose
+ * bounded wait on the tensor cores gives up sets the sticky device error word
+ * (ssm_check_device_errors returns SSM_ERR_TIMEOUT; outputs undefined).
+ */
+typedef struct {
+  int64_t batch, seqlen, nheads, headdim, dstate;
+} ssm_ssd_shapes;
+
+ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const void* B,
+                       const void* C, const float* D, const void* z, const int32_t* valid_len,
+                       const float* h0, void* out_y, float* out_final_state,
+                       const ssm_ssd_shapes* shapes, ssm_dtype dtype, cudaStream_t stream);
+
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional
  * tensors the call passes.  Writes the tier to *kernel and the launch grid

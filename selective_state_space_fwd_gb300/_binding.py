@@ -59,6 +59,12 @@ class Options(ctypes.Structure):
 _lib = None
 
 
+class SsdShapes(ctypes.Structure):
+    """ssm_ssd_shapes."""
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64)]
+
+
 class DeltaPrep(ctypes.Structure):
     """ssm_delta_prep: the fused step-size preparation."""
     _fields_ = [("dt_bias", ctypes.c_void_p), ("softplus", ctypes.c_int32),
@@ -103,6 +109,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_scan_fwd_host_static.argtypes = [P, P, P, P, P, P, P, P, P, P, SP, I32, P]
     lib.ssm_scan_host_static_capacity.restype = SZ
     lib.ssm_scan_host_static_capacity.argtypes = []
+    lib.ssm_ssd_fwd.restype = I32
+    lib.ssm_ssd_fwd.argtypes = [P] * 11 + [ctypes.POINTER(SsdShapes), I32, P]
     lib.ssm_scan_bwd.restype = I32
     lib.ssm_scan_bwd.argtypes = [P] * 19 + [SP, I32, P]
     lib.ssm_decode_step.restype = I32
@@ -444,6 +452,57 @@ def scan_bwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_states,
     if st != 0:
         raise SsmError(st, "ssm_scan_bwd")
     return out
+
+
+def ssd_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, nheads: int, h0=None,
+            want_final: bool = False, out=None, out_final=None, stream=None):
+    """The SSD form of the scan (one decay per head) on the tensor cores.
+
+    x, z: bf16 [batch, L, nheads * headdim]; delta: bf16 [batch, L, nheads];
+    A: fp32 [nheads]; B, C: bf16 [batch, L, dstate]; D: fp32 [nheads * headdim];
+    valid_len: int32 [batch]; h0: fp32 [batch, nheads * headdim, dstate].
+    Returns y, or (y, final_state) with ``want_final``."""
+    import torch
+    lib = load()
+    if x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev, dt = x.device, x.dtype
+    code = _dtype_code(dt)
+    batch, L, dim = x.shape
+    if dim % nheads:
+        raise ValueError("the channel count must be a multiple of nheads")
+    headdim = dim // nheads
+    dstate = B.shape[-1]
+    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, nheads), dt),
+                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
+                                ("A", A, (nheads,), torch.float32)):
+        _check(t, name, shape, tdt, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, dev)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, dstate), torch.float32, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", (batch, L, dim), dt, dev)
+    fin = None
+    if want_final:
+        fin = torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev) \
+            if out_final is None else out_final
+        _check(fin, "out_final", (batch, dim, dstate), torch.float32, dev)
+    s = SsdShapes(batch, L, nheads, headdim, dstate)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        st = lib.ssm_ssd_fwd(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                             _ptr(valid_len), _ptr(h0), _ptr(y), _ptr(fin), ctypes.byref(s),
+                             int(code), ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_ssd_fwd")
+    return (y, fin) if want_final else y
 
 
 def static_capacity() -> int:

@@ -10,6 +10,7 @@
 #include <new>
 
 #include "ssmscan.h"
+#include "ssd.h"
 #include "tiers.h"
 
 namespace {
@@ -372,6 +373,40 @@ const char* ssm_kernel_name(ssm_kernel kernel) {
     case SSM_KERNEL_STREAM: return "stream";
   }
   return "unknown";
+}
+
+ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const void* B,
+                       const void* C, const float* D, const void* z, const int32_t* valid_len,
+                       const float* h0, void* out_y, float* out_final_state,
+                       const ssm_ssd_shapes* shapes, ssm_dtype dtype, cudaStream_t stream) {
+  if (!shapes) return SSM_ERR_NULL;
+  if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+  const ssm_ssd_shapes& s = *shapes;
+  if (s.batch < 1 || s.seqlen < 0 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1)
+    return SSM_ERR_SHAPE;
+  if (dtype != SSM_BF16 || s.headdim != ssm::kSsdHeadDim || s.dstate != ssm::kSsdState)
+    return SSM_ERR_UNSUPPORTED;
+  int64_t dim, bl, bld, bln, bdn, bh;
+  const int64_t lim = int64_t(1) << 60;
+  if (!mul_ok(s.nheads, s.headdim, &dim) || !mul_ok(s.batch, s.seqlen, &bl) ||
+      !mul_ok(bl, dim, &bld) || !mul_ok(bl, s.dstate, &bln) || !mul_ok(s.batch, dim, &bdn) ||
+      !mul_ok(bdn, s.dstate, &bdn) || !mul_ok(s.batch, s.nheads, &bh) || bld > lim ||
+      bln > lim || bdn > lim || bh > 0x7FFFFFFF)
+    return SSM_ERR_SHAPE;
+  if (!x || !delta || !A || !B || !C || !out_y) return SSM_ERR_NULL;
+  if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(out_y, 16) ||
+      (z && !aligned(z, 16)) || !aligned(delta, 2) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (h0 && !aligned(h0, 4)) || (out_final_state && !aligned(out_final_state, 4)) ||
+      (valid_len && !aligned(valid_len, 4)))
+    return SSM_ERR_ALIGN;
+  ssm::SsdParams p;
+  p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+  p.valid_len = valid_len; p.h0 = h0; p.y = out_y; p.h_final = out_final_state;
+  p.batch = s.batch; p.seqlen = s.seqlen; p.nheads = s.nheads; p.headdim = s.headdim;
+  p.dstate = s.dstate;
+  p.err = ssm::stream::error_word();
+  if (!p.err) return SSM_ERR_CUDA;
+  return ssm::launch_ssd(p, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 int64_t ssm_chunk_count(const ssm_shapes* shapes) {

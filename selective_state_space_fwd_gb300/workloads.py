@@ -91,6 +91,67 @@ DECODE_WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    """A workload of the SSD form (one decay per head): channels in nheads heads
+    of headdim, bf16 I/O.  Mamba 2's usual settings: headdim 64, dstate 128,
+    A_h = -U(1, 16), delta = softplus(0.5 N(0,1) + dt_bias_h) with
+    dt_bias_h = softplus^-1(U(1e-3, 1e-1)), D = 1, x, z, B, C ~ N(0, 1)."""
+    key: int
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    gate: bool
+    mask: tuple[int, int] | None
+    seed: int
+
+    def scaled(self, **kw) -> "SsdWorkload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def dim(self) -> int:
+        return self.nheads * self.headdim
+
+    @property
+    def elements(self) -> int:
+        return self.batch * self.seqlen * self.dim
+
+
+SSD_WORKLOADS = {
+    1: SsdWorkload(201, "ssd-bf16-gated-b8-l4096-h32-p64-n128", 8, 4096, 32, 64, 128, True, None,
+                   21),
+}
+
+
+def make_ssd_inputs(w: SsdWorkload) -> dict:
+    """All inputs of an SSD workload: x, z [batch, L, nheads*headdim], delta
+    [batch, L, nheads], B, C [batch, L, dstate] as bf16 bit patterns; A
+    [nheads], D [nheads*headdim] fp32; valid_len int32 [batch] or None."""
+    Bt, L, H, N = w.batch, w.seqlen, w.nheads, w.dstate
+    act = (Bt, L, w.dim)
+    x = _normal(_rng(w.seed, _X), act)
+    u = _rng(w.seed, _DTBIAS).uniform(1e-3, 1e-1, H)
+    dt_bias = np.log(np.expm1(u))
+    g = _normal(_rng(w.seed, _DELTA), (Bt, L, H)).astype(np.float64)
+    delta = _softplus64(0.5 * g + dt_bias[None, None, :]).astype(np.float32)
+    A = -_rng(w.seed, _D).uniform(1.0, 16.0, H).astype(np.float32)
+    Bm = _normal(_rng(w.seed, _B), (Bt, L, N))
+    Cm = _normal(_rng(w.seed, _C), (Bt, L, N))
+    D = np.ones(w.dim, dtype=np.float32)
+    z = _normal(_rng(w.seed, _Z), act) if w.gate else None
+    valid = None
+    if w.mask is not None:
+        lo, hi = w.mask
+        valid = _rng(w.seed, _VALID).integers(lo, hi + 1, size=Bt).astype(np.int32)
+    x, delta, Bm, Cm = (f32_to_bf16_bits(t) for t in (x, delta, Bm, Cm))
+    z = f32_to_bf16_bits(z) if z is not None else None
+    return dict(x=x, delta=delta, A=A, B=Bm, C=Cm, D=D, z=z, valid_len=valid, dtype="bf16",
+                nheads=H)
+
+
 def make_raw_delta(w: Workload):
     """For the softplus recipe: the step inputs before the fused preparation,
     raw = 0.5 N(0,1) [batch, L, dim] (I/O dtype) and dt_bias [dim] fp32, from

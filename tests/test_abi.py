@@ -11,7 +11,7 @@ EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_f
             "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_bwd", "ssm_scan_plan",
             "ssm_scan_fwd_host_static", "ssm_scan_host_static_capacity", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
-            "ssm_kernel_name", "ssm_version", "ssm_check_device_errors"}
+            "ssm_kernel_name", "ssm_version", "ssm_check_device_errors", "ssm_ssd_fwd"}
 
 
 def test_every_declared_symbol_is_exported(ssmlib):
@@ -172,6 +172,40 @@ def _bwd(shapes=(2, 8, 4, 16, 4), z=None, dz=None, states=FAKE, dA=FAKE, x=FAKE,
 ])
 def test_bwd_argument_errors_return_status(ssmlib, kw, status):
     assert _bwd(**kw) == status
+
+
+def _ssd(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None, h0=None,
+         y=FAKE, final=None, shapes=(2, 256, 4, 64, 128), dtype=1, shapes_ptr=True):
+    P = ctypes.c_void_p
+    s = Bd.SsdShapes(*shapes)
+    return Bd.load().ssm_ssd_fwd(P(x), P(delta), P(A), P(B), P(C), P(D), P(z), P(valid), P(h0),
+                                 P(y), P(final), ctypes.byref(s) if shapes_ptr else None, dtype,
+                                 None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(shapes_ptr=False), Bd.Status.ERR_NULL),
+    (dict(x=None), Bd.Status.ERR_NULL),
+    (dict(delta=None), Bd.Status.ERR_NULL),
+    (dict(A=None), Bd.Status.ERR_NULL),
+    (dict(y=None), Bd.Status.ERR_NULL),
+    (dict(shapes=(0, 256, 4, 64, 128)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, -1, 4, 64, 128)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 256, 0, 64, 128)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(1 << 40, 1 << 30, 4, 64, 128)), Bd.Status.ERR_SHAPE),
+    (dict(dtype=0), Bd.Status.ERR_UNSUPPORTED),
+    (dict(dtype=7), Bd.Status.ERR_UNSUPPORTED),
+    (dict(shapes=(2, 256, 4, 32, 128)), Bd.Status.ERR_UNSUPPORTED),
+    (dict(shapes=(2, 256, 4, 64, 16)), Bd.Status.ERR_UNSUPPORTED),
+    (dict(x=FAKE + 8), Bd.Status.ERR_ALIGN),
+    (dict(B=FAKE + 2), Bd.Status.ERR_ALIGN),
+    (dict(y=FAKE + 4), Bd.Status.ERR_ALIGN),
+    (dict(z=FAKE + 8), Bd.Status.ERR_ALIGN),
+    (dict(delta=FAKE + 1), Bd.Status.ERR_ALIGN),
+    (dict(h0=FAKE + 2), Bd.Status.ERR_ALIGN),
+])
+def test_ssd_argument_errors_return_status(ssmlib, kw, status):
+    assert _ssd(**kw) == status
 
 
 def test_plan_serial_always_available(ssmlib):

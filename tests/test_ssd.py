@@ -1,0 +1,133 @@
+"""The SSD form (``ssm_ssd_fwd``, one decay per head, tensor-core products) on a
+GPU, against the fp64 oracle's SSD form.
+
+Tolerance, derived from the arithmetic: the products take bf16 operands (the
+inputs as stored, delta-scaled B rows, the decay-weighted and masked block
+matrix, x decayed to the block end, and the state entering a block), each
+rounded once to 8 significant bits (relative 2^-9), and accumulate in fp32;
+y is stored in bf16.  Sums of such terms stay within a few 2^-9 of the
+largest output, so y is checked to 1e-2 max-normalised (the bound of every
+bf16 output of the library) and the final state, which passes through the
+same rounded operands but is stored in fp32, to 1e-2 as well.
+"""
+import numpy as np
+import pytest
+import torch
+
+import selective_state_space_fwd_gb300 as S
+from selective_state_space_fwd_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL_Y = 1e-2
+TOL_STATE = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(ssmlib, oracle):
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    yield
+
+
+def rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+BASE = W.SSD_WORKLOADS[1]
+CASES = {
+    # several blocks of 128 steps with a ragged tail, gate, initial state
+    "b2-l300-h3-gate-h0": dict(w=dict(batch=2, seqlen=300, nheads=3, gate=True), h0=True),
+    # masked rows: one empty, one ending inside a block, one ending on a block edge
+    "b3-l384-h2-mask": dict(w=dict(batch=3, seqlen=384, nheads=2, gate=True), h0=True,
+                            valid=[384, 0, 128]),
+    "b2-l260-h2-mask-ragged": dict(w=dict(batch=2, seqlen=260, nheads=2, gate=False), h0=False,
+                                   valid=[200, 131]),
+    # exactly one block, no gate, no D
+    "b1-l128-h1-noD": dict(w=dict(batch=1, seqlen=128, nheads=1, gate=False), h0=False,
+                           no_d=True),
+    # a single step
+    "b2-l1-h2": dict(w=dict(batch=2, seqlen=1, nheads=2, gate=True), h0=True),
+    # long enough for the decay between blocks to matter, several heads
+    "b1-l1100-h4": dict(w=dict(batch=1, seqlen=1100, nheads=4, gate=True), h0=False),
+}
+
+
+def _run(case):
+    w = BASE.scaled(**case["w"])
+    inp = W.make_ssd_inputs(w)
+    if case.get("valid") is not None:
+        inp["valid_len"] = np.array(case["valid"], np.int32)
+    if case.get("no_d"):
+        inp["D"] = None
+    rng = np.random.default_rng(83)
+    h0 = rng.standard_normal((w.batch, w.dim, w.dstate)).astype(np.float32) if case["h0"] else None
+    t = W.to_torch(inp, "cuda")
+    h0t = torch.from_numpy(h0).cuda() if h0 is not None else None
+    y, fin = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                       t["valid_len"], nheads=w.nheads, h0=h0t, want_final=True)
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    return w, inp, h0, y, fin
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_ssd_matches_oracle(oracle, name):
+    case = CASES[name]
+    w, inp, h0, y, fin = _run(case)
+    y_ref, f_ref = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["valid_len"], h0, nheads=w.nheads,
+                                  want_final=True)
+    yg = y.float().cpu().numpy().astype(np.float64)
+    fg = fin.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(yg)) and np.all(np.isfinite(fg))
+    ey, ef = rel(yg, y_ref), rel(fg, f_ref)
+    assert ey <= TOL_Y, f"y rel err {ey:.3e}"
+    assert ef <= TOL_STATE, f"final state rel err {ef:.3e}"
+    if inp["valid_len"] is not None:
+        for b, v in enumerate(inp["valid_len"]):
+            assert np.all(yg[b, int(v):] == 0)  # past valid_len the output is exactly 0
+
+
+def test_ssd_split_equals_whole(oracle):
+    """Running [0, 256) and then [256, L) from the first call's final state
+    gives the single call's outputs: the carry between blocks is the state."""
+    w = BASE.scaled(batch=2, seqlen=400, nheads=2, gate=True)
+    inp = W.make_ssd_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    y, fin = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], None,
+                       nheads=w.nheads, want_final=True)
+    k = 256
+    part = {n: t[n][:, :k].contiguous() for n in ("x", "delta", "B", "C", "z")}
+    rest = {n: t[n][:, k:].contiguous() for n in ("x", "delta", "B", "C", "z")}
+    y1, f1 = S.ssd_fwd(part["x"], part["delta"], t["A"], part["B"], part["C"], t["D"], part["z"],
+                       None, nheads=w.nheads, want_final=True)
+    y2, f2 = S.ssd_fwd(rest["x"], rest["delta"], t["A"], rest["B"], rest["C"], t["D"], rest["z"],
+                       None, nheads=w.nheads, h0=f1, want_final=True)
+    torch.cuda.synchronize()
+    # the same arithmetic on the same blocks: identical results
+    assert torch.equal(torch.cat([y1, y2], dim=1), y)
+    assert torch.equal(f2, fin)
+
+
+def test_ssd_full_size_sampled(oracle):
+    """The benchmark's workload at full size, in the launch configuration the
+    benchmark times; the oracle checks sampled (batch row, head) pairs, every
+    channel of the head over the whole sequence."""
+    w = BASE
+    inp = W.make_ssd_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    y = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], None,
+                  nheads=w.nheads)
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    P = w.headdim
+    for b, h in ((0, 0), (3, 17), (7, w.nheads - 1)):
+        ch = slice(h * P, (h + 1) * P)
+        sub = dict(x=inp["x"][b:b + 1, :, ch], delta=inp["delta"][b:b + 1, :, h:h + 1],
+                   A=inp["A"][h:h + 1], B=inp["B"][b:b + 1], C=inp["C"][b:b + 1],
+                   D=inp["D"][ch], z=inp["z"][b:b + 1, :, ch])
+        y_ref = oracle.ssd_fwd(*(np.ascontiguousarray(sub[k]) for k in
+                                 ("x", "delta", "A", "B", "C", "D", "z")), nheads=1)
+        yg = y[b:b + 1, :, ch].float().cpu().numpy().astype(np.float64)
+        e = rel(yg, y_ref)
+        assert e <= TOL_Y, f"(b={b}, h={h}) y rel err {e:.3e}"
