@@ -4,26 +4,31 @@
 // from block to block by the recurrence itself).
 //
 // Per head h with decay a_t = exp(delta_t A_h) and a block of Q = 128 steps,
-// write cs_t = sum_{r<=t} delta_r A_h (in log2 units) inside the block and
-// S for the state entering it ([N x P]: state n, channel p of the head):
-//   G'[t,s] = C_t . (delta_s B_s)                          (tensor cores, K = N)
-//   Ym[t,s] = G'[t,s] 2^(cs_t - cs_s) for s <= t, else 0   (registers)
-//   Yd      = Ym x                                         (tensor cores, K = Q)
-//   Yo      = C S                                          (tensor cores, K = N)
+// write cs_t = sum_{r<=t} delta_r A_h (in log2 units) inside the block,
+// e_s = cs_s - log2(delta_s) and S for the state entering the block ([N x P]:
+// state n, channel p of the head):
+//   G[t,s]  = C_t . B_s                                     (tensor cores, K = N)
+//   Ym[t,s] = G[t,s] 2^(cs_t - e_s) for s <= t, else 0      (registers)
+//   Yd      = Ym x                                          (tensor cores, K = Q)
+//   Yo      = C S                                           (tensor cores, K = N)
 //   y_t     = (Yd_t + 2^cs_t Yo_t + D x_t) silu(z_t)
-//   S      <- 2^cs_end S + (delta B)^T (2^(cs_end - cs_s) x_s)   (tensor cores, K = Q)
+//   S      <- 2^cs_end S + B^T (delta_s 2^(cs_end - cs_s) x_s)   (tensor cores, K = Q)
 // which is the recurrence regrouped: the output of step t is the inputs of
 // the block weighted by the decay between their step and t, plus the state
-// entering the block decayed to t.  Operands are bf16 in shared memory in
-// the non-swizzled core-matrix layout (umma.cuh), products accumulate in
-// fp32 in tensor memory, and the state stays fp32 in registers between
-// blocks (rounded to bf16 only as an operand of Yo).
+// entering the block decayed to t.  Operands are bf16 in shared memory in the
+// non-swizzled core-matrix layout (umma.cuh), products accumulate in fp32 in
+// tensor memory, and the state stays fp32 in registers between blocks
+// (rounded to bf16 only as an operand of Yo).
 //
-// One CTA of 128 threads per (batch row, head), blocks in order.  Thread i is
-// step i of the block when staging and in the epilogue (TMEM lane i holds row
-// i of G', Yd and Yo) and state row i for the state update (lane i of dS).
-// Shared memory is about 113 KB, so two CTAs share an SM and one CTA's
-// staging and epilogue overlap the other's matrix products.
+// One CTA of 128 threads per (batch row, head), blocks in order.  The C, B
+// and x tiles of a block arrive by TMA, one 16-byte column strip of 128 rows
+// per copy, which is exactly a column of core matrices; threads write only
+// the scaled x and the state.  Thread i is step i of the block for the
+// masked block matrix and the epilogue (TMEM lane i holds row i of G, Yd and
+// Yo) and state row i for the state update (lane i of dS).  Shared memory is
+// about 113 KB, so two CTAs share an SM and one CTA's copies, staging and
+// epilogue overlap the other's matrix products.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -37,26 +42,29 @@ constexpr int Q = kSsdChunk, P = kSsdHeadDim, N = kSsdState;
 constexpr int kThreads = 128;
 constexpr unsigned kSsdWaitLimit = 1u << 24;  // try_wait polls before a wait gives up
 constexpr unsigned kErrSsdWait = 2u;
-static_assert(N == Q, "the C / B tile and the masked-G tile share one layout");
+static_assert(N == Q, "the C / B tile and the masked block matrix share one layout");
 
-// Tiles (byte offsets in dynamic shared memory).  A K-major [rows x K] tile
-// puts core matrix (r8, k8) at r8 * (K / 8) * 128 + k8 * 128; an MN-major
-// tile of MN extent E puts core matrix (mn8, k8) at k8 * (E / 8) * 128 + mn8 * 128.
-constexpr uint32_t kTileC = 0;                    // C rows, K-major [t x n]
-constexpr uint32_t kTileB = kTileC + Q * N * 2;   // delta-scaled B rows, K-major [s x n]; then Ym [t x s]
-constexpr uint32_t kTileX = kTileB + Q * N * 2;   // x, MN-major [p x s]
-constexpr uint32_t kTileXw = kTileX + Q * P * 2;  // x decayed to the block end, MN-major [p x s]
-constexpr uint32_t kTileS = kTileXw + Q * P * 2;  // state entering the block, MN-major [p x n]
-constexpr uint32_t kCs = kTileS + N * P * 2;      // cs per step of the block, fp32 [Q]
-constexpr uint32_t kDs = kCs + Q * 4;             // D of the head's channels, fp32 [P]
+// Every tile is a set of column strips: strip c holds 16 bytes (8 bf16) of
+// each of the 128 rows, row r at c * kStrip + r * 16.  Read as an operand,
+// core matrix (r8, c) sits at c * kStrip + r8 * 128: a K-major operand when
+// the strips run along K (K stride kStrip, M/N stride 128), an MN-major one
+// when they run along M/N (K stride 128, M/N stride kStrip).
+constexpr uint32_t kStrip = Q * 16;
+constexpr uint32_t kTileC = 0;                    // C rows [t x n], strips along n
+constexpr uint32_t kTileB = kTileC + N * Q * 2;   // B rows [s x n], strips along n; then Ym [t x s]
+constexpr uint32_t kTileX = kTileB + N * Q * 2;   // x rows [s x p], strips along p
+constexpr uint32_t kTileXw = kTileX + P * Q * 2;  // delta_s 2^(cs_end - cs_s) x_s, as x
+constexpr uint32_t kTileS = kTileXw + P * Q * 2;  // state rows [n x p] entering the block, as x
+constexpr uint32_t kE = kTileS + P * N * 2;       // e_s per step of the block, fp32 [Q]
+constexpr uint32_t kDs = kE + Q * 4;              // D of the head's channels, fp32 [P]
 constexpr uint32_t kWarpTot = kDs + P * 4;        // per-warp totals of the scan of cs
-constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier
-constexpr uint32_t kSlot = kBar + 8;              // TMEM base address
+constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier of the matrix products
+constexpr uint32_t kTBar = kBar + 8;              // mbarrier of the TMA copies
+constexpr uint32_t kSlot = kTBar + 8;             // TMEM base address
 constexpr uint32_t kSmemBytes = kSlot + 8;
-constexpr uint32_t kRowK = (N / 8) * 128;  // core-matrix row stride of the K-major tiles (2048)
-constexpr uint32_t kRowX = (P / 8) * 128;  // K-direction stride of the MN-major tiles (1024)
+constexpr uint32_t kTmaBytes = (2 * N + P) * Q * 2;  // C, B and x tiles of one block
 
-// TMEM columns (fp32): G' [0,128) then Yd [0,64); Yo [128,192); dS [192,256).
+// TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); dS [192,256).
 constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColDS = 192, kTmemCols = 256;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -74,63 +82,81 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 __device__ __forceinline__ uint4 pack8(const float* f) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
-__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
+// Shared-memory accesses at byte offsets from the dynamic base.
+__device__ __forceinline__ void sts128(unsigned char* base, uint32_t off, const uint4& v) {
+  *reinterpret_cast<uint4*>(base + off) = v;
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+__device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<const uint4*>(base + off);
 }
 __device__ __forceinline__ uint4 ldg128(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
+// log2 with the MUFU unit (PTX lg2.approx.ftz.f32): -inf at 0.
+__device__ __forceinline__ float lg2(float v) {
+  float r;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
 
 template <bool GATE>
-__global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kThreads, 2)
+    ssd_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_b,
+               const __grid_constant__ CUtensorMap tm_x, const SsdParams p) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t H = p.nheads, L = p.seqlen, Dm = p.nheads * P;
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const uint32_t s0 = umma::smem_u32(sm);
-  const uint32_t bar = s0 + kBar;
-  float* sCs = reinterpret_cast<float*>(sm + kCs);
+  const uint32_t bar = s0 + kBar, tbar = s0 + kTBar;
+  float* sE = reinterpret_cast<float*>(sm + kE);
   float* sD = reinterpret_cast<float*>(sm + kDs);
   float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
-  const auto* xg = static_cast<const __nv_bfloat16*>(p.x);
   const auto* zg = static_cast<const __nv_bfloat16*>(p.z);
-  const auto* Bg = static_cast<const __nv_bfloat16*>(p.B);
-  const auto* Cg = static_cast<const __nv_bfloat16*>(p.C);
   auto* yg = static_cast<__nv_bfloat16*>(p.y);
-
-  if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
-  if (tid == 0) umma::mbar_init(bar, 1);
-  if (tid < P) sD[tid] = p.D ? __ldg(p.D + h * P + tid) : 0.f;
-  umma::fence_before_sync();
-  __syncthreads();
-  umma::fence_after_sync();
-  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kSlot);
-  const uint32_t tl = tm + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
 
   int64_t Lv = L;
   if (p.valid_len) {
     Lv = p.valid_len[b];
     Lv = Lv < 0 ? 0 : (Lv > L ? L : Lv);
   }
-  const float al = __ldg(p.A + h) * kLog2e;  // A_h in log2 units
+  // the C, B and x tiles of the block starting at step t0, by one thread
+  auto issue_copies = [&](int64_t t0) {
+    const int row = static_cast<int>(b * L + t0);
+    umma::mbar_expect_tx(tbar, kTmaBytes);
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      umma::tma_load_2d(s0 + kTileC + c * kStrip, &tm_c, c * 8, row, tbar);
+      umma::tma_load_2d(s0 + kTileB + c * kStrip, &tm_b, c * 8, row, tbar);
+    }
+#pragma unroll
+    for (int c = 0; c < P / 8; ++c)
+      umma::tma_load_2d(s0 + kTileX + c * kStrip, &tm_x, static_cast<int>(h * P) + c * 8, row,
+                        tbar);
+  };
+
+  if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
+  if (tid == 0) {
+    umma::mbar_init(bar, 1);
+    umma::mbar_init(tbar, 1);
+    if (Lv > 0) issue_copies(0);
+  }
+  if (tid < P) sD[tid] = p.D ? __ldg(p.D + h * P + tid) : 0.f;
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kSlot);
+  const uint32_t tl = tm + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
+  const float al = __ldg(p.A + h) * kLog2e;                           // A_h in log2 units
+  const uint32_t rowo = tid * 16;  // this thread's row in every strip
 
   // S[n][p] for this thread's state row n = tid
   float S[P];
 #pragma unroll
   for (int j = 0; j < P; ++j) S[j] = p.h0 ? p.h0[((b * Dm + h * P + j) * N) + tid] : 0.f;
 
-  uint32_t phase = 0;
-  bool bad = false;
+  uint32_t phase = 0, tphase = 0;
+  bool bad = false, copying = Lv > 0;
   for (int64_t t0 = 0; t0 < L; t0 += Q) {
     const int64_t t = t0 + tid;
     const bool in = t < Lv;  // a valid step (Lv <= L)
@@ -143,8 +169,15 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       }
       continue;
     }
-    // step size and the inclusive scan of delta A over the block
-    const float dt = in ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.delta)[row * H + h]) : 0.f;
+    // step size, the gate row, and the inclusive scan of delta A over the block
+    const float dt =
+        in ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.delta)[row * H + h]) : 0.f;
+    uint4 zr[GATE ? P / 8 : 1];
+    if (GATE) {
+#pragma unroll
+      for (int c = 0; c < P / 8; ++c)
+        zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
+    }
     float cs = dt * al;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -161,41 +194,33 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       tot += v;
     }
     cs += pre;
-    sCs[tid] = cs;
-    const float wend = ex2(tot - cs);  // decay from step t to the end of the block
+    sE[tid] = cs - lg2(dt);            // +inf past valid_len: its column of Ym is 0
+    const float u = dt * ex2(tot - cs);  // weight of step t in the state at the block end
 
-    // stage this step's rows (zero rows past valid_len, so that nothing there
-    // reaches a product)
-    const uint32_t rk = (tid >> 3) * kRowK + (tid & 7) * 16;  // row tid of a K-major tile
-    const uint32_t rx = (tid >> 3) * kRowX + (tid & 7) * 16;  // K-row tid of an MN-major tile
-#pragma unroll
-    for (int c = 0; c < N / 8; ++c) {
-      const uint4 v = in ? ldg128(Cg + row * N + c * 8) : make_uint4(0, 0, 0, 0);
-      sts128(s0 + kTileC + rk + c * 128, v);
+    if (umma::mbar_wait(tbar, tphase, kSsdWaitLimit)) {
+      tphase ^= 1;
+      copying = false;
+    } else {
+      bad = true;  // the copies stay pending: waited for again before exit
     }
+    if (__syncthreads_or(bad)) { bad = true; break; }
+    // rows past valid_len (or past the sequence) must not reach a product: zero
+    // them in the B and x tiles
+    if (!in) {
 #pragma unroll
-    for (int c = 0; c < N / 8; ++c) {
-      const uint4 v = in ? ldg128(Bg + row * N + c * 8) : make_uint4(0, 0, 0, 0);
-      float f[8];
-      unpack8(v, f);
+      for (int c = 0; c < N / 8; ++c) sts128(sm, kTileB + c * kStrip + rowo, make_uint4(0, 0, 0, 0));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] *= dt;
-      sts128(s0 + kTileB + rk + c * 128, pack8(f));
+      for (int c = 0; c < P / 8; ++c) sts128(sm, kTileX + c * kStrip + rowo, make_uint4(0, 0, 0, 0));
     }
-    uint4 zr[GATE ? P / 8 : 1];
 #pragma unroll
     for (int c = 0; c < P / 8; ++c) {
-      const uint4 v = in ? ldg128(xg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
-      sts128(s0 + kTileX + rx + c * 128, v);
       float f[8];
-      unpack8(v, f);
+      unpack8(in ? lds128(sm, kTileX + c * kStrip + rowo) : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] *= wend;
-      sts128(s0 + kTileXw + rx + c * 128, pack8(f));
-      if (GATE) zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < 8; ++j) f[j] *= u;
+      sts128(sm, kTileXw + c * kStrip + rowo, pack8(f));
+      sts128(sm, kTileS + c * kStrip + rowo, pack8(S + c * 8));
     }
-#pragma unroll
-    for (int c = 0; c < P / 8; ++c) sts128(s0 + kTileS + rx + c * 128, pack8(S + c * 8));
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -206,17 +231,17 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       constexpr uint32_t idO = umma::idesc_bf16(128, P, false, true);
       constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
 #pragma unroll
-      for (int k = 0; k < N / 16; ++k)  // G' = C (delta B)^T
-        umma::mma_bf16(tm + kColG, umma::smem_desc(s0 + kTileC + k * 256, 128, kRowK),
-                       umma::smem_desc(s0 + kTileB + k * 256, 128, kRowK), idG, k > 0);
+      for (int k = 0; k < N / 16; ++k)  // G = C B^T
+        umma::mma_bf16(tm + kColG, umma::smem_desc(s0 + kTileC + k * 2 * kStrip, kStrip, 128),
+                       umma::smem_desc(s0 + kTileB + k * 2 * kStrip, kStrip, 128), idG, k > 0);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)  // Yo = C S
-        umma::mma_bf16(tm + kColYo, umma::smem_desc(s0 + kTileC + k * 256, 128, kRowK),
-                       umma::smem_desc(s0 + kTileS + k * 2 * kRowX, kRowX, 128), idO, k > 0);
+        umma::mma_bf16(tm + kColYo, umma::smem_desc(s0 + kTileC + k * 2 * kStrip, kStrip, 128),
+                       umma::smem_desc(s0 + kTileS + k * 256, 128, kStrip), idO, k > 0);
 #pragma unroll
-      for (int k = 0; k < Q / 16; ++k)  // dS = (delta B)^T (x decayed to the block end)
-        umma::mma_bf16(tm + kColDS, umma::smem_desc(s0 + kTileB + k * 2 * kRowK, kRowK, 128),
-                       umma::smem_desc(s0 + kTileXw + k * 2 * kRowX, kRowX, 128), idS, k > 0);
+      for (int k = 0; k < Q / 16; ++k)  // dS = B^T Xw
+        umma::mma_bf16(tm + kColDS, umma::smem_desc(s0 + kTileB + k * 256, 128, kStrip),
+                       umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, k > 0);
       umma::mma_commit(bar);
     }
     __syncwarp();
@@ -232,10 +257,16 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       if (sb <= warp) {  // warp-uniform: columns past the warp's last row are all masked
         float g[32];
         umma::tmem_ld32(tl + kColG + sb * 32, g);
+        const float4* e4 = reinterpret_cast<const float4*>(sE + sb * 32);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int s = sb * 32 + j;
-          g[j] = s <= tid ? g[j] * ex2(cs - sCs[s]) : 0.f;
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 e = e4[j4];
+          const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = j4 * 4 + i, s = sb * 32 + j;
+            g[j] = s <= tid ? g[j] * ex2(cs - ev[i]) : 0.f;
+          }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) o[q] = pack8(g + q * 8);
@@ -244,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
         for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sts128(s0 + kTileB + rk + (sb * 4 + q) * 128, o[q]);
+      for (int q = 0; q < 4; ++q) sts128(sm, kTileB + (sb * 4 + q) * kStrip + rowo, o[q]);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -255,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       constexpr uint32_t idY = umma::idesc_bf16(128, P, false, true);
 #pragma unroll
       for (int k = 0; k < Q / 16; ++k)  // Yd = Ym x
-        umma::mma_bf16(tm + kColYd, umma::smem_desc(s0 + kTileB + k * 256, 128, kRowK),
-                       umma::smem_desc(s0 + kTileX + k * 2 * kRowX, kRowX, 128), idY, k > 0);
+        umma::mma_bf16(tm + kColYd, umma::smem_desc(s0 + kTileB + k * 2 * kStrip, kStrip, 128),
+                       umma::smem_desc(s0 + kTileX + k * 256, 128, kStrip), idY, k > 0);
       umma::mma_commit(bar);
     }
     __syncwarp();
@@ -276,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
       for (int q = 0; q < 4; ++q) {
         const int c = half * 4 + q;
         float xv[8], zv[8], o[8];
-        unpack8(lds128(s0 + kTileX + rx + c * 128), xv);
+        unpack8(lds128(sm, kTileX + c * kStrip + rowo), xv);
         if (GATE) unpack8(zr[c], zv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -296,14 +327,22 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) S[half * 32 + j] = fmaf(etot, S[half * 32 + j], ds[j]);
     }
+    // every tile is free again: the copies of the next block may start
+    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
+    if (t0 + Q < Lv) {
+      copying = true;
+      if (tid == 0) issue_copies(t0 + Q);
+    }
   }
 
   if (bad) {
     if (tid == 0) atomicOr(p.err, kErrSsdWait);
-    umma::mbar_wait(bar, phase ^ 1u, kSsdWaitLimit);  // the products still in flight, bounded
-  } else if (p.h_final) {
+    umma::mbar_wait(bar, phase ^ 1u, kSsdWaitLimit);  // products still in flight, bounded
+  }
+  if (copying) umma::mbar_wait(tbar, tphase, kSsdWaitLimit);  // copies still in flight, bounded
+  if (!bad && p.h_final) {
 #pragma unroll
     for (int j = 0; j < P; ++j) p.h_final[((b * Dm + h * P + j) * N) + tid] = S[j];
   }
@@ -312,8 +351,43 @@ __global__ void __launch_bounds__(kThreads, 2) ssd_kernel(const SsdParams p) {
   if (warp == 0) umma::tmem_dealloc(tm, kTmemCols);
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D map over a bf16 [rows, inner] tensor with a box of 8 elements x 128 rows
+// (one column strip of a tile); rows past the end read as zeros.
+bool strip_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows) {
+  EncodeTiledFn fn = encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(inner * 2)};
+  cuuint32_t box[2] = {8, cuuint32_t(Q)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool GATE>
-cudaError_t launch_g(const SsdParams& p, cudaStream_t s) {
+cudaError_t launch_g(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
+                     const SsdParams& p, cudaStream_t s) {
   auto* k = ssd_kernel<GATE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes));
@@ -321,7 +395,7 @@ cudaError_t launch_g(const SsdParams& p, cudaStream_t s) {
   e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.batch * p.nheads;
-  k<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(p);
+  k<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(mc, mb, mx, p);
   return cudaGetLastError();
 }
 
@@ -331,9 +405,14 @@ size_t ssd_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
   if (p.headdim != P || p.dstate != N || p.batch * p.nheads <= 0 ||
-      p.batch * p.nheads > 0x7FFFFFFF)
+      p.batch * p.nheads > 0x7FFFFFFF || p.batch * p.seqlen > 0x7FFFFFFF)
     return cudaErrorInvalidValue;
-  return p.z ? launch_g<true>(p, s) : launch_g<false>(p, s);
+  CUtensorMap mc, mb, mx;
+  const int64_t rows = p.batch * p.seqlen > 0 ? p.batch * p.seqlen : 1;
+  if (!strip_map(&mc, p.C, N, rows) || !strip_map(&mb, p.B, N, rows) ||
+      !strip_map(&mx, p.x, p.nheads * P, rows))
+    return cudaErrorInvalidValue;
+  return p.z ? launch_g<true>(mc, mb, mx, p, s) : launch_g<false>(mc, mb, mx, p, s);
 }
 
 }  // namespace ssm
