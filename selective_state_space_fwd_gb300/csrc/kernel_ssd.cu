@@ -42,27 +42,31 @@ constexpr int Q = kSsdChunk, P = kSsdHeadDim, N = kSsdState;
 constexpr int kThreads = 128;
 constexpr unsigned kSsdWaitLimit = 1u << 24;  // try_wait polls before a wait gives up
 constexpr unsigned kErrSsdWait = 2u;
+constexpr unsigned kErrSsdAlign = 4u;  // shared memory not 1024-byte aligned: nothing computed
 static_assert(N == Q, "the C / B tile and the masked block matrix share one layout");
 
-// Every tile is a set of column strips: strip c holds 16 bytes (8 bf16) of
-// each of the 128 rows, row r at c * kStrip + r * 16.  Read as an operand,
-// core matrix (r8, c) sits at c * kStrip + r8 * 128: a K-major operand when
-// the strips run along K (K stride kStrip, M/N stride 128), an MN-major one
-// when they run along M/N (K stride 128, M/N stride kStrip).
+// Two tile layouts.  The tiles that arrive by TMA (C, B, x) are 128-byte
+// swizzled: 64 bf16 of each of the 128 rows per 16 KB half, row r at r * 128,
+// its 16-byte chunk c stored at chunk c ^ (r mod 8), in 1024-byte atoms of 8
+// rows (the pattern the TMA writes and the tensor core reads).  The tiles that
+// threads write (Xw, S, Ym) are column strips: strip c holds 16 bytes (8 bf16)
+// of each of the 128 rows, row r at c * kStrip + r * 16; core matrix (r8, c)
+// then sits at c * kStrip + r8 * 128, a K-major operand when the strips run
+// along K and an MN-major one when they run along M/N.
 constexpr uint32_t kStrip = Q * 16;
-constexpr uint32_t kTileC = 0;                    // C rows [t x n], strips along n
-constexpr uint32_t kTileB = kTileC + N * Q * 2;   // B rows [s x n], strips along n; then Ym [t x s]
-constexpr uint32_t kTileX = kTileB + N * Q * 2;   // x rows [s x p], strips along p
+constexpr uint32_t kHalf = Q * 128;               // one 64-column half of a swizzled tile
+constexpr uint32_t kTileC = 0;                    // C rows [t x n], swizzled, halves n < 64, n >= 64
+constexpr uint32_t kTileB = kTileC + N * Q * 2;   // B rows [s x n], as C; then Ym [t x s] in strips
+constexpr uint32_t kTileX = kTileB + N * Q * 2;   // x rows [s x p], swizzled
 constexpr uint32_t kTileXw = kTileX + P * Q * 2;  // delta_s 2^(cs_end - cs_s) x_s, as x
 constexpr uint32_t kTileS = kTileXw + P * Q * 2;  // state rows [n x p] entering the block, as x
-constexpr uint32_t kE = kTileS + P * N * 2;       // e_s per step of the block, fp32 [Q]
-constexpr uint32_t kDs = kE + Q * 4;              // D of the head's channels, fp32 [P]
+constexpr uint32_t kDs = kTileS + P * N * 2;      // D of the head's channels, fp32 [P]
 constexpr uint32_t kWarpTot = kDs + P * 4;        // per-warp totals of the scan of cs
 constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier of the matrix products
 constexpr uint32_t kTBar = kBar + 8;              // mbarrier of the TMA copies
 constexpr uint32_t kSlot = kTBar + 8;             // TMEM base address
 constexpr uint32_t kSmemBytes = kSlot + 8;
-constexpr uint32_t kTmaBytes = (2 * N + P) * Q * 2;  // C, B and x tiles of one block
+constexpr uint32_t kTileBytesC = N * Q * 2, kTileBytesB = N * Q * 2, kTileBytesX = P * Q * 2;
 
 // TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); dS [192,256).
 constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColDS = 192, kTmemCols = 256;
@@ -92,6 +96,25 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* base, uint32_t off)
 __device__ __forceinline__ uint4 ldg128(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
+// Descriptor of a 128-byte-swizzled operand (layout type 2).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t k_stride, uint32_t mn_stride) {
+  return umma::smem_desc(addr, k_stride, mn_stride) | (uint64_t(2) << 61);
+}
+// K-major swizzled operand with 128 rows and K = 128 in two halves: the
+// descriptor of K step k (16 elements): half k / 4, 32 bytes per step inside
+// the 128-byte rows, 1024 bytes between 8-row groups.
+__device__ __forceinline__ uint64_t desc_kmaj_sw(uint32_t tile, int k) {
+  return desc_sw128(tile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+}
+// MN-major swizzled operand (rows along K): K step k is 16 rows = 2048 bytes,
+// 1024 bytes between 8-row groups, kHalf between 64-wide MN halves.
+__device__ __forceinline__ uint64_t desc_mnmaj_sw(uint32_t tile, int k) {
+  return desc_sw128(tile + k * 2048, kHalf, 1024);
+}
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a swizzled half
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
 // log2 with the MUFU unit (PTX lg2.approx.ftz.f32): -inf at 0.
 __device__ __forceinline__ float lg2(float v) {
   float r;
@@ -109,9 +132,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const uint32_t s0 = umma::smem_u32(sm);
   const uint32_t bar = s0 + kBar, tbar = s0 + kTBar;
-  float* sE = reinterpret_cast<float*>(sm + kE);
   float* sD = reinterpret_cast<float*>(sm + kDs);
   float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
+  // e_s and the column factors of the block matrix, in the x-scaled tile once
+  // the first products are done with it
+  float* sE = reinterpret_cast<float*>(sm + kTileXw);
+  float* sF = sE + Q;
+  const auto* dg = static_cast<const __nv_bfloat16*>(p.delta);
   const auto* zg = static_cast<const __nv_bfloat16*>(p.z);
   auto* yg = static_cast<__nv_bfloat16*>(p.y);
 
@@ -120,26 +147,34 @@ __global__ void __launch_bounds__(kThreads, 2)
     Lv = p.valid_len[b];
     Lv = Lv < 0 ? 0 : (Lv > L ? L : Lv);
   }
-  // the C, B and x tiles of the block starting at step t0, by one thread
-  auto issue_copies = [&](int64_t t0) {
-    const int row = static_cast<int>(b * L + t0);
-    umma::mbar_expect_tx(tbar, kTmaBytes);
-#pragma unroll
-    for (int c = 0; c < N / 8; ++c) {
-      umma::tma_load_2d(s0 + kTileC + c * kStrip, &tm_c, c * 8, row, tbar);
-      umma::tma_load_2d(s0 + kTileB + c * kStrip, &tm_b, c * 8, row, tbar);
-    }
-#pragma unroll
-    for (int c = 0; c < P / 8; ++c)
-      umma::tma_load_2d(s0 + kTileX + c * kStrip, &tm_x, static_cast<int>(h * P) + c * 8, row,
-                        tbar);
+  // Copies of the block starting at t0, by one thread: the C tile, and the B
+  // and x tiles.  The copy barrier takes two arrivals per block, one each.
+  auto copy_c = [&](int64_t t0) {
+    const int r = static_cast<int>(b * L + t0);
+    umma::mbar_expect_tx(tbar, kTileBytesC);
+    umma::tma_load_2d(s0 + kTileC, &tm_c, 0, r, tbar);
+    umma::tma_load_2d(s0 + kTileC + kHalf, &tm_c, 64, r, tbar);
   };
+  auto copy_bx = [&](int64_t t0) {
+    const int r = static_cast<int>(b * L + t0);
+    umma::mbar_expect_tx(tbar, kTileBytesB + kTileBytesX);
+    umma::tma_load_2d(s0 + kTileB, &tm_b, 0, r, tbar);
+    umma::tma_load_2d(s0 + kTileB + kHalf, &tm_b, 64, r, tbar);
+    umma::tma_load_2d(s0 + kTileX, &tm_x, static_cast<int>(h * P), r, tbar);
+  };
+  if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment; report, compute nothing
+    if (tid == 0) atomicOr(p.err, kErrSsdAlign);
+    return;
+  }
 
   if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
   if (tid == 0) {
     umma::mbar_init(bar, 1);
-    umma::mbar_init(tbar, 1);
-    if (Lv > 0) issue_copies(0);
+    umma::mbar_init(tbar, 2);
+    if (Lv > 0) {
+      copy_c(0);
+      copy_bx(0);
+    }
   }
   if (tid < P) sD[tid] = p.D ? __ldg(p.D + h * P + tid) : 0.f;
   umma::fence_before_sync();
@@ -156,7 +191,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int j = 0; j < P; ++j) S[j] = p.h0 ? p.h0[((b * Dm + h * P + j) * N) + tid] : 0.f;
 
   uint32_t phase = 0, tphase = 0;
-  bool bad = false, copying = Lv > 0;
+  int pending = Lv > 0 ? 2 : 0;  // arrivals made on the copy barrier's current phase
+  bool bad = false;
+  float dt_next = tid < Lv ? __bfloat162float(dg[(b * L + tid) * H + h]) : 0.f;
   for (int64_t t0 = 0; t0 < L; t0 += Q) {
     const int64_t t = t0 + tid;
     const bool in = t < Lv;  // a valid step (Lv <= L)
@@ -169,15 +206,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       continue;
     }
-    // step size, the gate row, and the inclusive scan of delta A over the block
-    const float dt =
-        in ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.delta)[row * H + h]) : 0.f;
+    const bool more = t0 + Q < Lv;  // the next block has valid steps
+    const float dt = dt_next;
+    dt_next = t + Q < Lv ? __bfloat162float(dg[(row + Q) * H + h]) : 0.f;
     uint4 zr[GATE ? P / 8 : 1];
     if (GATE) {
 #pragma unroll
       for (int c = 0; c < P / 8; ++c)
         zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
     }
+    // inclusive scan of delta A over the block
     float cs = dt * al;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -194,28 +232,36 @@ __global__ void __launch_bounds__(kThreads, 2)
       tot += v;
     }
     cs += pre;
-    sE[tid] = cs - lg2(dt);            // +inf past valid_len: its column of Ym is 0
+    const float e = cs - lg2(dt);  // +inf past valid_len: its column of Ym is 0
+    // column factor for the rows of later 32-step parts: delta_s 2^(cs_ref - cs_s),
+    // cs_ref = cs at the last step of this warp's part (<= delta_s)
+    const float colf = dt * ex2(__shfl_sync(0xFFFFFFFFu, cs, 31) - cs);
     const float u = dt * ex2(tot - cs);  // weight of step t in the state at the block end
 
     if (umma::mbar_wait(tbar, tphase, kSsdWaitLimit)) {
       tphase ^= 1;
-      copying = false;
+      pending = 0;
     } else {
       bad = true;  // the copies stay pending: waited for again before exit
     }
     if (__syncthreads_or(bad)) { bad = true; break; }
     // rows past valid_len (or past the sequence) must not reach a product: zero
-    // them in the B and x tiles
+    // them in the B and x tiles; this step's x row stays in registers
+    uint4 xr[P / 8];
+#pragma unroll
+    for (int c = 0; c < P / 8; ++c) xr[c] = in ? lds128(sm, kTileX + swz(tid, c)) : make_uint4(0, 0, 0, 0);
     if (!in) {
 #pragma unroll
-      for (int c = 0; c < N / 8; ++c) sts128(sm, kTileB + c * kStrip + rowo, make_uint4(0, 0, 0, 0));
-#pragma unroll
-      for (int c = 0; c < P / 8; ++c) sts128(sm, kTileX + c * kStrip + rowo, make_uint4(0, 0, 0, 0));
+      for (int c = 0; c < 8; ++c) {
+        sts128(sm, kTileB + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
+        sts128(sm, kTileB + kHalf + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
+        sts128(sm, kTileX + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
+      }
     }
 #pragma unroll
     for (int c = 0; c < P / 8; ++c) {
       float f[8];
-      unpack8(in ? lds128(sm, kTileX + c * kStrip + rowo) : make_uint4(0, 0, 0, 0), f);
+      unpack8(xr[c], f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] *= u;
       sts128(sm, kTileXw + c * kStrip + rowo, pack8(f));
@@ -232,15 +278,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)  // G = C B^T
-        umma::mma_bf16(tm + kColG, umma::smem_desc(s0 + kTileC + k * 2 * kStrip, kStrip, 128),
-                       umma::smem_desc(s0 + kTileB + k * 2 * kStrip, kStrip, 128), idG, k > 0);
+        umma::mma_bf16(tm + kColG, desc_kmaj_sw(s0 + kTileC, k), desc_kmaj_sw(s0 + kTileB, k), idG,
+                       k > 0);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)  // Yo = C S
-        umma::mma_bf16(tm + kColYo, umma::smem_desc(s0 + kTileC + k * 2 * kStrip, kStrip, 128),
+        umma::mma_bf16(tm + kColYo, desc_kmaj_sw(s0 + kTileC, k),
                        umma::smem_desc(s0 + kTileS + k * 256, 128, kStrip), idO, k > 0);
 #pragma unroll
       for (int k = 0; k < Q / 16; ++k)  // dS = B^T Xw
-        umma::mma_bf16(tm + kColDS, umma::smem_desc(s0 + kTileB + k * 256, 128, kStrip),
+        umma::mma_bf16(tm + kColDS, desc_mnmaj_sw(s0 + kTileB, k),
                        umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, k > 0);
       umma::mma_commit(bar);
     }
@@ -249,23 +295,49 @@ __global__ void __launch_bounds__(kThreads, 2)
     phase ^= 1;
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
+    // the C tile is free: the next block's copy may start
+    if (more) {
+      pending = 1;
+      if (tid == 0) copy_c(t0 + Q);
+    }
+    sE[tid] = e;
+    sF[tid] = colf;
+    __syncthreads();
 
-    // Ym row t = tid into the B tile (its products are done)
+    // Ym row t = tid into the B tile (its products are done).  Parts of 32
+    // columns before this warp's own: no mask, the decay factored into a row
+    // factor 2^(cs_t - cs_ref) <= 1 and the column factors; the warp's own
+    // part: the exact factor and the causal mask; later parts: zero.
+    float cref = 0.f;
 #pragma unroll
     for (int sb = 0; sb < Q / 32; ++sb) {
+      cref += sWt[sb];  // cs at the last step of part sb
       uint4 o[4];
-      if (sb <= warp) {  // warp-uniform: columns past the warp's last row are all masked
+      if (sb <= warp) {  // warp-uniform
         float g[32];
         umma::tmem_ld32(tl + kColG + sb * 32, g);
-        const float4* e4 = reinterpret_cast<const float4*>(sE + sb * 32);
+        if (sb < warp) {
+          const float rf = ex2(cs - cref);
+          const float4* f4 = reinterpret_cast<const float4*>(sF + sb * 32);
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 e = e4[j4];
-          const float ev[4] = {e.x, e.y, e.z, e.w};
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 f = f4[j4];
+            g[j4 * 4 + 0] *= f.x * rf;
+            g[j4 * 4 + 1] *= f.y * rf;
+            g[j4 * 4 + 2] *= f.z * rf;
+            g[j4 * 4 + 3] *= f.w * rf;
+          }
+        } else {
+          const float4* e4 = reinterpret_cast<const float4*>(sE + sb * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = j4 * 4 + i, s = sb * 32 + j;
-            g[j] = s <= tid ? g[j] * ex2(cs - ev[i]) : 0.f;
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 ee = e4[j4];
+            const float ev[4] = {ee.x, ee.y, ee.z, ee.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int j = j4 * 4 + i;
+              g[j] = j <= lane ? g[j] * ex2(cs - ev[i]) : 0.f;
+            }
           }
         }
 #pragma unroll
@@ -287,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int k = 0; k < Q / 16; ++k)  // Yd = Ym x
         umma::mma_bf16(tm + kColYd, umma::smem_desc(s0 + kTileB + k * 2 * kStrip, kStrip, 128),
-                       umma::smem_desc(s0 + kTileX + k * 256, 128, kStrip), idY, k > 0);
+                       desc_mnmaj_sw(s0 + kTileX, k), idY, k > 0);
       umma::mma_commit(bar);
     }
     __syncwarp();
@@ -295,6 +367,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     phase ^= 1;
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
+    // the B and x tiles are free: the next block's copies may start
+    if (more) {
+      pending = 2;
+      if (tid == 0) copy_bx(t0 + Q);
+    }
 
     // epilogue: y of step t = tid, then the state row n = tid
     const float eo = ex2(cs);
@@ -307,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int q = 0; q < 4; ++q) {
         const int c = half * 4 + q;
         float xv[8], zv[8], o[8];
-        unpack8(lds128(sm, kTileX + c * kStrip + rowo), xv);
+        unpack8(xr[c], xv);
         if (GATE) unpack8(zr[c], zv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -327,21 +404,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int j = 0; j < 32; ++j) S[half * 32 + j] = fmaf(etot, S[half * 32 + j], ds[j]);
     }
-    // every tile is free again: the copies of the next block may start
-    umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
-    if (t0 + Q < Lv) {
-      copying = true;
-      if (tid == 0) issue_copies(t0 + Q);
-    }
   }
 
   if (bad) {
     if (tid == 0) atomicOr(p.err, kErrSsdWait);
     umma::mbar_wait(bar, phase ^ 1u, kSsdWaitLimit);  // products still in flight, bounded
   }
-  if (copying) umma::mbar_wait(tbar, tphase, kSsdWaitLimit);  // copies still in flight, bounded
+  if (pending > 0) {  // copies still in flight (only after a wait gave up), bounded
+    if (pending == 1 && tid == 0) umma::mbar_arrive(tbar);  // the second arrival of the phase
+    umma::mbar_wait(tbar, tphase, kSsdWaitLimit);
+  }
   if (!bad && p.h_final) {
 #pragma unroll
     for (int j = 0; j < P; ++j) p.h_final[((b * Dm + h * P + j) * N) + tid] = S[j];
@@ -371,17 +445,17 @@ EncodeTiledFn encode() {
   return fn;
 }
 
-// 2-D map over a bf16 [rows, inner] tensor with a box of 8 elements x 128 rows
-// (one column strip of a tile); rows past the end read as zeros.
-bool strip_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows) {
+// 2-D map over a bf16 [rows, inner] tensor with a box of 64 elements x 128
+// rows, 128-byte swizzled (one half of a tile).  Rows past the end read as zeros.
+bool tile_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows) {
   EncodeTiledFn fn = encode();
   if (!fn) return false;
   cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(inner * 2)};
-  cuuint32_t box[2] = {8, cuuint32_t(Q)};
+  cuuint32_t box[2] = {64, cuuint32_t(Q)};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -409,8 +483,8 @@ cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   CUtensorMap mc, mb, mx;
   const int64_t rows = p.batch * p.seqlen > 0 ? p.batch * p.seqlen : 1;
-  if (!strip_map(&mc, p.C, N, rows) || !strip_map(&mb, p.B, N, rows) ||
-      !strip_map(&mx, p.x, p.nheads * P, rows))
+  if (!tile_map(&mc, p.C, N, rows) || !tile_map(&mb, p.B, N, rows) ||
+      !tile_map(&mx, p.x, p.nheads * P, rows))
     return cudaErrorInvalidValue;
   return p.z ? launch_g<true>(mc, mb, mx, p, s) : launch_g<false>(mc, mb, mx, p, s);
 }

@@ -134,6 +134,21 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
                : "memory");
 }
 
+// A plain arrival on the mbarrier (no copies announced).
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+
+// 3-D tiled TMA load of the map's box at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+      : "memory");
+}
+
 // 2-D tiled TMA load of the map's box at element coordinates (x, y) into
 // shared memory, completing `bytes` on the mbarrier (x * element size must be
 // a multiple of 16 bytes).
