@@ -15,19 +15,20 @@
 //   S      <- 2^cs_end S + B^T (delta_s 2^(cs_end - cs_s) x_s)   (tensor cores, K = Q)
 // which is the recurrence regrouped: the output of step t is the inputs of
 // the block weighted by the decay between their step and t, plus the state
-// entering the block decayed to t.  Operands are bf16 in shared memory in the
-// non-swizzled core-matrix layout (umma.cuh), products accumulate in fp32 in
-// tensor memory, and the state stays fp32 in registers between blocks
-// (rounded to bf16 only as an operand of Yo).
+// entering the block decayed to t.  Operands are bf16 in shared memory,
+// products accumulate in fp32 in tensor memory.  The state stays fp32 in
+// tensor memory between blocks: before the products of a block each thread
+// reads its state row (rounded to bf16 as the operand of Yo) and writes it
+// back scaled by 2^cs_end, and the state-update product accumulates onto it.
 //
 // One CTA of 128 threads per (batch row, head), blocks in order.  The C, B
-// and x tiles of a block arrive by TMA, one 16-byte column strip of 128 rows
-// per copy, which is exactly a column of core matrices; threads write only
-// the scaled x and the state.  Thread i is step i of the block for the
+// and x tiles of a block arrive by TMA as 128-byte swizzled boxes; the C copy
+// of the next block starts once the first products are done with C, the B
+// and x copies once the second is.  Thread i is step i of the block for the
 // masked block matrix and the epilogue (TMEM lane i holds row i of G, Yd and
-// Yo) and state row i for the state update (lane i of dS).  Shared memory is
-// about 113 KB, so two CTAs share an SM and one CTA's copies, staging and
-// epilogue overlap the other's matrix products.
+// Yo) and state row i (lane i of S).  Shared memory is about 113 KB, so two
+// CTAs share an SM and one CTA's staging and epilogue overlap the other's
+// matrix products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -66,10 +67,12 @@ constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier of the matrix prod
 constexpr uint32_t kTBar = kBar + 8;              // mbarrier of the TMA copies
 constexpr uint32_t kSlot = kTBar + 8;             // TMEM base address
 constexpr uint32_t kSmemBytes = kSlot + 8;
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM (1 KB reserved per CTA)");
 constexpr uint32_t kTileBytesC = N * Q * 2, kTileBytesB = N * Q * 2, kTileBytesX = P * Q * 2;
 
-// TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); dS [192,256).
-constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColDS = 192, kTmemCols = 256;
+// TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); the state
+// S [192,256) (row n in lane n), which the state-update product accumulates onto.
+constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColS = 192, kTmemCols = 256;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -131,13 +134,16 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t H = p.nheads, L = p.seqlen, Dm = p.nheads * P;
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const uint32_t s0 = umma::smem_u32(sm);
+  // Each mbarrier completes at most one phase between two waits of every
+  // thread (a barrier of all threads separates a wait from the next commit
+  // or copy), so a parity wait never falls two phases behind.
   const uint32_t bar = s0 + kBar, tbar = s0 + kTBar;
-  float* sD = reinterpret_cast<float*>(sm + kDs);
-  float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
   // e_s and the column factors of the block matrix, in the x-scaled tile once
   // the first products are done with it
   float* sE = reinterpret_cast<float*>(sm + kTileXw);
   float* sF = sE + Q;
+  float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
+  float* sD = reinterpret_cast<float*>(sm + kDs);
   const auto* dg = static_cast<const __nv_bfloat16*>(p.delta);
   const auto* zg = static_cast<const __nv_bfloat16*>(p.z);
   auto* yg = static_cast<__nv_bfloat16*>(p.y);
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
   if (tid == 0) {
-    umma::mbar_init(bar, 1);
+    umma::mbar_init(bar, 2);  // two arrivals per phase: see the product issue
     umma::mbar_init(tbar, 2);
     if (Lv > 0) {
       copy_c(0);
@@ -185,12 +191,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   const float al = __ldg(p.A + h) * kLog2e;                           // A_h in log2 units
   const uint32_t rowo = tid * 16;  // this thread's row in every strip
 
-  // S[n][p] for this thread's state row n = tid
-  float S[P];
+  // the state row n = tid into TMEM: h0, else zeros
 #pragma unroll
-  for (int j = 0; j < P; ++j) S[j] = p.h0 ? p.h0[((b * Dm + h * P + j) * N) + tid] : 0.f;
+  for (int half = 0; half < 2; ++half) {
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      r[j] = __float_as_uint(p.h0 ? p.h0[((b * Dm + h * P + half * 32 + j) * N) + tid] : 0.f);
+    umma::tmem_st32(tl + kColS + half * 32, r);
+  }
+  umma::tmem_wait_st();
 
   uint32_t phase = 0, tphase = 0;
+  int inflight = 0;  // commits on bar not yet waited for
   int pending = Lv > 0 ? 2 : 0;  // arrivals made on the copy barrier's current phase
   bool bad = false;
   float dt_next = tid < Lv ? __bfloat162float(dg[(b * L + tid) * H + h]) : 0.f;
@@ -209,12 +222,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool more = t0 + Q < Lv;  // the next block has valid steps
     const float dt = dt_next;
     dt_next = t + Q < Lv ? __bfloat162float(dg[(row + Q) * H + h]) : 0.f;
-    uint4 zr[GATE ? P / 8 : 1];
-    if (GATE) {
-#pragma unroll
-      for (int c = 0; c < P / 8; ++c)
-        zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
-    }
     // inclusive scan of delta A over the block
     float cs = dt * al;
 #pragma unroll
@@ -265,38 +272,73 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] *= u;
       sts128(sm, kTileXw + c * kStrip + rowo, pack8(f));
-      sts128(sm, kTileS + c * kStrip + rowo, pack8(S + c * 8));
+    }
+    {  // the state entering the block: bf16 operand of Yo; kept scaled by 2^cs_end
+      const float etot = ex2(tot);
+      uint32_t r0[32], r1[32];
+      umma::tmem_ld32_async(tl + kColS, r0);
+      umma::tmem_ld32_async(tl + kColS + 32, r1);
+      umma::tmem_wait_ld(r0);
+      umma::tmem_wait_ld(r1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
+        sts128(sm, kTileS + c * kStrip + rowo, pack8(f));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r1[c * 8 + j]);
+        sts128(sm, kTileS + (c + 4) * kStrip + rowo, pack8(f));
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
+        r1[j] = __float_as_uint(__uint_as_float(r1[j]) * etot);
+      }
+      umma::tmem_st32(tl + kColS, r0);
+      umma::tmem_st32(tl + kColS + 32, r1);
+      umma::tmem_wait_st();
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
 
+    // Two threads of different warps issue the first products in parallel,
+    // each committing its own to the product barrier (two arrivals).
     if (tid == 0) {
       umma::fence_after_sync();
       constexpr uint32_t idG = umma::idesc_bf16(128, Q, false, false);
-      constexpr uint32_t idO = umma::idesc_bf16(128, P, false, true);
-      constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)  // G = C B^T
         umma::mma_bf16(tm + kColG, desc_kmaj_sw(s0 + kTileC, k), desc_kmaj_sw(s0 + kTileB, k), idG,
                        k > 0);
+      umma::mma_commit(bar);
+    }
+    if (tid == 32) {
+      umma::fence_after_sync();
+      constexpr uint32_t idO = umma::idesc_bf16(128, P, false, true);
+      constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)  // Yo = C S
         umma::mma_bf16(tm + kColYo, desc_kmaj_sw(s0 + kTileC, k),
                        umma::smem_desc(s0 + kTileS + k * 256, 128, kStrip), idO, k > 0);
 #pragma unroll
-      for (int k = 0; k < Q / 16; ++k)  // dS = B^T Xw
-        umma::mma_bf16(tm + kColDS, desc_mnmaj_sw(s0 + kTileB, k),
-                       umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, k > 0);
+      for (int k = 0; k < Q / 16; ++k)  // S += B^T Xw
+        umma::mma_bf16(tm + kColS, desc_mnmaj_sw(s0 + kTileB, k),
+                       umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, true);
       umma::mma_commit(bar);
     }
     __syncwarp();
-    if (!umma::mbar_wait(bar, phase, kSsdWaitLimit)) bad = true;
-    phase ^= 1;
+    inflight = 1;
+    if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {  // all three products
+      phase ^= 1;
+      --inflight;
+    } else {
+      bad = true;
+    }
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
-    // the C tile is free: the next block's copy may start
-    if (more) {
+    if (more) {  // the C tile is free: the next block's C copy may start
       pending = 1;
       if (tid == 0) copy_c(t0 + Q);
     }
@@ -309,13 +351,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     // factor 2^(cs_t - cs_ref) <= 1 and the column factors; the warp's own
     // part: the exact factor and the causal mask; later parts: zero.
     float cref = 0.f;
-#pragma unroll
-    for (int sb = 0; sb < Q / 32; ++sb) {
+    auto ym_part = [&](int sb, uint32_t (&gr)[32]) {
       cref += sWt[sb];  // cs at the last step of part sb
       uint4 o[4];
       if (sb <= warp) {  // warp-uniform
         float g[32];
-        umma::tmem_ld32(tl + kColG + sb * 32, g);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(gr[j]);
         if (sb < warp) {
           const float rf = ex2(cs - cref);
           const float4* f4 = reinterpret_cast<const float4*>(sF + sb * 32);
@@ -327,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             g[j4 * 4 + 2] *= f.z * rf;
             g[j4 * 4 + 3] *= f.w * rf;
           }
-        } else {
+        } else {  // this warp's own part: exact factors and the causal mask
           const float4* e4 = reinterpret_cast<const float4*>(sE + sb * 32);
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
@@ -348,6 +390,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) sts128(sm, kTileB + (sb * 4 + q) * kStrip + rowo, o[q]);
+    };
+#pragma unroll
+    for (int pb = 0; pb < Q / 64; ++pb) {  // two 32-column parts per round of TMEM loads
+      const int sa = 2 * pb, sc = 2 * pb + 1;
+      uint32_t ga[32], gc[32];
+      if (sa <= warp) umma::tmem_ld32_async(tl + kColG + sa * 32, ga);
+      if (sc <= warp) umma::tmem_ld32_async(tl + kColG + sc * 32, gc);
+      if (sa <= warp) umma::tmem_wait_ld(ga);
+      if (sc <= warp) umma::tmem_wait_ld(gc);
+      ym_part(sa, ga);
+      ym_part(sc, gc);
+    }
+    uint4 zr[GATE ? P / 8 : 1];  // the gate row, in flight during the second product
+    if (GATE) {
+#pragma unroll
+      for (int c = 0; c < P / 8; ++c)
+        zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -362,9 +421,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                        desc_mnmaj_sw(s0 + kTileX, k), idY, k > 0);
       umma::mma_commit(bar);
     }
+    if (tid == 32) umma::mbar_arrive(bar);  // the second arrival of this phase
     __syncwarp();
-    if (!umma::mbar_wait(bar, phase, kSsdWaitLimit)) bad = true;
-    phase ^= 1;
+    inflight = 1;
+    if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {
+      phase ^= 1;
+      --inflight;
+    } else {
+      bad = true;
+    }
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
     // the B and x tiles are free: the next block's copies may start
@@ -377,9 +442,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float eo = ex2(cs);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      float yd[32], yo[32];
-      umma::tmem_ld32(tl + kColYd + half * 32, yd);
-      umma::tmem_ld32(tl + kColYo + half * 32, yo);
+      uint32_t yd[32], yo[32];
+      umma::tmem_ld32_async(tl + kColYd + half * 32, yd);
+      umma::tmem_ld32_async(tl + kColYo + half * 32, yo);
+      umma::tmem_wait_ld(yd);
+      umma::tmem_wait_ld(yo);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int c = half * 4 + q;
@@ -388,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (GATE) unpack8(zr[c], zv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float v = fmaf(eo, yo[q * 8 + j], yd[q * 8 + j]);
+          float v = fmaf(eo, __uint_as_float(yo[q * 8 + j]), __uint_as_float(yd[q * 8 + j]));
           v = fmaf(sD[c * 8 + j], xv[j], v);
           if (GATE) v *= silu(zv[j]);
           o[j] = in ? v : 0.f;
@@ -396,21 +463,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (t < L) *reinterpret_cast<uint4*>(yg + row * Dm + h * P + c * 8) = pack8(o);
       }
     }
-    const float etot = ex2(tot);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float ds[32];
-      umma::tmem_ld32(tl + kColDS + half * 32, ds);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[half * 32 + j] = fmaf(etot, S[half * 32 + j], ds[j]);
-    }
     umma::fence_before_sync();
     __syncthreads();
   }
 
   if (bad) {
     if (tid == 0) atomicOr(p.err, kErrSsdWait);
-    umma::mbar_wait(bar, phase ^ 1u, kSsdWaitLimit);  // products still in flight, bounded
+    if (inflight > 0) umma::mbar_wait(bar, phase, kSsdWaitLimit);  // products in flight, bounded
   }
   if (pending > 0) {  // copies still in flight (only after a wait gave up), bounded
     if (pending == 1 && tid == 0) umma::mbar_arrive(tbar);  // the second arrival of the phase
@@ -418,7 +477,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (!bad && p.h_final) {
 #pragma unroll
-    for (int j = 0; j < P; ++j) p.h_final[((b * Dm + h * P + j) * N) + tid] = S[j];
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      umma::tmem_ld32_async(tl + kColS + half * 32, r);
+      umma::tmem_wait_ld(r);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        p.h_final[((b * Dm + h * P + half * 32 + j) * N) + tid] = __uint_as_float(r[j]);
+    }
   }
   umma::fence_before_sync();
   __syncthreads();
