@@ -62,3 +62,16 @@ def test_channel_slice_is_indexing():
     assert np.array_equal(s["B"][0], inp["B"][5])
     assert np.array_equal(s["A"][0], inp["A"][3])
     assert s["valid_len"][0] == inp["valid_len"][5]
+
+
+def test_ssd_inputs_shapes_and_ranges():
+    w = W.SSD_WORKLOADS[1].scaled(batch=2, seqlen=96, nheads=3)
+    a, b = W.make_ssd_inputs(w), W.make_ssd_inputs(w)
+    for k in ("x", "delta", "A", "B", "C", "D", "z"):
+        assert np.array_equal(a[k], b[k]), k  # seeded
+    assert a["x"].shape == (2, 96, 3 * 64) and a["x"].dtype == np.uint16
+    assert a["delta"].shape == (2, 96, 3) and a["B"].shape == (2, 96, 128)
+    assert a["A"].shape == (3,) and np.all((a["A"] <= -1.0) & (a["A"] >= -16.0))
+    dt = W.bf16_bits_to_f32(a["delta"])
+    assert np.all(dt > 0) and np.all(dt < 1.0)
+    assert np.all(a["D"] == 1.0) and a["valid_len"] is None
