@@ -39,17 +39,30 @@ struct BwdShape {
   static constexpr int CPB = CWB * (kBwdThreads / 32);
 };
 
-// Shared-memory floats per thread for chunks of cl steps: the checkpoints,
-// the piece's K + 1 states, and the piece's per-channel inputs (delta, x, dy,
-// z).  The piece's B and C rows are shared by the CTA (one batch row).
-__host__ __device__ inline int bwd_floats(int64_t cl, int gb) {
+// Shared-memory float4 slots per thread for chunks of cl steps: the
+// checkpoints, the piece's K + 1 states (a thread's up to 4 states in one
+// slot), and the piece's per-step inputs (delta, x, dy, z in one slot).  The
+// piece's B and C rows follow, shared by the CTA (one batch row).
+__host__ __device__ inline int bwd_slots(int64_t cl) {
   const int nck = static_cast<int>((cl + kBwdK - 1) / kBwdK);
-  return nck * gb + (kBwdK + 1) * gb + 4 * kBwdK;
+  return nck + 2 * kBwdK + 1;
 }
 __host__ __device__ inline size_t bwd_smem(int64_t cl, int n) {
-  const int gb = n >= 4 ? 4 : n;
-  return (size_t(bwd_floats(cl, gb)) * kBwdThreads + 2 * kBwdK * n) * sizeof(float);
+  return (size_t(bwd_slots(cl)) * 4 * kBwdThreads + 2 * kBwdK * n) * sizeof(float);
 }
+
+template <int G>
+__device__ __forceinline__ float4 to4(const float (&a)[G]) {
+  return make_float4(a[0], G > 1 ? a[1 % G] : 0.f, G > 2 ? a[2 % G] : 0.f, G > 3 ? a[3 % G] : 0.f);
+}
+template <int G>
+__device__ __forceinline__ void from4(const float4& v, float (&a)[G]) {
+  a[0] = v.x;
+  if (G > 1) a[1 % G] = v.y;
+  if (G > 2) a[2 % G] = v.z;
+  if (G > 3) a[3 % G] = v.w;
+}
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
 template <int N, typename T, bool GATE>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
@@ -66,12 +79,13 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
   const int64_t L = p.fwd.seqlen, CL = p.fwd.chunk_len, D_ = p.fwd.dim;
   const int64_t lv = valid_steps(p.fwd, b);
   const int nck = static_cast<int>((CL + K - 1) / K);
-  // this thread's float i of its shared-memory area: sm[i * blockDim + tid]
-  auto f = [&](int i) -> float& { return sm[i * kBwdThreads + tid]; };
-  const int CK = 0, HS = nck * GB, IDT = HS + (K + 1) * GB, IX = IDT + K, IDY = IX + K,
-            IZ = IDY + K;
+  // this thread's slot i of its shared-memory area (16-byte slots, thread-
+  // interleaved so that a warp's accesses of one slot are contiguous)
+  float4* sv = reinterpret_cast<float4*>(sm);
+  auto v4 = [&](int i) -> float4& { return sv[i * kBwdThreads + tid]; };
+  const int CK = 0, HS = nck, IN = HS + K + 1;
   // the piece's B and C rows [K][N], shared by the CTA, after the threads' areas
-  float* sB = sm + bwd_floats(CL, GB) * kBwdThreads;
+  float* sB = sm + bwd_slots(CL) * 4 * kBwdThreads;
   float* sC = sB + K * N;
 
   float av[GB], al[GB];  // A of this thread's states, and scaled by log2(e)
@@ -114,8 +128,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
     // state before the piece) every K steps; the loads of a half piece are
     // issued together
     for (int64_t s0 = t0; s0 < tv; s0 += K) {
-#pragma unroll
-      for (int g = 0; g < GB; ++g) f(CK + static_cast<int>((s0 - t0) / K) * GB + g) = h[g];
+      v4(CK + static_cast<int>((s0 - t0) / K)) = to4<GB>(h);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float dt[H], ux[H], bb[H][GB];
@@ -139,8 +152,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
     // pass 2: the pieces, newest first
     for (int64_t j = (tv - t0 - 1) / K; j >= 0; --j) {
       const int64_t s0 = t0 + j * K, s1 = min(s0 + K, tv);
-#pragma unroll
-      for (int g = 0; g < GB; ++g) h[g] = f(CK + static_cast<int>(j) * GB + g);
+      from4<GB>(v4(CK + static_cast<int>(j)), h);
       // the piece's B and C rows, once per CTA (every warp of the CTA walks the
       // same pieces: one batch row); the previous piece is done with them
       __syncthreads();
@@ -170,41 +182,43 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
 #pragma unroll
         for (int k = 0; k < H; ++k) {
           const int kk = hh * H + k;
-          f(IDT + kk) = dt[k];
-          f(IX + kk) = xv[k];
-          f(IDY + kk) = dyv[k];
-          f(IZ + kk) = zv[k];
-#pragma unroll
-          for (int g = 0; g < GB; ++g) f(HS + kk * GB + g) = h[g];  // h_{t-1}
+          v4(IN + kk) = make_float4(dt[k], xv[k], dyv[k], zv[k]);
+          v4(HS + kk) = to4<GB>(h);  // h_{t-1}
           const float ux = dt[k] * xv[k];
 #pragma unroll
           for (int g = 0; g < GB; ++g)
             h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * sB[kk * N + n0 + g]);
         }
       }
-#pragma unroll
-      for (int g = 0; g < GB; ++g) f(HS + K * GB + g) = h[g];  // beyond s1 the steps were identities
+      v4(HS + K) = to4<GB>(h);  // beyond s1 the steps were identities
       // reverse over the piece
       for (int k = static_cast<int>(s1 - s0) - 1; k >= 0; --k) {
         const int64_t t = s0 + k;
         const int64_t e = (b * L + t) * D_ + dd, r = (b * L + t) * N + n0;
-        const float dt = f(IDT + k), xv = f(IX + k), dyv = f(IDY + k);
+        const float4 in4 = v4(IN + k);
+        const float dt = in4.x, xv = in4.y, dyv = in4.z;
         float hp[GB], hc[GB], bb[GB], cc[GB];
+        from4<GB>(v4(HS + k), hp);
+        from4<GB>(v4(HS + k + 1), hc);
+        if (GB == 4) {
+          from4<GB>(*reinterpret_cast<const float4*>(sB + k * N + n0), bb);
+          from4<GB>(*reinterpret_cast<const float4*>(sC + k * N + n0), cc);
+        } else {
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            bb[g] = sB[k * N + n0 + g];
+            cc[g] = sC[k * N + n0 + g];
+          }
+        }
         float yp = 0.f;
 #pragma unroll
-        for (int g = 0; g < GB; ++g) {
-          hp[g] = f(HS + k * GB + g);
-          hc[g] = f(HS + (k + 1) * GB + g);
-          bb[g] = sB[k * N + n0 + g];
-          cc[g] = sC[k * N + n0 + g];
-          yp = fmaf(cc[g], hc[g], yp);
-        }
+        for (int g = 0; g < GB; ++g) yp = fmaf(cc[g], hc[g], yp);
 #pragma unroll
         for (int m = NL / 2; m >= 1; m /= 2) yp += __shfl_xor_sync(0xffffffffu, yp, m);
         yp = fmaf(dsk, xv, yp);  // C h + D x, before the gate
         float dyp = dyv, dzv = 0.f;
         if (GATE) {
-          const float zz = f(IZ + k);
+          const float zz = in4.w;
           const float sg = __fdividef(1.f, 1.f + ex2(-zz * kLog2e));
           dyp = dyv * zz * sg;                           // dy silu(z)
           dzv = dyv * yp * sg * (1.f + zz * (1.f - sg));  // dy yp silu'(z)
@@ -226,20 +240,42 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
           pdt += __shfl_xor_sync(0xffffffffu, pdt, m);
           pdx += __shfl_xor_sync(0xffffffffu, pdx, m);
         }
-        // sums over the warp's channels (lanes sl + NL k)
+        // sums over the warp's channels (the lanes sl + NL j), as a
+        // reduce-scatter: while a lane holds more than one value, each round
+        // sends half of them to the partner and keeps the other half summed;
+        // the remaining rounds are plain xor sums.  The lane ends with values
+        // [vb, vb + VF) of (db[0..GB), dc[0..GB)).
+        constexpr int V = 2 * GB, RND = ilog2(32 / NL);
+        constexpr int VF = (V >> RND) > 1 ? (V >> RND) : 1;
+        float v[V];
 #pragma unroll
-        for (int m = 16; m >= NL; m /= 2) {
+        for (int g = 0; g < GB; ++g) {
+          v[g] = db[g];
+          v[GB + g] = dc[g];
+        }
+        int vb = 0, dup = 0;
 #pragma unroll
-          for (int g = 0; g < GB; ++g) {
-            db[g] += __shfl_xor_sync(0xffffffffu, db[g], m);
-            dc[g] += __shfl_xor_sync(0xffffffffu, dc[g], m);
+        for (int j = 0; j < RND; ++j) {
+          const int m = 16 >> j, c = V >> j;
+          if (c > 1) {
+            const bool up = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < c / 2; ++i) {
+              const float send = up ? v[i] : v[i + c / 2];
+              const float keep = up ? v[i + c / 2] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+            vb += up ? c / 2 : 0;
+          } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+            dup |= m;
           }
         }
-        if (lane < NL) {
+        if ((lane & dup) == 0) {
 #pragma unroll
-          for (int g = 0; g < GB; ++g) {
-            atomicAdd(p.dB + r + g, db[g]);
-            atomicAdd(p.dC + r + g, dc[g]);
+          for (int i = 0; i < VF; ++i) {
+            const int vi = vb + i;
+            atomicAdd(vi < GB ? p.dB + r + vi : p.dC + r + (vi - GB), v[i]);
           }
         }
         if (ok && sl == 0) {
