@@ -125,34 +125,58 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
       h[g] = v;
     }
     // pass 1: the forward's arithmetic over the chunk, a checkpoint (the
-    // state before the piece) every K steps; the loads of a half piece are
-    // issued together
-    for (int64_t s0 = t0; s0 < tv; s0 += K) {
-      v4(CK + static_cast<int>((s0 - t0) / K)) = to4<GB>(h);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float dt[H], ux[H], bb[H][GB];
+    // state before the piece) every K steps.  The loads of a half piece are
+    // issued together, one half ahead of its arithmetic.
+    {
+      float dtA[H], xA[H], bA[H][GB], dtB[H], xB[H], bB[H][GB];
+      auto load_half = [&](int64_t s, float (&dt)[H], float (&xr)[H], float (&bb)[H][GB]) {
 #pragma unroll
         for (int k = 0; k < H; ++k) {
-          const int64_t t = s0 + hh * H + k;
+          const int64_t t = s + k;
           const bool in = t < tv;
-          const int64_t tt = in ? t : s0;
+          const int64_t tt = in ? t : t0;
           const int64_t e = (b * L + tt) * D_ + dd;
           dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;  // past the chunk: identity
-          ux[k] = dt[k] * IO<T>::load(p.fwd.x, e);
+          xr[k] = IO<T>::load(p.fwd.x, e);
 #pragma unroll
           for (int g = 0; g < GB; ++g) bb[k][g] = IO<T>::load(p.fwd.B, (b * L + tt) * N + n0 + g);
         }
+      };
+      auto run_half = [&](const float (&dt)[H], const float (&xr)[H], const float (&bb)[H][GB]) {
 #pragma unroll
-        for (int k = 0; k < H; ++k)
+        for (int k = 0; k < H; ++k) {
+          const float ux = dt[k] * xr[k];
 #pragma unroll
-          for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux[k] * bb[k][g]);
+          for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * bb[k][g]);
+        }
+      };
+      load_half(t0, dtA, xA, bA);
+      for (int64_t s0 = t0; s0 < tv; s0 += K) {
+        v4(CK + static_cast<int>((s0 - t0) / K)) = to4<GB>(h);
+        load_half(s0 + H, dtB, xB, bB);
+        run_half(dtA, xA, bA);
+        if (s0 + K < tv) load_half(s0 + K, dtA, xA, bA);
+        run_half(dtB, xB, bB);
       }
     }
     // pass 2: the pieces, newest first
     for (int64_t j = (tv - t0 - 1) / K; j >= 0; --j) {
       const int64_t s0 = t0 + j * K, s1 = min(s0 + K, tv);
       from4<GB>(v4(CK + static_cast<int>(j)), h);
+      // this thread's inputs of the piece, every step issued together with the
+      // shared B and C rows below
+      float dt[K], xv[K], dyv[K], zv[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        const int64_t t = s0 + k;
+        const bool in = t < s1;
+        const int64_t tt = in ? t : s0;
+        const int64_t e = (b * L + tt) * D_ + dd;
+        dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;
+        xv[k] = IO<T>::load(p.fwd.x, e);
+        dyv[k] = (in && ok) ? IO<T>::load(p.dy, e) : 0.f;
+        zv[k] = GATE ? IO<T>::load(p.fwd.z, e) : 0.f;
+      }
       // the piece's B and C rows, once per CTA (every warp of the CTA walks the
       // same pieces: one batch row); the previous piece is done with them
       __syncthreads();
@@ -166,29 +190,12 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
       __syncthreads();
       // replay: the piece's inputs to shared memory, its states h_{t-1}
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float dt[H], xv[H], dyv[H], zv[H];
+      for (int k = 0; k < K; ++k) {
+        v4(IN + k) = make_float4(dt[k], xv[k], dyv[k], zv[k]);
+        v4(HS + k) = to4<GB>(h);  // h_{t-1}
+        const float ux = dt[k] * xv[k];
 #pragma unroll
-        for (int k = 0; k < H; ++k) {
-          const int64_t t = s0 + hh * H + k;
-          const bool in = t < s1;
-          const int64_t tt = in ? t : s0;
-          const int64_t e = (b * L + tt) * D_ + dd;
-          dt[k] = in ? IO<T>::load(p.fwd.delta, e) : 0.f;
-          xv[k] = IO<T>::load(p.fwd.x, e);
-          dyv[k] = (in && ok) ? IO<T>::load(p.dy, e) : 0.f;
-          zv[k] = GATE ? IO<T>::load(p.fwd.z, e) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < H; ++k) {
-          const int kk = hh * H + k;
-          v4(IN + kk) = make_float4(dt[k], xv[k], dyv[k], zv[k]);
-          v4(HS + kk) = to4<GB>(h);  // h_{t-1}
-          const float ux = dt[k] * xv[k];
-#pragma unroll
-          for (int g = 0; g < GB; ++g)
-            h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * sB[kk * N + n0 + g]);
-        }
+        for (int g = 0; g < GB; ++g) h[g] = fmaf(ex2(dt[k] * al[g]), h[g], ux * sB[k * N + n0 + g]);
       }
       v4(HS + K) = to4<GB>(h);  // beyond s1 the steps were identities
       // reverse over the piece
