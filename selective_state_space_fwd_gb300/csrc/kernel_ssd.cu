@@ -21,14 +21,15 @@
 // reads its state row (rounded to bf16 as the operand of Yo) and writes it
 // back scaled by 2^cs_end, and the state-update product accumulates onto it.
 //
-// One CTA of 128 threads per (batch row, head), blocks in order.  The C, B
+// One CTA of 256 threads per (batch row, head), blocks in order.  The C, B
 // and x tiles of a block arrive by TMA as 128-byte swizzled boxes; the C copy
 // of the next block starts once the first products are done with C, the B
-// and x copies once the second is.  Thread i is step i of the block for the
-// masked block matrix and the epilogue (TMEM lane i holds row i of G, Yd and
-// Yo) and state row i (lane i of S).  Shared memory is about 113 KB, so two
-// CTAs share an SM and one CTA's staging and epilogue overlap the other's
-// matrix products.
+// and x copies once the second is.  Threads i and i + 128 share row i: step
+// i of the block for the masked block matrix and the epilogue (TMEM lane i
+// holds row i of G, Yd and Yo) and state row i (lane i of S), each taking
+// half of the columns (warps w and w + 4 read the same TMEM lanes).  Shared
+// memory is about 115 KB, so two CTAs share an SM and one CTA's staging and
+// epilogue overlap the other's matrix products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -126,20 +127,18 @@ __device__ __forceinline__ float lg2(float v) {
 }
 
 template <bool GATE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(2 * kThreads, 2)
     ssd_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_x, const SsdParams p) {
   extern __shared__ __align__(1024) unsigned char sm[];
+  // 256 threads: thread (row, hf) handles row `row` of the block (step, or
+  // state row) and the 32-column half `hf` of its 64 channels
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & (kThreads - 1), hf = tid >> 7, lw = warp & 3;
   const int64_t H = p.nheads, L = p.seqlen, Dm = p.nheads * P;
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const uint32_t s0 = umma::smem_u32(sm);
-  // Each mbarrier completes at most one phase between two waits of every
-  // thread (a barrier of all threads separates a wait from the next commit
-  // or copy), so a parity wait never falls two phases behind.
   const uint32_t bar = s0 + kBar, tbar = s0 + kTBar;
-  // e_s and the column factors of the block matrix, in the x-scaled tile once
-  // the first products are done with it
   float* sE = reinterpret_cast<float*>(sm + kTileXw);
   float* sF = sE + Q;
   float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
@@ -153,8 +152,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     Lv = p.valid_len[b];
     Lv = Lv < 0 ? 0 : (Lv > L ? L : Lv);
   }
-  // Copies of the block starting at t0, by one thread: the C tile, and the B
-  // and x tiles.  The copy barrier takes two arrivals per block, one each.
   auto copy_c = [&](int64_t t0) {
     const int r = static_cast<int>(b * L + t0);
     umma::mbar_expect_tx(tbar, kTileBytesC);
@@ -168,14 +165,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     umma::tma_load_2d(s0 + kTileB + kHalf, &tm_b, 64, r, tbar);
     umma::tma_load_2d(s0 + kTileX, &tm_x, static_cast<int>(h * P), r, tbar);
   };
-  if (s0 & 1023u) {  // the swizzled tiles need 1024-byte alignment; report, compute nothing
+  if (s0 & 1023u) {
     if (tid == 0) atomicOr(p.err, kErrSsdAlign);
     return;
   }
 
   if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
   if (tid == 0) {
-    umma::mbar_init(bar, 2);  // two arrivals per phase: see the product issue
+    umma::mbar_init(bar, 2);
     umma::mbar_init(tbar, 2);
     if (Lv > 0) {
       copy_c(0);
@@ -187,129 +184,110 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   umma::fence_after_sync();
   const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kSlot);
-  const uint32_t tl = tm + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
-  const float al = __ldg(p.A + h) * kLog2e;                           // A_h in log2 units
-  const uint32_t rowo = tid * 16;  // this thread's row in every strip
+  const uint32_t tl = tm + (static_cast<uint32_t>(lw * 32) << 16);  // this warp's TMEM lanes
+  const float al = __ldg(p.A + h) * kLog2e;
+  const uint32_t rowo = row * 16;
+  const int c0 = hf * 4;  // this thread's first 8-channel chunk
 
-  // the state row n = tid into TMEM: h0, else zeros
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  {  // this thread's half of state row n = row into TMEM: h0, else zeros
     uint32_t r[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      r[j] = __float_as_uint(p.h0 ? p.h0[((b * Dm + h * P + half * 32 + j) * N) + tid] : 0.f);
-    umma::tmem_st32(tl + kColS + half * 32, r);
+      r[j] = __float_as_uint(p.h0 ? p.h0[((b * Dm + h * P + hf * 32 + j) * N) + row] : 0.f);
+    umma::tmem_st32(tl + kColS + hf * 32, r);
+    umma::tmem_wait_st();
   }
-  umma::tmem_wait_st();
 
   uint32_t phase = 0, tphase = 0;
-  int inflight = 0;  // commits on bar not yet waited for
-  int pending = Lv > 0 ? 2 : 0;  // arrivals made on the copy barrier's current phase
+  int pending = Lv > 0 ? 2 : 0;
+  int inflight = 0;
   bool bad = false;
-  float dt_next = tid < Lv ? __bfloat162float(dg[(b * L + tid) * H + h]) : 0.f;
+  float dt_next = row < Lv ? __bfloat162float(dg[(b * L + row) * H + h]) : 0.f;
   for (int64_t t0 = 0; t0 < L; t0 += Q) {
-    const int64_t t = t0 + tid;
-    const bool in = t < Lv;  // a valid step (Lv <= L)
-    const int64_t row = b * L + t;
-    if (t0 >= Lv) {  // the whole block is past valid_len: output 0, state frozen
+    const int64_t t = t0 + row;
+    const bool in = t < Lv;
+    const int64_t grow = b * L + t;
+    if (t0 >= Lv) {
       if (t < L) {
 #pragma unroll
-        for (int c = 0; c < P / 8; ++c)
-          *reinterpret_cast<uint4*>(yg + row * Dm + h * P + c * 8) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(yg + grow * Dm + h * P + (c0 + c) * 8) = make_uint4(0, 0, 0, 0);
       }
       continue;
     }
-    const bool more = t0 + Q < Lv;  // the next block has valid steps
+    const bool more = t0 + Q < Lv;
     const float dt = dt_next;
-    dt_next = t + Q < Lv ? __bfloat162float(dg[(row + Q) * H + h]) : 0.f;
-    // inclusive scan of delta A over the block
+    dt_next = t + Q < Lv ? __bfloat162float(dg[(grow + Q) * H + h]) : 0.f;
     float cs = dt * al;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float v = __shfl_up_sync(0xFFFFFFFFu, cs, o);
       if (lane >= o) cs += v;
     }
-    if (lane == 31) sWt[warp] = cs;
+    if (hf == 0 && lane == 31) sWt[lw] = cs;
     __syncthreads();
     float pre = 0.f, tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) {
       const float v = sWt[w];
-      pre += w < warp ? v : 0.f;
+      pre += w < lw ? v : 0.f;
       tot += v;
     }
     cs += pre;
-    const float e = cs - lg2(dt);  // +inf past valid_len: its column of Ym is 0
-    // column factor for the rows of later 32-step parts: delta_s 2^(cs_ref - cs_s),
-    // cs_ref = cs at the last step of this warp's part (<= delta_s)
+    const float e = cs - lg2(dt);
     const float colf = dt * ex2(__shfl_sync(0xFFFFFFFFu, cs, 31) - cs);
-    const float u = dt * ex2(tot - cs);  // weight of step t in the state at the block end
+    const float u = dt * ex2(tot - cs);
 
     if (umma::mbar_wait(tbar, tphase, kSsdWaitLimit)) {
       tphase ^= 1;
       pending = 0;
     } else {
-      bad = true;  // the copies stay pending: waited for again before exit
+      bad = true;
     }
     if (__syncthreads_or(bad)) { bad = true; break; }
-    // rows past valid_len (or past the sequence) must not reach a product: zero
-    // them in the B and x tiles; this step's x row stays in registers
-    uint4 xr[P / 8];
+    uint4 xr[4];
 #pragma unroll
-    for (int c = 0; c < P / 8; ++c) xr[c] = in ? lds128(sm, kTileX + swz(tid, c)) : make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < 4; ++c) xr[c] = in ? lds128(sm, kTileX + swz(row, c0 + c)) : make_uint4(0, 0, 0, 0);
     if (!in) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        sts128(sm, kTileB + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
-        sts128(sm, kTileB + kHalf + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
-        sts128(sm, kTileX + tid * 128 + c * 16, make_uint4(0, 0, 0, 0));
-      }
+      for (int c = 0; c < 8; ++c) sts128(sm, kTileB + hf * kHalf + row * 128 + c * 16, make_uint4(0, 0, 0, 0));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sts128(sm, kTileX + row * 128 + (c0 + c) * 16, make_uint4(0, 0, 0, 0));
     }
 #pragma unroll
-    for (int c = 0; c < P / 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       float f[8];
       unpack8(xr[c], f);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] *= u;
-      sts128(sm, kTileXw + c * kStrip + rowo, pack8(f));
+      sts128(sm, kTileXw + (c0 + c) * kStrip + rowo, pack8(f));
     }
-    {  // the state entering the block: bf16 operand of Yo; kept scaled by 2^cs_end
+    {  // this thread's half of the state row: bf16 operand of Yo; kept scaled by 2^cs_end
       const float etot = ex2(tot);
-      uint32_t r0[32], r1[32];
-      umma::tmem_ld32_async(tl + kColS, r0);
-      umma::tmem_ld32_async(tl + kColS + 32, r1);
+      uint32_t r0[32];
+      umma::tmem_ld32_async(tl + kColS + hf * 32, r0);
       umma::tmem_wait_ld(r0);
-      umma::tmem_wait_ld(r1);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float f[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
-        sts128(sm, kTileS + c * kStrip + rowo, pack8(f));
-#pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r1[c * 8 + j]);
-        sts128(sm, kTileS + (c + 4) * kStrip + rowo, pack8(f));
+        sts128(sm, kTileS + (c0 + c) * kStrip + rowo, pack8(f));
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
-        r1[j] = __float_as_uint(__uint_as_float(r1[j]) * etot);
-      }
-      umma::tmem_st32(tl + kColS, r0);
-      umma::tmem_st32(tl + kColS + 32, r1);
+      for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
+      umma::tmem_st32(tl + kColS + hf * 32, r0);
       umma::tmem_wait_st();
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
     __syncthreads();
 
-    // Two threads of different warps issue the first products in parallel,
-    // each committing its own to the product barrier (two arrivals).
     if (tid == 0) {
       umma::fence_after_sync();
       constexpr uint32_t idG = umma::idesc_bf16(128, Q, false, false);
 #pragma unroll
-      for (int k = 0; k < N / 16; ++k)  // G = C B^T
+      for (int k = 0; k < N / 16; ++k)
         umma::mma_bf16(tm + kColG, desc_kmaj_sw(s0 + kTileC, k), desc_kmaj_sw(s0 + kTileB, k), idG,
                        k > 0);
       umma::mma_commit(bar);
@@ -319,18 +297,18 @@ __global__ void __launch_bounds__(kThreads, 2)
       constexpr uint32_t idO = umma::idesc_bf16(128, P, false, true);
       constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
 #pragma unroll
-      for (int k = 0; k < N / 16; ++k)  // Yo = C S
+      for (int k = 0; k < N / 16; ++k)
         umma::mma_bf16(tm + kColYo, desc_kmaj_sw(s0 + kTileC, k),
                        umma::smem_desc(s0 + kTileS + k * 256, 128, kStrip), idO, k > 0);
 #pragma unroll
-      for (int k = 0; k < Q / 16; ++k)  // S += B^T Xw
+      for (int k = 0; k < Q / 16; ++k)
         umma::mma_bf16(tm + kColS, desc_mnmaj_sw(s0 + kTileB, k),
                        umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, true);
       umma::mma_commit(bar);
     }
     __syncwarp();
     inflight = 1;
-    if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {  // all three products
+    if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {
       phase ^= 1;
       --inflight;
     } else {
@@ -338,27 +316,32 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
-    if (more) {  // the C tile is free: the next block's C copy may start
+    if (more) {
       pending = 1;
       if (tid == 0) copy_c(t0 + Q);
     }
-    sE[tid] = e;
-    sF[tid] = colf;
+    if (hf == 0) {
+      sE[row] = e;
+      sF[row] = colf;
+    }
     __syncthreads();
 
-    // Ym row t = tid into the B tile (its products are done).  Parts of 32
-    // columns before this warp's own: no mask, the decay factored into a row
-    // factor 2^(cs_t - cs_ref) <= 1 and the column factors; the warp's own
-    // part: the exact factor and the causal mask; later parts: zero.
-    float cref = 0.f;
-    auto ym_part = [&](int sb, uint32_t (&gr)[32]) {
-      cref += sWt[sb];  // cs at the last step of part sb
+    // Ym: parts sb = hf and hf + 2 of this row (32 columns each)
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int sb = hf + 2 * q2;
       uint4 o[4];
-      if (sb <= warp) {  // warp-uniform
+      if (sb <= lw) {  // warp-uniform
+        uint32_t gr[32];
+        umma::tmem_ld32_async(tl + kColG + sb * 32, gr);
+        umma::tmem_wait_ld(gr);
         float g[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) g[j] = __uint_as_float(gr[j]);
-        if (sb < warp) {
+        if (sb < lw) {
+          float cref = 0.f;
+#pragma unroll
+          for (int w = 0; w < kThreads / 32; ++w) cref += w <= sb ? sWt[w] : 0.f;
           const float rf = ex2(cs - cref);
           const float4* f4 = reinterpret_cast<const float4*>(sF + sb * 32);
 #pragma unroll
@@ -369,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             g[j4 * 4 + 2] *= f.z * rf;
             g[j4 * 4 + 3] *= f.w * rf;
           }
-        } else {  // this warp's own part: exact factors and the causal mask
+        } else {
           const float4* e4 = reinterpret_cast<const float4*>(sE + sb * 32);
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
@@ -390,23 +373,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) sts128(sm, kTileB + (sb * 4 + q) * kStrip + rowo, o[q]);
-    };
-#pragma unroll
-    for (int pb = 0; pb < Q / 64; ++pb) {  // two 32-column parts per round of TMEM loads
-      const int sa = 2 * pb, sc = 2 * pb + 1;
-      uint32_t ga[32], gc[32];
-      if (sa <= warp) umma::tmem_ld32_async(tl + kColG + sa * 32, ga);
-      if (sc <= warp) umma::tmem_ld32_async(tl + kColG + sc * 32, gc);
-      if (sa <= warp) umma::tmem_wait_ld(ga);
-      if (sc <= warp) umma::tmem_wait_ld(gc);
-      ym_part(sa, ga);
-      ym_part(sc, gc);
     }
-    uint4 zr[GATE ? P / 8 : 1];  // the gate row, in flight during the second product
+    uint4 zr[GATE ? 4 : 1];
     if (GATE) {
 #pragma unroll
-      for (int c = 0; c < P / 8; ++c)
-        zr[c] = in ? ldg128(zg + row * Dm + h * P + c * 8) : make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < 4; ++c)
+        zr[c] = in ? ldg128(zg + grow * Dm + h * P + (c0 + c) * 8) : make_uint4(0, 0, 0, 0);
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -416,12 +388,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       umma::fence_after_sync();
       constexpr uint32_t idY = umma::idesc_bf16(128, P, false, true);
 #pragma unroll
-      for (int k = 0; k < Q / 16; ++k)  // Yd = Ym x
+      for (int k = 0; k < Q / 16; ++k)
         umma::mma_bf16(tm + kColYd, umma::smem_desc(s0 + kTileB + k * 2 * kStrip, kStrip, 128),
                        desc_mnmaj_sw(s0 + kTileX, k), idY, k > 0);
       umma::mma_commit(bar);
     }
-    if (tid == 32) umma::mbar_arrive(bar);  // the second arrival of this phase
+    if (tid == 32) umma::mbar_arrive(bar);
     __syncwarp();
     inflight = 1;
     if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {
@@ -432,27 +404,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (__syncthreads_or(bad)) { bad = true; break; }
     umma::fence_after_sync();
-    // the B and x tiles are free: the next block's copies may start
     if (more) {
       pending = 2;
       if (tid == 0) copy_bx(t0 + Q);
     }
 
-    // epilogue: y of step t = tid, then the state row n = tid
+    // epilogue: y of step t = row, channels hf*32 .. hf*32 + 31
     const float eo = ex2(cs);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    {
       uint32_t yd[32], yo[32];
-      umma::tmem_ld32_async(tl + kColYd + half * 32, yd);
-      umma::tmem_ld32_async(tl + kColYo + half * 32, yo);
+      umma::tmem_ld32_async(tl + kColYd + hf * 32, yd);
+      umma::tmem_ld32_async(tl + kColYo + hf * 32, yo);
       umma::tmem_wait_ld(yd);
       umma::tmem_wait_ld(yo);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int c = half * 4 + q;
+        const int c = c0 + q;
         float xv[8], zv[8], o[8];
-        unpack8(xr[c], xv);
-        if (GATE) unpack8(zr[c], zv);
+        unpack8(xr[q], xv);
+        if (GATE) unpack8(zr[q], zv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           float v = fmaf(eo, __uint_as_float(yo[q * 8 + j]), __uint_as_float(yd[q * 8 + j]));
@@ -460,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (GATE) v *= silu(zv[j]);
           o[j] = in ? v : 0.f;
         }
-        if (t < L) *reinterpret_cast<uint4*>(yg + row * Dm + h * P + c * 8) = pack8(o);
+        if (t < L) *reinterpret_cast<uint4*>(yg + grow * Dm + h * P + c * 8) = pack8(o);
       }
     }
     umma::fence_before_sync();
@@ -469,22 +439,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (bad) {
     if (tid == 0) atomicOr(p.err, kErrSsdWait);
-    if (inflight > 0) umma::mbar_wait(bar, phase, kSsdWaitLimit);  // products in flight, bounded
+    if (inflight > 0) umma::mbar_wait(bar, phase, kSsdWaitLimit);
   }
-  if (pending > 0) {  // copies still in flight (only after a wait gave up), bounded
-    if (pending == 1 && tid == 0) umma::mbar_arrive(tbar);  // the second arrival of the phase
+  if (pending > 0) {
+    if (pending == 1 && tid == 0) umma::mbar_arrive(tbar);
     umma::mbar_wait(tbar, tphase, kSsdWaitLimit);
   }
   if (!bad && p.h_final) {
+    uint32_t r[32];
+    umma::tmem_ld32_async(tl + kColS + hf * 32, r);
+    umma::tmem_wait_ld(r);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t r[32];
-      umma::tmem_ld32_async(tl + kColS + half * 32, r);
-      umma::tmem_wait_ld(r);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        p.h_final[((b * Dm + h * P + half * 32 + j) * N) + tid] = __uint_as_float(r[j]);
-    }
+    for (int j = 0; j < 32; ++j)
+      p.h_final[((b * Dm + h * P + hf * 32 + j) * N) + row] = __uint_as_float(r[j]);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -535,7 +502,7 @@ cudaError_t launch_g(const CUtensorMap& mc, const CUtensorMap& mb, const CUtenso
   e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.batch * p.nheads;
-  k<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(mc, mb, mx, p);
+  k<<<static_cast<unsigned>(grid), 2 * kThreads, kSmemBytes, s>>>(mc, mb, mx, p);
   return cudaGetLastError();
 }
 
