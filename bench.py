@@ -377,7 +377,8 @@ def decode_main(args):
                    "l2": "flushed between steps (256 MiB memset outside the timed events)"
                          if not args.no_flush else "not flushed"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": measured_traffic("decode", w.name),
                      "peak_source": peaks_src, "kernel": "decode",
                      "algorithmic": {"bytes": c["bytes"]}},
         "cpu_baseline": None if args.no_cpu_baseline else decode_cpu(w, args.cpu_seconds),
@@ -524,7 +525,8 @@ def bwd_main(args):
         roofline = {"bound": "alu", "achieved": c["fp32_ops"] / t_meas / 1e12,
                     "peak": FP32_PER_SM_CLK * sms * mhz * 1e6 / 1e12, "unit": "TFLOP/s fp32",
                     "frac": r["t_roof"] / t_meas}
-    roofline.update({"traffic": None, "kernel": "bwd", "peak_source": peaks_src,
+    roofline.update({"traffic": measured_traffic("bwd", w.name), "kernel": "bwd",
+                     "peak_source": peaks_src,
                      "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
                                  "fp32": r["t_fp32"] * 1e6},
                      "algorithmic": {"bytes": c["bytes"], "exps": c["exps"],
