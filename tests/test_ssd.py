@@ -131,3 +131,69 @@ def test_ssd_full_size_sampled(oracle):
         yg = y[b:b + 1, :, ch].float().cpu().numpy().astype(np.float64)
         e = rel(yg, y_ref)
         assert e <= TOL_Y, f"(b={b}, h={h}) y rel err {e:.3e}"
+
+
+def _halves(t, key):
+    """Split the state dimension (last axis) of B or C in two contiguous halves."""
+    return t[key][..., :64].contiguous(), t[key][..., 64:].contiguous()
+
+
+def test_ssd_agrees_with_the_diagonal_scan(oracle):
+    """With the head's step size and decay copied to its channels and states,
+    the diagonal scan (STREAM tier, fp32 state) computes the same recurrence.
+    The scan takes at most 64 states, so the 128 states are split in two and,
+    without the gate, y is the sum of the two halves' outputs (D counted in
+    one).  Both paths match the oracle, and each other within twice the bf16
+    bound (two roundings of the summed outputs)."""
+    w = BASE.scaled(batch=2, seqlen=640, nheads=2, gate=False)
+    inp = W.make_ssd_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    P, N = w.headdim, w.dstate
+    y_ssd = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], None, None,
+                      nheads=w.nheads)
+    delta_full = t["delta"].repeat_interleave(P, dim=2).contiguous()
+    A_half = t["A"].repeat_interleave(P)[:, None].expand(w.dim, N // 2).contiguous()
+    (B1, B2), (C1, C2) = _halves(t, "B"), _halves(t, "C")
+    y1, _ = S.scan_fwd(t["x"], delta_full, A_half, B1, C1, t["D"], None, None)
+    y2, _ = S.scan_fwd(t["x"], delta_full, A_half, B2, C2, None, None, None)
+    torch.cuda.synchronize()
+    y_ref = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           None, nheads=w.nheads)
+    a = y_ssd.float().cpu().numpy().astype(np.float64)
+    s2 = (y1.float() + y2.float()).cpu().numpy().astype(np.float64)
+    assert rel(a, y_ref) <= TOL_Y
+    assert rel(s2, y_ref) <= 2 * TOL_Y
+    assert rel(a, s2) <= 2 * TOL_Y
+
+
+def test_decode_continues_an_ssd_sequence(oracle):
+    """The SSD form's final state, handed to the decode step (with the head's
+    step size and decay copied to its channels and states, and the 128 states
+    in two halves of 64 as for the scan), continues the sequence: decoding the
+    last steps one by one gives the oracle's outputs for the whole sequence at
+    those steps."""
+    w = BASE.scaled(batch=2, seqlen=260, nheads=2, gate=False)
+    inp = W.make_ssd_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    P, N, k = w.headdim, w.dstate, 256
+    pre = {n: t[n][:, :k].contiguous() for n in ("x", "delta", "B", "C")}
+    _, state = S.ssd_fwd(pre["x"], pre["delta"], t["A"], pre["B"], pre["C"], t["D"], None, None,
+                         nheads=w.nheads, want_final=True)
+    st1, st2 = state[..., :64].contiguous(), state[..., 64:].contiguous()
+    A_half = t["A"].repeat_interleave(P)[:, None].expand(w.dim, N // 2).contiguous()
+    ys = []
+    for s in range(k, w.seqlen):
+        xs = t["x"][:, s].contiguous()
+        dstep = t["delta"][:, s].repeat_interleave(P, dim=1).contiguous()
+        Bs, Cs = t["B"][:, s], t["C"][:, s]
+        ya = S.decode_step(xs, dstep, A_half, Bs[:, :64].contiguous(), Cs[:, :64].contiguous(),
+                           t["D"], None, state=st1)
+        yb = S.decode_step(xs, dstep, A_half, Bs[:, 64:].contiguous(), Cs[:, 64:].contiguous(),
+                           None, None, state=st2)
+        ys.append(ya.float() + yb.float())
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    y_ref = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], None,
+                           nheads=w.nheads)
+    got = torch.stack(ys, dim=1).cpu().numpy().astype(np.float64)
+    assert rel(got, y_ref[:, k:]) <= 2 * TOL_Y
