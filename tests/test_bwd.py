@@ -38,6 +38,9 @@ CASES = {
     "fp32-n2-gate-chunk7": dict(e=dict(batch=2, L=60, dim=8, N=2, gate=True), chunk=7, h0=False),
     "bf16-n8-mask-chunk512": dict(e=dict(batch=3, L=1100, dim=32, N=8, dtype="bf16",
                                          mask=[1100, 5, 1024]), chunk=512, h0=True),
+    # chunks of exactly one replay piece: the chunk states are the checkpoints
+    "fp32-gate-mask-chunk16": dict(e=dict(batch=2, L=100, dim=24, N=16, gate=True,
+                                          mask=[100, 37]), chunk=16, h0=True),
 }
 
 
