@@ -198,6 +198,8 @@ def parse():
                          "backward, replaying from chunk states (--bwd-chunk); ssd: the "
                          "SSD form (one decay per head) on the tensor cores")
     ap.add_argument("--bwd-chunk", type=int, default=256)
+    ap.add_argument("--ssd-workload", type=int, default=1,
+                    help="with --op ssd: 1 = 128 states, 2 = 256 states")
     return ap.parse_args()
 
 
@@ -640,7 +642,7 @@ def ssd_main(args):
     from selective_state_space_fwd_gb300 import build as Bld
     from selective_state_space_fwd_gb300 import workloads as W
     rank, world, local = dist_env()
-    w = W.SSD_WORKLOADS[1]
+    w = W.SSD_WORKLOADS[args.ssd_workload]
     inp = W.make_ssd_inputs(w)
     if args.impl == "reference":
         if rank == 0:

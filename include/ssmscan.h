@@ -248,8 +248,8 @@ ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const 
  *   out_y     : device bf16 [batch, seqlen, nheads*headdim], 16-byte aligned.
  *   out_final_state : device fp32 [batch, nheads*headdim, dstate], the state
  *               after the last step, or NULL.
- * Supported: dtype SSM_BF16, headdim 64, dstate 128; other sizes or fp32 return
- * SSM_ERR_UNSUPPORTED.  The products take bf16 operands (the inputs, the masked
+ * Supported: dtype SSM_BF16, headdim 64, dstate 128 or 256; other sizes or fp32
+ * return SSM_ERR_UNSUPPORTED.  The products take bf16 operands (the inputs, the masked
  * decay-weighted block matrix and the state entering a block, rounded to bf16)
  * and accumulate in fp32; the state between blocks of 128 steps stays fp32.
  * All pointers are caller-owned; nothing is allocated.  Asynchronous on

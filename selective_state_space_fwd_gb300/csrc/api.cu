@@ -384,7 +384,7 @@ ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const v
   const ssm_ssd_shapes& s = *shapes;
   if (s.batch < 1 || s.seqlen < 0 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1)
     return SSM_ERR_SHAPE;
-  if (dtype != SSM_BF16 || s.headdim != ssm::kSsdHeadDim || s.dstate != ssm::kSsdState)
+  if (dtype != SSM_BF16 || s.headdim != ssm::kSsdHeadDim || !ssm::ssd_supported_state(s.dstate))
     return SSM_ERR_UNSUPPORTED;
   int64_t dim, bl, bld, bln, bdn, bh;
   const int64_t lim = int64_t(1) << 60;

@@ -40,40 +40,55 @@
 namespace ssm {
 namespace {
 
-constexpr int Q = kSsdChunk, P = kSsdHeadDim, N = kSsdState;
-constexpr int kThreads = 128;
+constexpr int Q = kSsdChunk, P = kSsdHeadDim;
+constexpr int kThreads = 128;  // rows of a block; the CTA has two threads per row
 constexpr unsigned kSsdWaitLimit = 1u << 24;  // try_wait polls before a wait gives up
 constexpr unsigned kErrSsdWait = 2u;
 constexpr unsigned kErrSsdAlign = 4u;  // shared memory not 1024-byte aligned: nothing computed
-static_assert(N == Q, "the C / B tile and the masked block matrix share one layout");
 
 // Two tile layouts.  The tiles that arrive by TMA (C, B, x) are 128-byte
-// swizzled: 64 bf16 of each of the 128 rows per 16 KB half, row r at r * 128,
+// swizzled: 64 bf16 of each of the 128 rows per 16 KB part, row r at r * 128,
 // its 16-byte chunk c stored at chunk c ^ (r mod 8), in 1024-byte atoms of 8
 // rows (the pattern the TMA writes and the tensor core reads).  The tiles that
 // threads write (Xw, S, Ym) are column strips: strip c holds 16 bytes (8 bf16)
-// of each of the 128 rows, row r at c * kStrip + r * 16; core matrix (r8, c)
-// then sits at c * kStrip + r8 * 128, a K-major operand when the strips run
+// of each row, row r at c * (strip size) + r * 16; core matrix (r8, c) then
+// sits at c * (strip size) + r8 * 128, a K-major operand when the strips run
 // along K and an MN-major one when they run along M/N.
-constexpr uint32_t kStrip = Q * 16;
-constexpr uint32_t kHalf = Q * 128;               // one 64-column half of a swizzled tile
-constexpr uint32_t kTileC = 0;                    // C rows [t x n], swizzled, halves n < 64, n >= 64
-constexpr uint32_t kTileB = kTileC + N * Q * 2;   // B rows [s x n], as C; then Ym [t x s] in strips
-constexpr uint32_t kTileX = kTileB + N * Q * 2;   // x rows [s x p], swizzled
-constexpr uint32_t kTileXw = kTileX + P * Q * 2;  // delta_s 2^(cs_end - cs_s) x_s, as x
-constexpr uint32_t kTileS = kTileXw + P * Q * 2;  // state rows [n x p] entering the block, as x
-constexpr uint32_t kDs = kTileS + P * N * 2;      // D of the head's channels, fp32 [P]
-constexpr uint32_t kWarpTot = kDs + P * 4;        // per-warp totals of the scan of cs
-constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier of the matrix products
-constexpr uint32_t kTBar = kBar + 8;              // mbarrier of the TMA copies
-constexpr uint32_t kSlot = kTBar + 8;             // TMEM base address
-constexpr uint32_t kSmemBytes = kSlot + 8;
-static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM (1 KB reserved per CTA)");
-constexpr uint32_t kTileBytesC = N * Q * 2, kTileBytesB = N * Q * 2, kTileBytesX = P * Q * 2;
+constexpr uint32_t kStrip = Q * 16;   // a strip of 128 rows
+constexpr uint32_t kHalf = Q * 128;   // one 64-column part of a swizzled tile
 
-// TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); the state
-// S [192,256) (row n in lane n), which the state-update product accumulates onto.
-constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColS = 192, kTmemCols = 256;
+// Layout for NS states: C and B tiles of NS / 64 swizzled parts, the state
+// tile [p x n] in strips of NS rows; TMEM holds NS / 128 state rows per lane.
+template <int NS>
+struct SsdCfg {
+  static_assert(NS == 128 || NS == 256, "128 or 256 states");
+  static constexpr int N = NS;
+  static constexpr int NQ = N / 64;   // 64-column parts of the C and B tiles
+  static constexpr int NH = N / 128;  // state rows per TMEM lane (row n, n + 128)
+  static constexpr uint32_t kStripS = N * 16;
+  static constexpr uint32_t kTileC = 0;                    // C rows [t x n], swizzled parts
+  static constexpr uint32_t kTileB = kTileC + N * Q * 2;   // B rows [s x n], as C; then Ym [t x s]
+  static constexpr uint32_t kTileX = kTileB + N * Q * 2;   // x rows [s x p], swizzled
+  static constexpr uint32_t kTileXw = kTileX + P * Q * 2;  // delta_s 2^(cs_end - cs_s) x_s, strips
+  static constexpr uint32_t kTileS = kTileXw + P * Q * 2;  // state rows [n x p], strips of N rows
+  static constexpr uint32_t kDs = kTileS + P * N * 2;      // D of the head's channels, fp32 [P]
+  static constexpr uint32_t kWarpTot = kDs + P * 4;        // per-warp totals of the scan of cs
+  static constexpr uint32_t kBar = kWarpTot + 16;          // mbarrier of the matrix products
+  static constexpr uint32_t kTBar = kBar + 8;              // mbarrier of the TMA copies
+  static constexpr uint32_t kSlot = kTBar + 8;             // TMEM base address
+  static constexpr uint32_t kSmemBytes = kSlot + 8;
+  static constexpr uint32_t kTileBytesC = N * Q * 2, kTileBytesB = N * Q * 2,
+                            kTileBytesX = P * Q * 2;
+  // TMEM columns (fp32): G [0,128) then Yd [0,64); Yo [128,192); the state
+  // [192, 192 + 64 NH) (rows n and n + 128 of lane n), which the state-update
+  // product accumulates onto.
+  static constexpr uint32_t kColG = 0, kColYd = 0, kColYo = 128, kColS = 192;
+  static constexpr uint32_t kTmemCols = NH == 1 ? 256 : 512;
+  static constexpr int kMinBlocks = NH == 1 ? 2 : 1;  // CTAs per SM
+  static_assert(kMinBlocks * (kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM (1 KB reserved each)");
+  static_assert(kMinBlocks * kTmemCols <= 512, "TMEM columns per SM");
+};
+static_assert(Q == 128, "the masked block matrix shares the C / B tile layout");
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -126,10 +141,15 @@ __device__ __forceinline__ float lg2(float v) {
   return r;
 }
 
-template <bool GATE>
-__global__ void __launch_bounds__(2 * kThreads, 2)
+template <int NS, bool GATE>
+__global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
     ssd_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_b,
                const __grid_constant__ CUtensorMap tm_x, const SsdParams p) {
+  using K = SsdCfg<NS>;
+  constexpr int N = K::N, NQ = K::NQ, NH = K::NH;
+  constexpr uint32_t kTileC = K::kTileC, kTileB = K::kTileB, kTileX = K::kTileX,
+                     kTileXw = K::kTileXw, kTileS = K::kTileS, kStripS = K::kStripS;
+  constexpr uint32_t kColG = K::kColG, kColYd = K::kColYd, kColYo = K::kColYo, kColS = K::kColS;
   extern __shared__ __align__(1024) unsigned char sm[];
   // 256 threads: thread (row, hf) handles row `row` of the block (step, or
   // state row) and the 32-column half `hf` of its 64 channels
@@ -138,11 +158,11 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
   const int64_t H = p.nheads, L = p.seqlen, Dm = p.nheads * P;
   const int64_t b = blockIdx.x / H, h = blockIdx.x % H;
   const uint32_t s0 = umma::smem_u32(sm);
-  const uint32_t bar = s0 + kBar, tbar = s0 + kTBar;
+  const uint32_t bar = s0 + K::kBar, tbar = s0 + K::kTBar;
   float* sE = reinterpret_cast<float*>(sm + kTileXw);
   float* sF = sE + Q;
-  float* sWt = reinterpret_cast<float*>(sm + kWarpTot);
-  float* sD = reinterpret_cast<float*>(sm + kDs);
+  float* sWt = reinterpret_cast<float*>(sm + K::kWarpTot);
+  float* sD = reinterpret_cast<float*>(sm + K::kDs);
   const auto* dg = static_cast<const __nv_bfloat16*>(p.delta);
   const auto* zg = static_cast<const __nv_bfloat16*>(p.z);
   auto* yg = static_cast<__nv_bfloat16*>(p.y);
@@ -154,15 +174,15 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
   }
   auto copy_c = [&](int64_t t0) {
     const int r = static_cast<int>(b * L + t0);
-    umma::mbar_expect_tx(tbar, kTileBytesC);
-    umma::tma_load_2d(s0 + kTileC, &tm_c, 0, r, tbar);
-    umma::tma_load_2d(s0 + kTileC + kHalf, &tm_c, 64, r, tbar);
+    umma::mbar_expect_tx(tbar, K::kTileBytesC);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) umma::tma_load_2d(s0 + kTileC + q * kHalf, &tm_c, 64 * q, r, tbar);
   };
   auto copy_bx = [&](int64_t t0) {
     const int r = static_cast<int>(b * L + t0);
-    umma::mbar_expect_tx(tbar, kTileBytesB + kTileBytesX);
-    umma::tma_load_2d(s0 + kTileB, &tm_b, 0, r, tbar);
-    umma::tma_load_2d(s0 + kTileB + kHalf, &tm_b, 64, r, tbar);
+    umma::mbar_expect_tx(tbar, K::kTileBytesB + K::kTileBytesX);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) umma::tma_load_2d(s0 + kTileB + q * kHalf, &tm_b, 64 * q, r, tbar);
     umma::tma_load_2d(s0 + kTileX, &tm_x, static_cast<int>(h * P), r, tbar);
   };
   if (s0 & 1023u) {
@@ -170,7 +190,7 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
     return;
   }
 
-  if (warp == 0) umma::tmem_alloc(s0 + kSlot, kTmemCols);
+  if (warp == 0) umma::tmem_alloc(s0 + K::kSlot, K::kTmemCols);
   if (tid == 0) {
     umma::mbar_init(bar, 2);
     umma::mbar_init(tbar, 2);
@@ -183,20 +203,22 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + kSlot);
+  const uint32_t tm = *reinterpret_cast<volatile uint32_t*>(sm + K::kSlot);
   const uint32_t tl = tm + (static_cast<uint32_t>(lw * 32) << 16);  // this warp's TMEM lanes
   const float al = __ldg(p.A + h) * kLog2e;
   const uint32_t rowo = row * 16;
   const int c0 = hf * 4;  // this thread's first 8-channel chunk
 
-  {  // this thread's half of state row n = row into TMEM: h0, else zeros
+#pragma unroll
+  for (int jh = 0; jh < NH; ++jh) {  // this thread's half of state row row + 128 jh: h0, else 0
     uint32_t r[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      r[j] = __float_as_uint(p.h0 ? p.h0[((b * Dm + h * P + hf * 32 + j) * N) + row] : 0.f);
-    umma::tmem_st32(tl + kColS + hf * 32, r);
-    umma::tmem_wait_st();
+      r[j] = __float_as_uint(
+          p.h0 ? p.h0[((b * Dm + h * P + hf * 32 + j) * N) + row + 128 * jh] : 0.f);
+    umma::tmem_st32(tl + kColS + 64 * jh + hf * 32, r);
   }
+  umma::tmem_wait_st();
 
   uint32_t phase = 0, tphase = 0;
   int pending = Lv > 0 ? 2 : 0;
@@ -250,7 +272,10 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
     for (int c = 0; c < 4; ++c) xr[c] = in ? lds128(sm, kTileX + swz(row, c0 + c)) : make_uint4(0, 0, 0, 0);
     if (!in) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) sts128(sm, kTileB + hf * kHalf + row * 128 + c * 16, make_uint4(0, 0, 0, 0));
+      for (int q = hf; q < NQ; q += 2)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          sts128(sm, kTileB + q * kHalf + row * 128 + c * 16, make_uint4(0, 0, 0, 0));
 #pragma unroll
       for (int c = 0; c < 4; ++c) sts128(sm, kTileX + row * 128 + (c0 + c) * 16, make_uint4(0, 0, 0, 0));
     }
@@ -262,21 +287,24 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
       for (int j = 0; j < 8; ++j) f[j] *= u;
       sts128(sm, kTileXw + (c0 + c) * kStrip + rowo, pack8(f));
     }
-    {  // this thread's half of the state row: bf16 operand of Yo; kept scaled by 2^cs_end
+    {  // this thread's halves of the state rows: bf16 operand of Yo; kept scaled by 2^cs_end
       const float etot = ex2(tot);
-      uint32_t r0[32];
-      umma::tmem_ld32_async(tl + kColS + hf * 32, r0);
-      umma::tmem_wait_ld(r0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float f[8];
+      for (int jh = 0; jh < NH; ++jh) {
+        uint32_t r0[32];
+        umma::tmem_ld32_async(tl + kColS + 64 * jh + hf * 32, r0);
+        umma::tmem_wait_ld(r0);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
-        sts128(sm, kTileS + (c0 + c) * kStrip + rowo, pack8(f));
+        for (int c = 0; c < 4; ++c) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
+          sts128(sm, kTileS + (c0 + c) * kStripS + (row + 128 * jh) * 16, pack8(f));
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
+        umma::tmem_st32(tl + kColS + 64 * jh + hf * 32, r0);
       }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
-      umma::tmem_st32(tl + kColS + hf * 32, r0);
       umma::tmem_wait_st();
     }
     umma::fence_smem_to_async();
@@ -290,6 +318,13 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
       for (int k = 0; k < N / 16; ++k)
         umma::mma_bf16(tm + kColG, desc_kmaj_sw(s0 + kTileC, k), desc_kmaj_sw(s0 + kTileB, k), idG,
                        k > 0);
+      if (NH == 2) {  // the second half of the state rows (n >= 128), parts 2 and 3 of B
+        constexpr uint32_t idS = umma::idesc_bf16(128, P, true, true);
+#pragma unroll
+        for (int k = 0; k < Q / 16; ++k)
+          umma::mma_bf16(tm + kColS + 64, desc_mnmaj_sw(s0 + kTileB + 2 * kHalf, k),
+                         umma::smem_desc(s0 + kTileXw + k * 256, 128, kStrip), idS, true);
+      }
       umma::mma_commit(bar);
     }
     if (tid == 32) {
@@ -299,7 +334,7 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
 #pragma unroll
       for (int k = 0; k < N / 16; ++k)
         umma::mma_bf16(tm + kColYo, desc_kmaj_sw(s0 + kTileC, k),
-                       umma::smem_desc(s0 + kTileS + k * 256, 128, kStrip), idO, k > 0);
+                       umma::smem_desc(s0 + kTileS + k * 256, 128, kStripS), idO, k > 0);
 #pragma unroll
       for (int k = 0; k < Q / 16; ++k)
         umma::mma_bf16(tm + kColS, desc_mnmaj_sw(s0 + kTileB, k),
@@ -446,16 +481,19 @@ __global__ void __launch_bounds__(2 * kThreads, 2)
     umma::mbar_wait(tbar, tphase, kSsdWaitLimit);
   }
   if (!bad && p.h_final) {
-    uint32_t r[32];
-    umma::tmem_ld32_async(tl + kColS + hf * 32, r);
-    umma::tmem_wait_ld(r);
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      p.h_final[((b * Dm + h * P + hf * 32 + j) * N) + row] = __uint_as_float(r[j]);
+    for (int jh = 0; jh < NH; ++jh) {
+      uint32_t r[32];
+      umma::tmem_ld32_async(tl + kColS + 64 * jh + hf * 32, r);
+      umma::tmem_wait_ld(r);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        p.h_final[((b * Dm + h * P + hf * 32 + j) * N) + row + 128 * jh] = __uint_as_float(r[j]);
+    }
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 0) umma::tmem_dealloc(tm, kTmemCols);
+  if (warp == 0) umma::tmem_dealloc(tm, K::kTmemCols);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -492,34 +530,39 @@ bool tile_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool GATE>
+template <int NS, bool GATE>
 cudaError_t launch_g(const CUtensorMap& mc, const CUtensorMap& mb, const CUtensorMap& mx,
                      const SsdParams& p, cudaStream_t s) {
-  auto* k = ssd_kernel<GATE>;
+  using K = SsdCfg<NS>;
+  auto* k = ssd_kernel<NS, GATE>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
+                                       static_cast<int>(K::kSmemBytes));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   const int64_t grid = p.batch * p.nheads;
-  k<<<static_cast<unsigned>(grid), 2 * kThreads, kSmemBytes, s>>>(mc, mb, mx, p);
+  k<<<static_cast<unsigned>(grid), 2 * kThreads, K::kSmemBytes, s>>>(mc, mb, mx, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t ssd_smem_bytes() { return kSmemBytes; }
+size_t ssd_smem_bytes(int64_t dstate) {
+  return dstate == 256 ? SsdCfg<256>::kSmemBytes : SsdCfg<128>::kSmemBytes;
+}
 
 cudaError_t launch_ssd(const SsdParams& p, cudaStream_t s) {
-  if (p.headdim != P || p.dstate != N || p.batch * p.nheads <= 0 ||
+  if (p.headdim != P || !ssd_supported_state(p.dstate) || p.batch * p.nheads <= 0 ||
       p.batch * p.nheads > 0x7FFFFFFF || p.batch * p.seqlen > 0x7FFFFFFF)
     return cudaErrorInvalidValue;
   CUtensorMap mc, mb, mx;
   const int64_t rows = p.batch * p.seqlen > 0 ? p.batch * p.seqlen : 1;
-  if (!tile_map(&mc, p.C, N, rows) || !tile_map(&mb, p.B, N, rows) ||
+  if (!tile_map(&mc, p.C, p.dstate, rows) || !tile_map(&mb, p.B, p.dstate, rows) ||
       !tile_map(&mx, p.x, p.nheads * P, rows))
     return cudaErrorInvalidValue;
-  return p.z ? launch_g<true>(mc, mb, mx, p, s) : launch_g<false>(mc, mb, mx, p, s);
+  if (p.dstate == 256)
+    return p.z ? launch_g<256, true>(mc, mb, mx, p, s) : launch_g<256, false>(mc, mb, mx, p, s);
+  return p.z ? launch_g<128, true>(mc, mb, mx, p, s) : launch_g<128, false>(mc, mb, mx, p, s);
 }
 
 }  // namespace ssm

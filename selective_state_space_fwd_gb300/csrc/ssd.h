@@ -26,9 +26,9 @@ struct SsdParams {
 // Steps per block (the M of every product), and the supported head and state sizes.
 constexpr int kSsdChunk = 128;
 constexpr int kSsdHeadDim = 64;
-constexpr int kSsdState = 128;
+inline bool ssd_supported_state(int64_t n) { return n == 128 || n == 256; }
 
-size_t ssd_smem_bytes();
+size_t ssd_smem_bytes(int64_t dstate);
 
 namespace stream {
 unsigned int* error_word();  // the library's sticky device error word (kernel_stream.cu)

@@ -123,6 +123,8 @@ class SsdWorkload:
 SSD_WORKLOADS = {
     1: SsdWorkload(201, "ssd-bf16-gated-b8-l4096-h32-p64-n128", 8, 4096, 32, 64, 128, True, None,
                    21),
+    2: SsdWorkload(202, "ssd-bf16-gated-b8-l4096-h32-p64-n256", 8, 4096, 32, 64, 256, True, None,
+                   22),
 }
 
 

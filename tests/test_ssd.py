@@ -49,6 +49,11 @@ CASES = {
     "b2-l1-h2": dict(w=dict(batch=2, seqlen=1, nheads=2, gate=True), h0=True),
     # long enough for the decay between blocks to matter, several heads
     "b1-l1100-h4": dict(w=dict(batch=1, seqlen=1100, nheads=4, gate=True), h0=False),
+    # 256 states: four 64-column parts of C and B, two state rows per TMEM lane
+    "n256-b2-l300-h2-gate-h0": dict(w=dict(batch=2, seqlen=300, nheads=2, gate=True, dstate=256),
+                                    h0=True),
+    "n256-b3-l260-h1-mask": dict(w=dict(batch=3, seqlen=260, nheads=1, gate=False, dstate=256),
+                                 h0=False, valid=[260, 0, 131]),
 }
 
 
@@ -107,6 +112,24 @@ def test_ssd_split_equals_whole(oracle):
     # the same arithmetic on the same blocks: identical results
     assert torch.equal(torch.cat([y1, y2], dim=1), y)
     assert torch.equal(f2, fin)
+
+
+def test_ssd_n256_split_equals_whole(oracle):
+    """As above with 256 states: the state rows n and n + 128 share a TMEM lane."""
+    w = BASE.scaled(batch=1, seqlen=384, nheads=2, gate=True, dstate=256)
+    inp = W.make_ssd_inputs(w)
+    t = W.to_torch(inp, "cuda")
+    y, fin = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], None,
+                       nheads=w.nheads, want_final=True)
+    k = 128
+    part = {n: t[n][:, :k].contiguous() for n in ("x", "delta", "B", "C", "z")}
+    rest = {n: t[n][:, k:].contiguous() for n in ("x", "delta", "B", "C", "z")}
+    _, f1 = S.ssd_fwd(part["x"], part["delta"], t["A"], part["B"], part["C"], t["D"], part["z"],
+                      None, nheads=w.nheads, want_final=True)
+    y2, f2 = S.ssd_fwd(rest["x"], rest["delta"], t["A"], rest["B"], rest["C"], t["D"], rest["z"],
+                       None, nheads=w.nheads, h0=f1, want_final=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y[:, k:]) and torch.equal(f2, fin)
 
 
 def test_ssd_full_size_sampled(oracle):
