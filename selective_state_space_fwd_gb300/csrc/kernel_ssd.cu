@@ -26,10 +26,11 @@
 // of the next block starts once the first products are done with C, the B
 // and x copies once the second is.  Threads i and i + 128 share row i: step
 // i of the block for the masked block matrix and the epilogue (TMEM lane i
-// holds row i of G, Yd and Yo) and state row i (lane i of S), each taking
-// half of the columns (warps w and w + 4 read the same TMEM lanes).  Shared
-// memory is about 115 KB, so two CTAs share an SM and one CTA's staging and
-// epilogue overlap the other's matrix products.
+// holds row i of G, Yd and Yo) and state row i (and i + 128 with 256 states;
+// lane i of S), each taking half of the columns (warps w and w + 4 read the
+// same TMEM lanes).  With 128 states shared memory is about 115 KB, so two
+// CTAs share an SM and one CTA's staging and epilogue overlap the other's
+// matrix products; with 256 states (C and B tiles of 64 KB) one CTA fits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -119,18 +120,18 @@ __device__ __forceinline__ uint4 ldg128(const void* p) {
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t k_stride, uint32_t mn_stride) {
   return umma::smem_desc(addr, k_stride, mn_stride) | (uint64_t(2) << 61);
 }
-// K-major swizzled operand with 128 rows and K = 128 in two halves: the
-// descriptor of K step k (16 elements): half k / 4, 32 bytes per step inside
+// K-major swizzled operand with 128 rows, K in 64-column parts: the
+// descriptor of K step k (16 elements): part k / 4, 32 bytes per step inside
 // the 128-byte rows, 1024 bytes between 8-row groups.
 __device__ __forceinline__ uint64_t desc_kmaj_sw(uint32_t tile, int k) {
   return desc_sw128(tile + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
 }
 // MN-major swizzled operand (rows along K): K step k is 16 rows = 2048 bytes,
-// 1024 bytes between 8-row groups, kHalf between 64-wide MN halves.
+// 1024 bytes between 8-row groups, kHalf between 64-wide MN parts.
 __device__ __forceinline__ uint64_t desc_mnmaj_sw(uint32_t tile, int k) {
   return desc_sw128(tile + k * 2048, kHalf, 1024);
 }
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a swizzled half
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a swizzled part
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
@@ -517,7 +518,7 @@ EncodeTiledFn encode() {
 }
 
 // 2-D map over a bf16 [rows, inner] tensor with a box of 64 elements x 128
-// rows, 128-byte swizzled (one half of a tile).  Rows past the end read as zeros.
+// rows, 128-byte swizzled (one part of a tile).  Rows past the end read as zeros.
 bool tile_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows) {
   EncodeTiledFn fn = encode();
   if (!fn) return false;
