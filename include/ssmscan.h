@@ -253,7 +253,8 @@ ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const 
  * decay-weighted block matrix and the state entering a block, rounded to bf16)
  * and accumulate in fp32; the state between blocks of 128 steps stays fp32.
  * All pointers are caller-owned; nothing is allocated.  Asynchronous on
- * `stream`; argument errors return a status before launch.  A CTA whose
+ * `stream`; argument errors return a status before launch (an empty sequence,
+ * seqlen 0, is SSM_ERR_SHAPE, as for the scan).  A CTA whose
  * bounded wait on the tensor cores gives up sets the sticky device error word
  * (ssm_check_device_errors returns SSM_ERR_TIMEOUT; outputs undefined).
  */

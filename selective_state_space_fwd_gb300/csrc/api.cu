@@ -382,7 +382,7 @@ ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const v
   if (!shapes) return SSM_ERR_NULL;
   if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
   const ssm_ssd_shapes& s = *shapes;
-  if (s.batch < 1 || s.seqlen < 0 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1)
+  if (s.batch < 1 || s.seqlen < 1 || s.nheads < 1 || s.headdim < 1 || s.dstate < 1)
     return SSM_ERR_SHAPE;
   if (dtype != SSM_BF16 || s.headdim != ssm::kSsdHeadDim || !ssm::ssd_supported_state(s.dstate))
     return SSM_ERR_UNSUPPORTED;

@@ -61,6 +61,7 @@ def _call(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None
     (dict(y=None), Bd.Status.ERR_NULL),
     (dict(shapes=(0, 8, 4, 16, 0)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(2, -1, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 0, 4, 16, 0)), Bd.Status.ERR_SHAPE),  # an empty sequence
     (dict(shapes=(2, 8, 0, 16, 0)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(2, 8, 4, 0, 0)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(2, 8, 4, 16, -5)), Bd.Status.ERR_SHAPE),
@@ -163,6 +164,7 @@ def _bwd(shapes=(2, 8, 4, 16, 4), z=None, dz=None, states=FAKE, dA=FAKE, x=FAKE,
 
 @pytest.mark.parametrize("kw,status", [
     (dict(shapes=(2, 8, 4, 16, 0)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 0, 4, 16, 4)), Bd.Status.ERR_SHAPE),  # an empty sequence
     (dict(shapes=(2, 8, 4, 16, 513)), Bd.Status.ERR_UNSUPPORTED),
     (dict(states=None), Bd.Status.ERR_NULL),
     (dict(dA=None), Bd.Status.ERR_NULL),
@@ -191,6 +193,7 @@ def _ssd(x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, valid=None,
     (dict(y=None), Bd.Status.ERR_NULL),
     (dict(shapes=(0, 256, 4, 64, 128)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(2, -1, 4, 64, 128)), Bd.Status.ERR_SHAPE),
+    (dict(shapes=(2, 0, 4, 64, 128)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(2, 256, 0, 64, 128)), Bd.Status.ERR_SHAPE),
     (dict(shapes=(1 << 40, 1 << 30, 4, 64, 128)), Bd.Status.ERR_SHAPE),
     (dict(dtype=0), Bd.Status.ERR_UNSUPPORTED),
