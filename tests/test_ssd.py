@@ -42,6 +42,9 @@ CASES = {
                             valid=[384, 0, 128]),
     "b2-l260-h2-mask-ragged": dict(w=dict(batch=2, seqlen=260, nheads=2, gate=False), h0=False,
                                    valid=[200, 131]),
+    # valid lengths outside [0, L] are clamped
+    "b2-l300-h1-mask-clamp": dict(w=dict(batch=2, seqlen=300, nheads=1, gate=True), h0=True,
+                                  valid=[500, -5]),
     # exactly one block, no gate, no D
     "b1-l128-h1-noD": dict(w=dict(batch=1, seqlen=128, nheads=1, gate=False), h0=False,
                            no_d=True),
@@ -90,7 +93,8 @@ def test_ssd_matches_oracle(oracle, name):
     assert ef <= TOL_STATE, f"final state rel err {ef:.3e}"
     if inp["valid_len"] is not None:
         for b, v in enumerate(inp["valid_len"]):
-            assert np.all(yg[b, int(v):] == 0)  # past valid_len the output is exactly 0
+            v = min(max(int(v), 0), w.seqlen)
+            assert np.all(yg[b, v:] == 0)  # past valid_len the output is exactly 0
 
 
 def test_ssd_split_equals_whole(oracle):
