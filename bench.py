@@ -459,6 +459,40 @@ def bwd_counts(w, inp, chunk: int) -> dict:
             "fp32_ops": BWD_FP32_PER_NELT * ev * N, "bytes": rd + wr}
 
 
+def bwd_cpu(w, chunk: int, seconds: float) -> dict:
+    """The oracle's backward on a bounded channel sample of the workload (the
+    first channels of every batch row; dB and dC are then partial sums over
+    those channels, which does not change the work per element)."""
+    from oracle import ref_scan
+    from selective_state_space_fwd_gb300 import workloads as W
+    threads = os.cpu_count() or 1
+    inp = W.make_inputs(w)
+    Bt, L, Dm = inp["x"].shape
+    rng = np.random.default_rng(7)
+
+    def run(ch):
+        s = cpu_sample_inputs(inp, ch)
+        dy = rng.standard_normal((Bt, L, ch))
+        t0 = time.perf_counter()
+        ref_scan.scan_bwd(s["x"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"],
+                          s["valid_len"], dy=dy, threads=threads)
+        return time.perf_counter() - t0
+
+    ch = 1
+    dt = run(ch)
+    while dt < 0.5 and ch < Dm:
+        ch = min(Dm, ch * 4)
+        dt = run(ch)
+    ch_target = int(min(Dm, max(1, ch * min(seconds, 20.0) / max(dt, 1e-6))))
+    if ch_target != ch:
+        ch = ch_target
+        dt = run(ch)
+    elems = Bt * L * ch
+    return {"value": elems / dt, "unit": "elements/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {Bt} batch rows x first {ch} of {Dm} channels x {L} steps "
+                      f"({elems} elements, {dt:.1f} s)"}
+
+
 def bwd_main(args):
     """The backward on device buffers, after one forward that writes the chunk states."""
     import torch
@@ -469,8 +503,17 @@ def bwd_main(args):
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps({"impl": "reference", "metric": BWD_METRIC,
-                              "unavailable": "the reference arm times only the forward oracle"}))
+            cpu = bwd_cpu(w, args.bwd_chunk, 150.0 / max(1, args.steps + args.warmup))
+            print(json.dumps({"impl": "reference", "metric": BWD_METRIC, "value": cpu["value"],
+                              "unit": "elements/s", "n_gpus": 1, "steps": args.steps,
+                              "warmup": args.warmup, "ms_per_step": None,
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                              "dtype": "f64", "data": "synthetic",
+                              "config": {"workload": w.name, "chunk_len": args.bwd_chunk},
+                              "cpu_baseline": cpu,
+                              "e2e": {"value": cpu["value"], "unit": "elements/s",
+                                      "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                  flush=True)
         return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -572,7 +615,8 @@ def bwd_main(args):
             "config": {"workload": w.name, "chunk_len": chunk, "gate": w.gate,
                        "masked": w.mask is not None,
                        "l2": "flushed between steps (256 MiB memset outside the timed events)"},
-            "roofline": roofline, "cpu_baseline": None,
+            "roofline": roofline,
+            "cpu_baseline": None if args.no_cpu_baseline else bwd_cpu(w, chunk, args.cpu_seconds),
             "e2e": {"value": c["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
                     "d2h_bytes_per_step": sum(v.numel() * v.element_size()
