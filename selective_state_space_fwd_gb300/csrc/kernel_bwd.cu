@@ -64,6 +64,29 @@ __device__ __forceinline__ void from4(const float4& v, float (&a)[G]) {
 }
 __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 
+// Paired fp32 (two states per f32x2 instruction) for the reverse step.
+typedef unsigned long long p64;
+__device__ __forceinline__ p64 pk(float lo, float hi) {
+  p64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk(p64 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ p64 mulx2(p64 a, p64 b) {
+  p64 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ p64 fmax2(p64 a, p64 b, p64 c) {
+  p64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 template <int N, typename T, bool GATE>
 __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
   using S = BwdShape<N>;
@@ -234,16 +257,47 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_kernel(const BwdParams p) {
           dzv = dyv * yp * sg * (1.f + zz * (1.f - sg));  // dy yp silu'(z)
         }
         float pdt = 0.f, pdx = 0.f, db[GB], dc[GB];
+        if constexpr (GB % 2 == 0) {  // two states per f32x2 instruction
+          const p64 dt2 = pk(dt, dt), xv2 = pk(xv, xv), dyp2 = pk(dyp, dyp);
+          p64 pdt2 = pk(0.f, 0.f), pdx2 = pk(0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < GB; ++g) {
-          const float a = ex2(dt * al[g]);
-          lam[g] = fmaf(cc[g], dyp, lam[g]);  // + C_t dyp_t
-          pdt = fmaf(lam[g], fmaf(bb[g], xv, av[g] * a * hp[g]), pdt);
-          pdx = fmaf(lam[g] * dt, bb[g], pdx);
-          db[g] = lam[g] * dt * xv;
-          dc[g] = dyp * hc[g];
-          dacc[g] = fmaf(lam[g] * dt * a, hp[g], dacc[g]);
-          lam[g] *= a;  // carried to step t - 1
+          for (int g = 0; g < GB; g += 2) {
+            const float2 arg = upk(mulx2(dt2, pk(al[g], al[g + 1])));
+            const p64 a2 = pk(ex2(arg.x), ex2(arg.y));
+            const p64 lam2 = fmax2(pk(cc[g], cc[g + 1]), dyp2, pk(lam[g], lam[g + 1]));  // + C dyp
+            const p64 q2 = mulx2(a2, pk(hp[g], hp[g + 1]));  // a_t h_{t-1}
+            const p64 bb2 = pk(bb[g], bb[g + 1]);
+            pdt2 = fmax2(lam2, fmax2(pk(av[g], av[g + 1]), q2, mulx2(bb2, xv2)), pdt2);
+            const p64 ld2 = mulx2(lam2, dt2);
+            pdx2 = fmax2(ld2, bb2, pdx2);
+            const float2 dbv = upk(mulx2(ld2, xv2));
+            const float2 dcv = upk(mulx2(dyp2, pk(hc[g], hc[g + 1])));
+            const float2 dav = upk(fmax2(ld2, q2, pk(dacc[g], dacc[g + 1])));
+            const float2 lv = upk(mulx2(lam2, a2));  // carried to step t - 1
+            db[g] = dbv.x;
+            db[g + 1] = dbv.y;
+            dc[g] = dcv.x;
+            dc[g + 1] = dcv.y;
+            dacc[g] = dav.x;
+            dacc[g + 1] = dav.y;
+            lam[g] = lv.x;
+            lam[g + 1] = lv.y;
+          }
+          const float2 pt = upk(pdt2), px = upk(pdx2);
+          pdt = pt.x + pt.y;
+          pdx = px.x + px.y;
+        } else {
+#pragma unroll
+          for (int g = 0; g < GB; ++g) {
+            const float a = ex2(dt * al[g]);
+            lam[g] = fmaf(cc[g], dyp, lam[g]);  // + C_t dyp_t
+            pdt = fmaf(lam[g], fmaf(bb[g], xv, av[g] * a * hp[g]), pdt);
+            pdx = fmaf(lam[g] * dt, bb[g], pdx);
+            db[g] = lam[g] * dt * xv;
+            dc[g] = dyp * hc[g];
+            dacc[g] = fmaf(lam[g] * dt * a, hp[g], dacc[g]);
+            lam[g] *= a;  // carried to step t - 1
+          }
         }
 #pragma unroll
         for (int m = NL / 2; m >= 1; m /= 2) {
