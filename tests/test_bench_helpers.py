@@ -42,3 +42,31 @@ def test_roof_terms():
 def test_measured_traffic_requires_matching_sources():
     assert bench.measured_traffic("stream", "no-such-workload") is None
     assert bench.measured_traffic("serial", W.WORKLOADS[2].name) is None
+
+
+def test_counts_ssd_workloads():
+    """The SSD form's bytes and product flops, by hand for both state sizes."""
+    for key, N in ((1, 128), (2, 256)):
+        w = W.SSD_WORKLOADS[key]
+        c = bench.ssd_counts(w)
+        Bt, L, H, P, Q = 8, 4096, 32, 64, 128
+        e = Bt * L * H * P
+        assert c["elements"] == e
+        # x, z read and y written (bf16), delta per (t, head), B and C rows, A and D
+        assert c["bytes"] == 3 * e * 2 + Bt * L * H * 2 + 2 * Bt * L * N * 2 + 4 * H + 4 * H * P
+        nb = L // Q
+        # C B^T once per (batch row, block); per head the block matrix times x, C times the
+        # state and the state update (2 flops per multiply-add)
+        assert c["flops"] == Bt * nb * 2 * Q * Q * N + Bt * H * nb * (2 * Q * Q * P + 4 * Q * N * P)
+
+
+def test_counts_backward():
+    w = W.WORKLOADS[2]
+    c = bench.bwd_counts(w, {"valid_len": None}, 256)
+    e = 8 * 4096 * 1024
+    assert c["exps"] == e * 16 and c["fp32_ops"] == bench.BWD_FP32_PER_NELT * e * 16
+    # reads: x, delta, dy, B, C, A, D, chunk states, valid rows; writes: dx, ddelta, dB, dC, dA, dD
+    reads = 3 * e * 4 + 2 * 8 * 4096 * 16 * 4 + 1024 * 16 * 4 + 1024 * 4 \
+        + 8 * 16 * 1024 * 16 * 4 + 8 * 4
+    writes = 2 * e * 4 + 2 * 8 * 4096 * 16 * 4 + 1024 * 16 * 4 + 1024 * 4
+    assert c["bytes"] == reads + writes
