@@ -231,3 +231,18 @@ def test_host_workspace_bytes(ssmlib):
         + 2 * 2 * 4 * 16 * 4 + 2 * 2 * 4 * 16 * 4
     assert need <= b <= need + 12 * 256
     assert Bd.host_workspace_bytes(0, 8, 4, 16) == 0
+
+
+def test_no_fallback_without_the_library(monkeypatch, tmp_path):
+    """Without the compiled library every entry fails loudly: there is no CPU path."""
+    import numpy as np
+    import torch
+    monkeypatch.setattr(Bd, "_lib", None)
+    monkeypatch.setattr(Bd, "LIB_PATH", str(tmp_path / "libssmscan.so"))
+    with pytest.raises(ImportError):
+        Bd.load()
+    x = torch.from_numpy(np.zeros((1, 4, 2), np.float32))
+    with pytest.raises(ImportError):
+        Bd.scan_fwd(x, x, torch.zeros(2, 4), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4))
+    with pytest.raises(ImportError):
+        Bd.ssd_fwd(x, x, torch.zeros(1), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4), nheads=1)
