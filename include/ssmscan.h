@@ -347,6 +347,17 @@ const char* ssm_kernel_name(ssm_kernel kernel);
  * SSM_ERR_TIMEOUT, or SSM_ERR_CUDA if the word cannot be read. */
 ssm_status ssm_check_device_errors(void);
 
+/* Self-test of the error path of the bounded device waits (no page
+ * counterpart: a diagnostic).  Launches, on `stream`, one thread that waits
+ * with the kernels' bounded wait on an mbarrier nothing ever arrives on (no
+ * copy or matrix product targets it, so nothing is in flight when it
+ * returns); after `polls` unsuccessful polls it gives up and sets the sticky
+ * error word.  A following ssm_check_device_errors() then returns
+ * SSM_ERR_TIMEOUT (and clears the word); the GPU context stays usable.
+ * polls > 2^20 returns SSM_ERR_SHAPE; a stream of another device than the
+ * current one returns SSM_ERR_CUDA. */
+ssm_status ssm_selftest_wait_timeout(uint32_t polls, cudaStream_t stream);
+
 /* Library version, e.g. "0.1.0". */
 const char* ssm_version(void);
 

@@ -132,6 +132,8 @@ def load() -> ctypes.CDLL:
     lib.ssm_version.argtypes = []
     lib.ssm_check_device_errors.restype = I32
     lib.ssm_check_device_errors.argtypes = []
+    lib.ssm_selftest_wait_timeout.restype = I32
+    lib.ssm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
     _lib = lib
     return lib
 
@@ -170,6 +172,19 @@ def check_device_errors() -> None:
     st = load().ssm_check_device_errors()
     if st != 0:
         raise SsmError(st, "ssm_check_device_errors")
+
+
+def selftest_wait_timeout(polls: int = 1000, stream=None) -> None:
+    """Run the bounded-wait self-test kernel: a wait on an mbarrier nothing
+    arrives on gives up after ``polls`` polls and sets the sticky error word
+    (read it with check_device_errors)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    with torch.cuda.device(stream.device):
+        st = load().ssm_selftest_wait_timeout(int(polls), ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise SsmError(st, "ssm_selftest_wait_timeout")
 
 
 def plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False, mask=False, chunk_len=0,
@@ -311,6 +326,32 @@ def host_workspace_bytes(batch, seqlen, dim, dstate, *, dtype="f32", has_D=True,
                                                     int(chunk_len > 0)))
 
 
+def _check_host_inputs(x, delta, A, B, C, D, z, valid_len):
+    """Dtype, shape, device (CPU) and contiguity of every input of the host
+    entry points: the library reads each as a dense host array of that shape."""
+    import torch
+    cpu = torch.device("cpu")
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"x: dtype {x.dtype}, expected float32 or bfloat16")
+    if x.dim() != 3:
+        raise ValueError(f"x: shape {tuple(x.shape)}, expected [batch, L, dim]")
+    dt = x.dtype
+    batch, L, dim = x.shape
+    if B.dim() != 3:
+        raise ValueError(f"B: shape {tuple(B.shape)}, expected [batch, L, dstate]")
+    dstate = B.shape[-1]
+    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, dim), dt),
+                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
+                                ("A", A, (dim, dstate), torch.float32)):
+        _check(t, name, shape, tdt, cpu)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, cpu)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, cpu)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, cpu)
+
+
 def scan_fwd_host(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: int = 0,
                   out=None, out_states=None, workspace=None, stream=None):
     """End-to-end form on HOST tensors (pinned CPU tensors give async copies).
@@ -322,32 +363,28 @@ def scan_fwd_host(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_le
     stream before reading the outputs."""
     import torch
     lib = load()
+    _check_host_inputs(x, delta, A, B, C, D, z, valid_len)
     dt = x.dtype
     code = _dtype_code(dt)
     batch, L, dim = x.shape
     dstate = B.shape[-1]
-    cpu = torch.device("cpu")
-    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, dim), dt),
-                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
-                                ("A", A, (dim, dstate), torch.float32)):
-        _check(t, name, shape, tdt, cpu)
-    if D is not None:
-        _check(D, "D", (dim,), torch.float32, cpu)
-    if z is not None:
-        _check(z, "z", (batch, L, dim), dt, cpu)
-    if valid_len is not None:
-        _check(valid_len, "valid_len", (batch,), torch.int32, cpu)
     y = torch.empty((batch, L, dim), dtype=dt, pin_memory=True) if out is None else out
+    _check(y, "out", (batch, L, dim), dt, torch.device("cpu"))
     states = None
     if chunk_len > 0:
         nch = (L + chunk_len - 1) // chunk_len
         states = (torch.empty((batch, nch, dim, dstate), dtype=torch.float32, pin_memory=True)
                   if out_states is None else out_states)
+        _check(states, "out_states", (batch, nch, dim, dstate), torch.float32,
+               torch.device("cpu"))
     need = host_workspace_bytes(batch, L, dim, dstate, dtype=dt, has_D=D is not None,
                                 gate=z is not None, mask=valid_len is not None,
                                 chunk_len=chunk_len)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if workspace.device.type != "cuda" or workspace.dtype != torch.uint8 \
+            or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA uint8 tensor")
     if stream is None:
         stream = torch.cuda.current_stream(workspace.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -513,11 +550,14 @@ def static_capacity() -> int:
 def scan_fwd_host_static(x, delta, A, B, C, D=None, z=None, valid_len=None, *, out, chunk_len=0,
                          out_states=None, stream=None):
     """scan_fwd_host without any allocation: the library's fixed device
-    workspace, every step on ``stream``.  ``out`` (and ``out_states`` when
-    chunk_len > 0) are caller-owned host tensors; nothing is allocated here.
-    Calls that overlap in time race on the workspace."""
+    workspace, every step on ``stream`` (default: the current stream of the
+    current device).  ``out`` (and ``out_states`` when chunk_len > 0) are
+    caller-owned host tensors; nothing is allocated here.  The call runs with
+    the stream's device current.  Calls that overlap in time race on the
+    workspace."""
     import torch
     lib = load()
+    _check_host_inputs(x, delta, A, B, C, D, z, valid_len)
     dt = x.dtype
     batch, L, dim = x.shape
     dstate = B.shape[-1]
@@ -525,15 +565,19 @@ def scan_fwd_host_static(x, delta, A, B, C, D=None, z=None, valid_len=None, *, o
     _check(out, "out", (batch, L, dim), dt, cpu)
     if chunk_len > 0:
         nch = (L + chunk_len - 1) // chunk_len
+        if out_states is None:
+            raise ValueError("out_states is required when chunk_len > 0")
         _check(out_states, "out_states", (batch, nch, dim, dstate), torch.float32, cpu)
     if stream is None:
         stream = torch.cuda.current_stream()
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if not hasattr(stream, "device"):
+        raise TypeError("stream must be a torch.cuda.Stream")
     s = _shapes(batch, L, dim, dstate, chunk_len)
-    st = lib.ssm_scan_fwd_host_static(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                      _ptr(z), _ptr(valid_len), _ptr(out), _ptr(out_states),
-                                      ctypes.byref(s), int(_dtype_code(dt)),
-                                      ctypes.c_void_p(handle))
+    with torch.cuda.device(stream.device):
+        st = lib.ssm_scan_fwd_host_static(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                          _ptr(z), _ptr(valid_len), _ptr(out), _ptr(out_states),
+                                          ctypes.byref(s), int(_dtype_code(dt)),
+                                          ctypes.c_void_p(stream.cuda_stream))
     if st != 0:
         raise SsmError(st, "ssm_scan_fwd_host_static")
     return out, out_states

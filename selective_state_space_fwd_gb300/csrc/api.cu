@@ -18,6 +18,7 @@ namespace {
 using ssm::ScanParams;
 
 constexpr int64_t kBwdMaxChunk = 512;  // longest chunk the backward replays in shared memory
+constexpr uint32_t kSelftestMaxPolls = 1u << 20;  // bound of ssm_selftest_wait_timeout
 
 bool supported_dstate(int64_t n) {
   return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
@@ -144,12 +145,28 @@ ssm_status apply_prep(const ssm_delta_prep* prep, P* p) {
   return SSM_OK;
 }
 
+// The entry points keep per-device state (the sticky error word of the
+// bounded waits, copy streams, the address of the fixed workspace) and look it
+// up by the calling thread's current device; `stream` must belong to that
+// device, else SSM_ERR_CUDA.  The special handles (0, legacy, per-thread)
+// always do.
+ssm_status current_device_for(cudaStream_t stream, int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return SSM_ERR_CUDA;
+  if (stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread)
+    return SSM_OK;
+  int sdev = -1;
+  if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return SSM_ERR_CUDA;
+  return sdev == *dev ? SSM_OK : SSM_ERR_CUDA;
+}
+
 // Launch the planned tier.
 ssm_status launch(const ScanParams& p, ssm_dtype dtype, const ssm_options* opts,
                   cudaStream_t stream) {
   Plan plan;
   ssm_status st = make_plan(p, dtype, opts, &plan);
   if (st != SSM_OK) return st;
+  int dev = 0;
+  if ((st = current_device_for(stream, &dev)) != SSM_OK) return st;
   const bool bf16 = dtype == SSM_BF16;
   cudaError_t err = cudaErrorInvalidValue;
   switch (plan.kernel) {
@@ -163,32 +180,53 @@ ssm_status launch(const ScanParams& p, ssm_dtype dtype, const ssm_options* opts,
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Byte layout of the device workspace used by ssm_scan_fwd_host.
+// Byte layout of the device workspace used by ssm_scan_fwd_host.  `total` is
+// SIZE_MAX when a region size or the running sum would not fit in size_t.
 struct HostLayout {
   size_t x, delta, z, B, C, A, D, valid, y, states, carry, total;
 };
 
+constexpr size_t kNoFit = SIZE_MAX;
+
+// a * b, or kNoFit when it does not fit.
+size_t mul_size(size_t a, size_t b) {
+  if (a != 0 && b > (kNoFit - 1) / a) return kNoFit;
+  return a * b;
+}
+
 HostLayout host_layout(const ssm_shapes* s, ssm_dtype dtype, int has_D, int has_z, int has_valid,
                        int has_states) {
   const size_t es = elem_size(dtype);
-  const size_t act = size_t(s->batch) * s->seqlen * s->dim * es;
-  const size_t bc = size_t(s->batch) * s->seqlen * s->dstate * es;
+  const size_t bl = mul_size(size_t(s->batch), size_t(s->seqlen));
+  const size_t act = mul_size(mul_size(bl, size_t(s->dim)), es);
+  const size_t bc = mul_size(mul_size(bl, size_t(s->dstate)), es);
+  const size_t dn4 = mul_size(mul_size(size_t(s->dim), size_t(s->dstate)), 4);
   const size_t nch = s->chunk_len > 0 ? size_t((s->seqlen + s->chunk_len - 1) / s->chunk_len) : 0;
   HostLayout l;
   size_t off = 0;
-  auto take = [&](size_t bytes) { size_t o = off; off = round_up(off + bytes, 256); return o; };
+  bool fits = true;
+  // region of `bytes` at the current offset; the next starts 256-byte aligned
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    if (bytes > kNoFit - 256 || off > kNoFit - 256 - bytes) {
+      fits = false;
+      return size_t(0);
+    }
+    off = round_up(off + bytes, 256);
+    return o;
+  };
   l.x = take(act);
   l.delta = take(act);
   l.z = has_z ? take(act) : 0;
   l.B = take(bc);
   l.C = take(bc);
-  l.A = take(size_t(s->dim) * s->dstate * 4);
-  l.D = has_D ? take(size_t(s->dim) * 4) : 0;
-  l.valid = has_valid ? take(size_t(s->batch) * 4) : 0;
+  l.A = take(dn4);
+  l.D = has_D ? take(mul_size(size_t(s->dim), 4)) : 0;
+  l.valid = has_valid ? take(mul_size(size_t(s->batch), 4)) : 0;
   l.y = take(act);
-  l.states = has_states ? take(size_t(s->batch) * nch * s->dim * s->dstate * 4) : 0;
-  l.carry = take(2 * size_t(s->batch) * s->dim * s->dstate * 4);
-  l.total = off;
+  l.states = has_states ? take(mul_size(mul_size(size_t(s->batch), nch), dn4)) : 0;
+  l.carry = take(mul_size(2 * size_t(s->batch), dn4));
+  l.total = fits ? off : kNoFit;
   return l;
 }
 
@@ -259,7 +297,8 @@ ssm_status run_host_pipeline(const void* x, const void* delta, const float* A, c
                              const ssm_shapes& s, ssm_dtype dtype, char* ws, const HostLayout& l,
                              cudaStream_t stream) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  const ssm_status ds = current_device_for(stream, &dev);
+  if (ds != SSM_OK) return ds;
   HostStreams* hs = host_streams(dev);
   if (hs == nullptr) return SSM_ERR_CUDA;
   std::lock_guard<std::mutex> lk(hs->mu);
@@ -346,6 +385,14 @@ extern "C" {
 
 const char* ssm_version(void) { return "0.1.0"; }
 
+ssm_status ssm_selftest_wait_timeout(uint32_t polls, cudaStream_t stream) {
+  if (polls > kSelftestMaxPolls) return SSM_ERR_SHAPE;
+  int dev = 0;
+  const ssm_status st = current_device_for(stream, &dev);
+  if (st != SSM_OK) return st;
+  return ssm::launch_wait_timeout_selftest(polls, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 ssm_status ssm_check_device_errors(void) {
   unsigned int word = 0;
   if (!ssm::read_and_clear_device_errors(&word)) return SSM_ERR_CUDA;
@@ -404,6 +451,9 @@ ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const v
   p.valid_len = valid_len; p.h0 = h0; p.y = out_y; p.h_final = out_final_state;
   p.batch = s.batch; p.seqlen = s.seqlen; p.nheads = s.nheads; p.headdim = s.headdim;
   p.dstate = s.dstate;
+  int dev = 0;
+  const ssm_status ds = current_device_for(stream, &dev);
+  if (ds != SSM_OK) return ds;
   p.err = ssm::stream::error_word();
   if (!p.err) return SSM_ERR_CUDA;
   return ssm::launch_ssd(p, stream) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
@@ -488,7 +538,8 @@ ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A, const 
 size_t ssm_scan_host_workspace_bytes(const ssm_shapes* shapes, ssm_dtype dtype, int has_D,
                                      int has_z, int has_valid_len, int has_states) {
   if (check_shapes(shapes, dtype, has_states != 0) != SSM_OK) return 0;
-  return host_layout(shapes, dtype, has_D, has_z, has_valid_len, has_states).total;
+  const size_t total = host_layout(shapes, dtype, has_D, has_z, has_valid_len, has_states).total;
+  return total == kNoFit ? 0 : total;
 }
 
 ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, const void* B,
@@ -503,7 +554,7 @@ ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A, c
   if (!aligned(workspace, 256)) return SSM_ERR_ALIGN;
   const HostLayout l = host_layout(shapes, dtype, D != nullptr, z != nullptr,
                                    valid_len != nullptr, want_states);
-  if (workspace_bytes < l.total) return SSM_ERR_SHAPE;
+  if (l.total == kNoFit || workspace_bytes < l.total) return SSM_ERR_SHAPE;
   return run_host_pipeline(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states, *shapes,
                            dtype, static_cast<char*>(workspace), l, stream);
 }
@@ -627,9 +678,10 @@ ssm_status ssm_scan_fwd_host_static(const void* x, const void* delta, const floa
   if (!x || !delta || !A || !B || !C || !out_y) return SSM_ERR_NULL;
   const HostLayout l = host_layout(shapes, dtype, D != nullptr, z != nullptr,
                                    valid_len != nullptr, want_states);
-  if (l.total > kStaticWsBytes) return SSM_ERR_SHAPE;  // larger than the fixed workspace
+  if (l.total == kNoFit || l.total > kStaticWsBytes)
+    return SSM_ERR_SHAPE;  // larger than the fixed workspace
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  if ((st = current_device_for(stream, &dev)) != SSM_OK) return st;
   char* ws = static_ws(dev);
   if (ws == nullptr) return SSM_ERR_CUDA;
 

@@ -11,7 +11,8 @@ EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_f
             "ssm_decode_step", "ssm_decode_step_prep", "ssm_scan_bwd", "ssm_scan_plan",
             "ssm_scan_fwd_host_static", "ssm_scan_host_static_capacity", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
-            "ssm_kernel_name", "ssm_version", "ssm_check_device_errors", "ssm_ssd_fwd"}
+            "ssm_kernel_name", "ssm_version", "ssm_check_device_errors", "ssm_ssd_fwd",
+            "ssm_selftest_wait_timeout"}
 
 
 def test_every_declared_symbol_is_exported(ssmlib):
@@ -246,3 +247,56 @@ def test_no_fallback_without_the_library(monkeypatch, tmp_path):
         Bd.scan_fwd(x, x, torch.zeros(2, 4), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4))
     with pytest.raises(ImportError):
         Bd.ssd_fwd(x, x, torch.zeros(1), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4), nheads=1)
+
+
+def test_host_workspace_bytes_overflow_is_refused(ssmlib):
+    """A workspace whose size would wrap size_t is reported as 0 (and refused by
+    both host entry points) rather than as a small wrapped total."""
+    # every element count is below 2^60, but six regions of them do not fit in 64 bits
+    dim = (1 << 20) - 1  # x, delta, z, y: four regions of almost 2^62 bytes each
+    assert Bd.host_workspace_bytes(1 << 20, 1 << 20, dim, 16, dtype="f32", gate=True) == 0
+    lib = Bd.load()
+    s = Bd.Shapes(1 << 20, 1 << 20, dim, 16, 0)
+    P = ctypes.c_void_p
+    st = lib.ssm_scan_fwd_host_static(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None,
+                                      P(FAKE), None, P(FAKE), None, ctypes.byref(s), 0, None)
+    assert st == Bd.Status.ERR_SHAPE
+    st = lib.ssm_scan_fwd_host(P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, P(FAKE), None,
+                               P(FAKE), None, ctypes.byref(s), 0, P(0x100000), 1 << 62, None)
+    assert st == Bd.Status.ERR_SHAPE
+
+
+def _host_args(**over):
+    import torch
+    a = dict(x=torch.zeros(2, 8, 4), delta=torch.zeros(2, 8, 4), A=torch.zeros(4, 16),
+             B=torch.zeros(2, 8, 16), C=torch.zeros(2, 8, 16), D=torch.zeros(4),
+             z=None, valid_len=None)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("entry", ["scan_fwd_host", "scan_fwd_host_static"])
+@pytest.mark.parametrize("over,exc", [
+    (lambda t: dict(A=t.zeros(4, 16, dtype=t.float64)), TypeError),
+    (lambda t: dict(x=t.zeros(2, 4, 8).transpose(1, 2)), ValueError),
+    (lambda t: dict(delta=t.zeros(2, 8, 4, dtype=t.bfloat16)), TypeError),
+    (lambda t: dict(valid_len=t.zeros(2, dtype=t.int64)), TypeError),
+    (lambda t: dict(D=t.zeros(5)), ValueError),
+    (lambda t: dict(B=t.zeros(2, 8, 16)[:, :, :8]), ValueError),
+    (lambda t: dict(x=t.zeros(2, 8, 4, dtype=t.float64)), TypeError),
+])
+def test_host_entries_check_every_input(ssmlib, entry, over, exc):
+    """Both host entry points refuse a wrong dtype, shape or layout of any input
+    before the library reads the host buffers (no GPU is touched)."""
+    import torch
+    a = _host_args(**over(torch))
+    fn = getattr(Bd, entry)
+    kw = {"out": torch.zeros(2, 8, 4)} if entry == "scan_fwd_host_static" else {}
+    with pytest.raises(exc):
+        fn(a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["valid_len"], **kw)
+
+
+def test_selftest_poll_bound(ssmlib):
+    """The bounded-wait self-test refuses a poll count above its bound before
+    launching anything."""
+    assert Bd.load().ssm_selftest_wait_timeout((1 << 20) + 1, None) == Bd.Status.ERR_SHAPE

@@ -1,10 +1,11 @@
 """The allocation-free end-to-end entry point (``ssm_scan_fwd_host_static``).
 
-It must give the result of ``ssm_scan_fwd_host`` (the same pieces chained by
-the carried state, the same kernels) on two calls in a row, within the
-parity tolerances, without allocating device memory; and refuse problems
-larger than its fixed workspace.  The file is collected last, and passes
-alone in a fresh process as well as after the other tests.
+It runs the same pieces, chained by the carried state, with the same kernels
+as ``ssm_scan_fwd_host``, so on two calls in a row its outputs must equal that
+entry point's bit for bit, and agree with the fp64 oracle within the parity
+tolerances; it must not allocate device memory, and must refuse problems
+larger than its fixed workspace.  The file is collected last, and passes alone
+in a fresh process as well as after the other tests.
 """
 import numpy as np
 import pytest
@@ -16,6 +17,7 @@ from selective_state_space_fwd_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 TOL = {"f32": 1e-5, "bf16": 1e-2}
+TOL_STATES = 1e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -24,32 +26,69 @@ def _built(ssmlib):
     yield
 
 
-def _rel(a, b):
-    a, b = a.float().numpy().astype(np.float64), b.float().numpy().astype(np.float64)
-    den = np.max(np.abs(b))
-    return float(np.max(np.abs(a - b)) / den) if den > 0 else float(np.max(np.abs(a)))
+def _f64(t):
+    return t.float().numpy().astype(np.float64)
+
+
+def _rel(a, ref):
+    den = np.max(np.abs(ref))
+    return float(np.max(np.abs(a - ref)) / den) if den > 0 else float(np.max(np.abs(a)))
+
+
+def _largest_seqlen_under_capacity(w):
+    """The longest sequence whose workspace still fits the fixed array (the
+    last 256-byte-aligned region then ends just below its end)."""
+    cap = S.static_capacity()
+
+    def need(L):
+        return S.host_workspace_bytes(w.batch, L, w.dim, w.dstate, dtype=w.dtype, has_D=True,
+                                      gate=w.gate, mask=w.mask is not None,
+                                      chunk_len=w.chunk_len)
+    lo, hi = 1, 1 << 22
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if need(mid) <= cap:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
+def _near_capacity():
+    w = W.WORKLOADS[2].scaled(batch=2, seqlen=64, dim=512)
+    return w.scaled(seqlen=_largest_seqlen_under_capacity(w))
 
 
 CASES = {
-    "fp32-long-pieces": W.WORKLOADS[2].scaled(batch=2, seqlen=3000, dim=64),
-    "bf16-gate-mask-states": W.WORKLOADS[4].scaled(batch=4, seqlen=700, dim=48),
+    "fp32-long-pieces": (W.WORKLOADS[2].scaled(batch=2, seqlen=3000, dim=64), True),
+    "fp32-no-D": (W.WORKLOADS[2].scaled(batch=3, seqlen=1500, dim=32), False),
+    "bf16-gate-mask-states": (W.WORKLOADS[4].scaled(batch=4, seqlen=700, dim=48), True),
+    "fp32-workspace-at-capacity": (None, True),
 }
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_matches_the_workspace_entry_on_two_calls(name):
-    w = CASES[name]
+def test_matches_the_workspace_entry_and_the_oracle_on_two_calls(oracle, name):
+    w, with_D = CASES[name]
+    if w is None:
+        w = _near_capacity()
     inp = W.make_inputs(w)
+    if not with_D:
+        inp["D"] = None
     if inp["valid_len"] is not None:
         inp["valid_len"] = np.array([700, 0, 333, 1], np.int32)
     t = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v)
          for k, v in W.to_torch(inp, "cpu").items()}
     cl = w.chunk_len
-    assert S.host_workspace_bytes(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
-                                  mask=w.mask is not None, chunk_len=cl) <= S.static_capacity()
+    need = S.host_workspace_bytes(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
+                                  has_D=with_D, gate=w.gate, mask=w.mask is not None,
+                                  chunk_len=cl)
+    assert need <= S.static_capacity()
     y_ref, s_ref = S.scan_fwd_host(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                                    t["valid_len"], chunk_len=cl)
     torch.cuda.synchronize()
+    yo, so = oracle.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                             inp["z"], inp["valid_len"], chunk_len=cl)
     nch = (w.seqlen + cl - 1) // cl if cl else 0
     y = torch.empty_like(y_ref).pin_memory()
     st = torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32).pin_memory() if cl else None
@@ -58,15 +97,20 @@ def test_matches_the_workspace_entry_on_two_calls(name):
     torch.cuda.synchronize()  # the first call has done its set-up
     free0, _ = torch.cuda.mem_get_info()
     for _ in range(2):
-        y.zero_()
+        y.fill_(float("nan"))
         if st is not None:
-            st.zero_()
+            st.fill_(float("nan"))
         S.scan_fwd_host_static(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                                t["valid_len"], out=y, chunk_len=cl, out_states=st)
         torch.cuda.synchronize()
-        assert _rel(y, y_ref) <= TOL[w.dtype]
+        assert torch.equal(y, y_ref), "differs from ssm_scan_fwd_host"
+        assert _rel(_f64(y), yo) <= TOL[w.dtype]
         if st is not None:
-            assert _rel(st, s_ref) <= 1e-5
+            assert torch.equal(st, s_ref), "chunk states differ from ssm_scan_fwd_host"
+            assert _rel(_f64(st), so) <= TOL_STATES
+        if inp["valid_len"] is not None:
+            for b, v in enumerate(inp["valid_len"]):
+                assert torch.all(y[b, int(v):] == 0)
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0, "the call allocated device memory"
 
