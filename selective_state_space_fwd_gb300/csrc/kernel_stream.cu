@@ -30,6 +30,18 @@ unsigned int* error_word() {
   return addr[dev];
 }
 
+// Self-test of the bounded-wait error path.  One thread waits, with the same
+// bounded wait as the kernels, on an mbarrier that nothing arrives on (no
+// copy, no matrix product and no other thread targets it, so nothing is in
+// flight when the kernel returns); after `polls` polls it gives up and sets
+// the sticky error word exactly as a kernel whose copy never landed would.
+__global__ void wait_timeout_selftest_kernel(unsigned polls, unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!mbar_wait(&bar, 0, polls)) atomicOr(err, kErrWait);
+}
+
 // Dynamic shared memory a STREAM CTA may use (the opt-in limit of sm_103).
 int max_dynamic_smem() { return 227 * 1024; }
 
@@ -192,6 +204,13 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
   sh.r = r;
   sh.stages = stages;
   return sh;
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned polls, cudaStream_t s) {
+  unsigned int* err = stream::error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  stream::wait_timeout_selftest_kernel<<<1, 1, 0, s>>>(polls, err);
+  return cudaGetLastError();
 }
 
 bool read_and_clear_device_errors(unsigned int* word) {

@@ -39,6 +39,10 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s);
 size_t bwd_smem_bytes(int64_t chunk_len, int dstate);
 
+// One thread runs a bounded wait on an mbarrier nothing arrives on, gives up
+// after `polls` polls and sets the sticky error word (test of the error path).
+cudaError_t launch_wait_timeout_selftest(unsigned polls, cudaStream_t s);
+
 // Sticky device error word of the tiers with bounded waits: read and clear.
 bool read_and_clear_device_errors(unsigned int* word);
 
