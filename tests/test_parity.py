@@ -170,16 +170,63 @@ def test_edge_cases(oracle, name, kernel):
     check(inp, y, s, y_ref, s_ref)
 
 
+def _poison_padding(inp):
+    """Write NaN, +Inf and -Inf into every padded position (steps at or past
+    valid_len) of x, delta, z, B and C.  Padded steps are the identity (1, 0)
+    ([P1] s2.3, s5.3): nothing there may reach y or the state."""
+    L = inp["x"].shape[1]
+    for k in ("x", "delta", "z", "B", "C"):
+        a = inp[k]
+        if a is None:
+            continue
+        a = a.copy()
+        for b, v in enumerate(inp["valid_len"]):
+            v = min(max(int(v), 0), L)
+            if v == L:
+                continue
+            n = a[b, v:].size
+            if a.dtype == np.uint16:  # bf16 bit patterns: NaN, +Inf, -Inf
+                pat = np.array([0x7FC0, 0x7F80, 0xFF80], np.uint16)
+            else:
+                pat = np.array([np.nan, np.inf, -np.inf], a.dtype)
+            a[b, v:] = np.resize(pat, n).reshape(a[b, v:].shape)
+        inp[k] = a
+    return inp
+
+
+@pytest.mark.parametrize("kernel", TIERS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_nonfinite_padding_is_ignored(oracle, kernel, dtype):
+    """Masked steps are a real identity: NaN and Inf in the padding of every
+    input leave y exactly 0 there, the chunk states frozen and every valid
+    output unchanged."""
+    inp = _edge(batch=5, L=300, dim=48, N=16, dtype=dtype, gate=True,
+                mask=[0, 1, 64, 150, 299], chunk=64, seed=11)
+    clean = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in inp.items()}
+    inp = _poison_padding(inp)
+    if not tier_supported(inp, kernel):
+        pytest.skip(f"{kernel} does not take this shape")
+    y_ref, s_ref = run_oracle(oracle, clean)
+    y, s = run_gpu(inp, kernel)
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(s))
+    check(inp, y, s, y_ref, s_ref)
+
+
 def test_error_grows_slowly_with_length(oracle):
     """[P1] s4.4: the error against the reference stays at fp32 level as L grows
-    from 256 to 8192 (fp32 accumulation of the prefix)."""
+    from 256 to 8192.  Every decay is below 1, so the state forgets old
+    rounding errors: the error must not grow with L the way a plain running sum
+    would (linearly, 32x over this range), only stay at the fp32 level."""
     errs = []
     for L in (256, 1024, 4096, 8192):
         inp = _edge(batch=1, L=L, dim=64, N=16, seed=40)
         y_ref, _ = run_oracle(oracle, inp)
         y, _ = run_gpu(inp)
         errs.append(check(inp, y, None, y_ref, None))
-    assert errs[-1] <= 1e-5
+    floor = 2.0 ** -23  # one fp32 rounding
+    for e_short, e_long in zip(errs, errs[1:]):
+        assert e_long <= 4 * max(e_short, 8 * floor), errs
+    assert errs[-1] <= 8 * max(errs[0], 8 * floor), errs
 
 
 def test_deterministic_bitwise():
@@ -193,12 +240,18 @@ def test_deterministic_bitwise():
 
 
 def test_tiers_agree_closely(oracle):
-    """All tiers compute the same function; they may round differently."""
-    inp = small_inputs("w3-bf16-gate-states")
-    outs = {k: run_gpu(inp, k) for k in TIERS if tier_supported(inp, k)}
-    ref = outs["serial"]
-    for k, (y, s) in outs.items():
-        assert rel_err(s, ref[1]) <= 2 * TOL_STATES, k
+    """All tiers compute the same function; they may round differently.  fp32:
+    y and the chunk states agree to a few fp32 roundings; bf16: the fp32
+    results agree as closely, so the stored y differ by at most one bf16 ulp
+    (2^-7 relative to the largest element)."""
+    for name, tol_y in (("w2-fp32", 2e-6), ("w3-bf16-gate-states", 2.0 ** -7)):
+        inp = small_inputs(name)
+        outs = {k: run_gpu(inp, k) for k in TIERS if tier_supported(inp, k)}
+        ref = outs["serial"]
+        for k, (y, s) in outs.items():
+            assert rel_err(y, ref[0]) <= tol_y, (name, k)
+            if s is not None:
+                assert rel_err(s, ref[1]) <= 2 * TOL_STATES, (name, k)
 
 
 def test_host_entry_point_matches_device(oracle):
@@ -250,38 +303,26 @@ def test_stream_argument_is_respected():
 
 
 # Full-size workloads, in the launch configuration the benchmark times (AUTO),
-# checked on sampled channels: the oracle recomputes those channels one by one.
-def _sample_channels(w, k=12, seed=0):
-    rng = np.random.default_rng(seed)
-    pts = {(0, 0), (w.batch - 1, w.dim - 1), (0, w.dim - 1), (w.batch - 1, 0)}
-    while len(pts) < k:
-        pts.add((int(rng.integers(w.batch)), int(rng.integers(w.dim))))
-    return sorted(pts)
-
-
+# compared with the oracle on the whole of y and of the chunk states (the
+# oracle runs every channel, one OpenMP thread per channel).
 @pytest.mark.parametrize("key", [1, 2, 3, 4, 5])
-def test_full_size_sampled(oracle, key):
+def test_full_size_whole_tensor(oracle, key):
     w = W.WORKLOADS[key]
     inp = W.make_inputs(w)
     t = W.to_torch(inp, "cuda")
     y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                       t["valid_len"], chunk_len=w.chunk_len)
     torch.cuda.synchronize()
+    S.check_device_errors()
     del t
-    ys, yr, ss, sr = [], [], [], []
-    for b, d in _sample_channels(w):
-        ci = W.channel_slice(inp, b, d)
-        y_ref, s_ref = run_oracle(oracle, ci, threads=1)
-        ys.append(to_f64(y[b, :, d]))
-        yr.append(y_ref[0, :, 0])
-        if s is not None:
-            ss.append(to_f64(s[b, :, d]))
-            sr.append(s_ref[0, :, 0])
-        if inp["valid_len"] is not None:
-            v = int(inp["valid_len"][b])
-            assert torch.all(y[b, v:, d] == 0)
-    e = rel_err(np.concatenate(ys), np.concatenate(yr))
-    assert e <= TOL_Y[w.dtype], f"workload {key}: sampled y rel err {e:.3e}"
-    if ss:
-        es = rel_err(np.concatenate(ss), np.concatenate(sr))
-        assert es <= TOL_STATES, f"workload {key}: sampled state rel err {es:.3e}"
+    y_ref, s_ref = run_oracle(oracle, inp)
+    yg = to_f64(y)
+    del y
+    e = rel_err(yg, y_ref)
+    assert e <= TOL_Y[w.dtype], f"workload {key}: y rel err {e:.3e}"
+    if inp["valid_len"] is not None:
+        for b, v in enumerate(inp["valid_len"]):
+            assert np.all(yg[b, int(v):] == 0), f"workload {key}: row {b} past valid_len"
+    if s is not None:
+        es = rel_err(to_f64(s), s_ref)
+        assert es <= TOL_STATES, f"workload {key}: state rel err {es:.3e}"

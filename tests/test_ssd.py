@@ -136,28 +136,23 @@ def test_ssd_n256_split_equals_whole(oracle):
     assert torch.equal(y2, y[:, k:]) and torch.equal(f2, fin)
 
 
-def test_ssd_full_size_sampled(oracle):
-    """The benchmark's workload at full size, in the launch configuration the
-    benchmark times; the oracle checks sampled (batch row, head) pairs, every
-    channel of the head over the whole sequence."""
-    w = BASE
+@pytest.mark.parametrize("key", sorted(W.SSD_WORKLOADS))
+def test_ssd_full_size_whole_tensor(oracle, key):
+    """The benchmark's workloads (128 and 256 states) at full size, in the
+    launch configuration the benchmark times; the oracle computes every
+    (batch row, head) and the whole of y is compared."""
+    w = W.SSD_WORKLOADS[key]
     inp = W.make_ssd_inputs(w)
     t = W.to_torch(inp, "cuda")
     y = S.ssd_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], None,
                   nheads=w.nheads)
     torch.cuda.synchronize()
     S.check_device_errors()
-    P = w.headdim
-    for b, h in ((0, 0), (3, 17), (7, w.nheads - 1)):
-        ch = slice(h * P, (h + 1) * P)
-        sub = dict(x=inp["x"][b:b + 1, :, ch], delta=inp["delta"][b:b + 1, :, h:h + 1],
-                   A=inp["A"][h:h + 1], B=inp["B"][b:b + 1], C=inp["C"][b:b + 1],
-                   D=inp["D"][ch], z=inp["z"][b:b + 1, :, ch])
-        y_ref = oracle.ssd_fwd(*(np.ascontiguousarray(sub[k]) for k in
-                                 ("x", "delta", "A", "B", "C", "D", "z")), nheads=1)
-        yg = y[b:b + 1, :, ch].float().cpu().numpy().astype(np.float64)
-        e = rel(yg, y_ref)
-        assert e <= TOL_Y, f"(b={b}, h={h}) y rel err {e:.3e}"
+    del t
+    y_ref = oracle.ssd_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                           inp["z"], nheads=w.nheads)
+    e = rel(y.float().cpu().numpy().astype(np.float64), y_ref)
+    assert e <= TOL_Y, f"y rel err {e:.3e}"
 
 
 def _halves(t, key):
