@@ -27,10 +27,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "selective-scan fwd B·L·D elems/s and achieved % of roofline, 1×GB300"
 UNIT = "elements/s"
-# Per-SM unit rates of GB300 (sm_103a) used for the ALU roof: MUFU ex2 is 32
-# lanes/clk/SM (measured with a throughput probe), FP32 is 128 lanes/clk/SM.
-MUFU_PER_SM_CLK = 32
-FP32_PER_SM_CLK = 128
+# Nominal per-SM unit rates of GB300 (sm_103a): MUFU ex2 32 lanes/clk/SM, fp32
+# FMA 128 lanes/clk/SM.  Used only when the probe kernels cannot run; the
+# roofline normally takes the rates measured on the GPU by unit_rates().
+NOMINAL_RATES = {"ex2_per_clk_sm": 32.0, "fp32_per_clk_sm": 128.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}
 
 
@@ -91,13 +91,67 @@ def algorithmic_counts(w, inp) -> dict:
                 fp32_ops=fp32, bytes=bytes_)
 
 
-def roof(counts, peaks, sms, sm_mhz) -> dict:
+def unit_rates() -> tuple[dict, str]:
+    """MUFU ex2 results and fp32 FMA lane-operations per SM clock, measured on
+    the current GPU by the throughput probes of libssmprobe.so
+    (selective_state_space_fwd_gb300/probe/unit_rates.cu); the nominal rates
+    when the probes cannot run."""
+    import ctypes
+    try:
+        from selective_state_space_fwd_gb300 import build as B
+        lib = ctypes.CDLL(B.build_probe())
+        e, f, f2 = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        n = ctypes.c_int()
+        rc = lib.ssmprobe_unit_rates(ctypes.byref(e), ctypes.byref(f), ctypes.byref(f2),
+                                     ctypes.byref(n))
+        if rc != 0 or not (e.value > 0 and f.value > 0 and f2.value > 0):
+            raise RuntimeError(f"probe status {rc}")
+    except Exception as ex:  # no GPU, no compiler: the nominal figures, said so
+        return dict(NOMINAL_RATES, error=str(ex)[:80]), "nominal"
+    return {"ex2_per_clk_sm": e.value, "fp32_per_clk_sm": max(f.value, f2.value),
+            "ffma_per_clk_sm": f.value, "ffma2_lanes_per_clk_sm": f2.value}, "measured"
+
+
+def roof(counts, peaks, sms, sm_mhz, rates=NOMINAL_RATES) -> dict:
     hbm = peaks["hbm_gbs"] * 1e9
     clk = sm_mhz * 1e6
     t_hbm = counts["bytes"] / hbm
-    t_mufu = counts["exps"] / (MUFU_PER_SM_CLK * sms * clk)
-    t_fp32 = counts["fp32_ops"] / (FP32_PER_SM_CLK * sms * clk)
+    t_mufu = counts["exps"] / (rates["ex2_per_clk_sm"] * sms * clk)
+    t_fp32 = counts["fp32_ops"] / (rates["fp32_per_clk_sm"] * sms * clk)
     return dict(t_hbm=t_hbm, t_mufu=t_mufu, t_fp32=t_fp32, t_roof=max(t_hbm, t_mufu, t_fp32))
+
+
+def _rates_text(rates) -> str:
+    return (f"{rates['ex2_per_clk_sm']:.1f} ex2 and {rates['fp32_per_clk_sm']:.1f} fp32 "
+            f"lanes/clk/SM")
+
+
+def roofline(counts, t_meas, peaks, rates, sms, sm_mhz) -> dict:
+    """The roofline against whichever term binds (the largest of HBM bytes at
+    the measured copy bandwidth, exps at the MUFU rate, fp32 operations at the
+    fp32 rate): achieved rate of that term, its peak, and their ratio, which
+    equals roof time / measured time."""
+    r = roof(counts, peaks, sms, sm_mhz, rates)
+    clk = sm_mhz * 1e6
+    terms = {"hbm": r["t_hbm"], "mufu": r["t_mufu"], "fp32": r["t_fp32"]}
+    bound = max(terms, key=terms.get)
+    if bound == "hbm":
+        out = {"bound": "hbm", "achieved": counts["bytes"] / t_meas / 1e9,
+               "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    elif bound == "mufu":
+        out = {"bound": "alu", "alu_unit": "MUFU ex2", "achieved": counts["exps"] / t_meas / 1e9,
+               "peak": rates["ex2_per_clk_sm"] * sms * clk / 1e9, "unit": "Gex2/s"}
+    else:
+        out = {"bound": "alu", "alu_unit": "fp32 FMA pipe",
+               "achieved": counts["fp32_ops"] / t_meas / 1e9,
+               "peak": rates["fp32_per_clk_sm"] * sms * clk / 1e9, "unit": "Gop/s fp32"}
+    out["frac"] = out["achieved"] / out["peak"]
+    out.update({"roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
+                            "fp32": r["t_fp32"] * 1e6},
+                "frac_of_roof": r["t_roof"] / t_meas,
+                "algorithmic": {"bytes": counts["bytes"], "exps": counts["exps"],
+                                "fp32_ops": counts["fp32_ops"]}})
+    return out
 
 
 class ClockSampler:
@@ -198,6 +252,11 @@ def parse():
                          "backward, replaying from chunk states (--bwd-chunk); ssd: the "
                          "SSD form (one decay per head) on the tensor cores")
     ap.add_argument("--bwd-chunk", type=int, default=256)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload, not the other full-size forwards")
+    ap.add_argument("--split-batch", action="store_true",
+                    help="under torchrun: split one workload's batch rows across the ranks "
+                         "(strong scaling) instead of one replica per rank")
     ap.add_argument("--ssd-workload", type=int, default=1,
                     help="with --op ssd: 1 = 128 states, 2 = 256 states")
     return ap.parse_args()
@@ -235,6 +294,78 @@ def shard_rows(batch: int, rank: int, world: int) -> tuple[int, int]:
     per, extra = divmod(batch, world)
     lo = rank * per + min(rank, extra)
     return lo, lo + per + (1 if rank < extra else 0)
+
+
+def slice_rows(inp: dict, lo: int, hi: int) -> dict:
+    """Batch rows [lo, hi) of a make_inputs() dict (pure indexing: x, delta, z,
+    B, C and valid_len have the batch as their first axis)."""
+    out = dict(inp)
+    for k in ("x", "delta", "z", "B", "C", "valid_len"):
+        if inp.get(k) is not None:
+            out[k] = np.ascontiguousarray(inp[k][lo:hi])
+    return out
+
+
+def args_kernel(args, S, w):
+    """The tier the library launches for this workload and the forced options."""
+    k, _ = S.plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
+                  mask=w.mask is not None, chunk_len=w.chunk_len, kernel=args.kernel,
+                  warps_per_block=args.warps_per_block, states_per_lane=args.states_per_lane,
+                  channels_per_lane=args.channels_per_lane)
+    return k
+
+
+def time_forward(args, S, w, inp, prep, dev, stream, flush, K, warmup, clocks_index=0,
+                 barrier=None) -> dict:
+    """K timed forwards of workload w on device-resident inputs: CUDA events on
+    the launch stream around each call, L2 flushed between calls (outside the
+    events), SM clocks sampled during the timed region, which `barrier` (all
+    ranks) and a device synchronise bracket on both sides."""
+    import torch
+    from selective_state_space_fwd_gb300 import workloads as W
+    t = W.to_torch(inp, dev)
+    y = torch.empty_like(t["x"])
+    nch = (w.seqlen + w.chunk_len - 1) // w.chunk_len if w.chunk_len else 0
+    states = (torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+              if w.chunk_len else None)
+
+    def step():
+        S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
+                   chunk_len=w.chunk_len, out=y, out_states=states, kernel=args.kernel,
+                   warps_per_block=args.warps_per_block,
+                   states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane,
+                   stream=stream, **prep)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            step()
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(clocks_index)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            if not args.no_flush:
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if barrier is not None:
+        barrier()
+    S.check_device_errors()
+    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms, one launch each
+    return {"ms": sum(per_step) / K, "t": t, "clocks": clk, "wall": wall, "launches": K,
+            "per_step": {"min": min(per_step), "median": statistics.median(per_step),
+                         "max": max(per_step)}}
 
 
 def reference_arm(args, w):
@@ -558,24 +689,11 @@ def bwd_main(args):
     peaks, peaks_src = load_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    r = roof(c, peaks, sms, mhz)
-    t_meas = ms * 1e-3
-    pk = MUFU_PER_SM_CLK * sms * mhz * 1e6 / 1e9
-    if r["t_hbm"] >= max(r["t_mufu"], r["t_fp32"]):
-        achieved = c["bytes"] / t_meas / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"]}
-    else:
-        achieved = r["t_roof"] / t_meas
-        roofline = {"bound": "alu", "achieved": c["fp32_ops"] / t_meas / 1e12,
-                    "peak": FP32_PER_SM_CLK * sms * mhz * 1e6 / 1e12, "unit": "TFLOP/s fp32",
-                    "frac": r["t_roof"] / t_meas}
-    roofline.update({"traffic": measured_traffic("bwd", w.name), "kernel": "bwd",
-                     "peak_source": peaks_src,
-                     "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
-                                 "fp32": r["t_fp32"] * 1e6},
-                     "algorithmic": {"bytes": c["bytes"], "exps": c["exps"],
-                                     "fp32_ops": c["fp32_ops"]}})
+    rates, rates_src = unit_rates()
+    roofline_ = roofline(c, ms * 1e-3, peaks, rates, sms, mhz)
+    roofline_.update({"traffic": measured_traffic("bwd", w.name), "kernel": "bwd",
+                      "peak_source": f"{peaks_src} HBM copy GB/s; {rates_src} unit rates "
+                                     f"{_rates_text(rates)} x {sms} SMs x {mhz:.0f} MHz"})
     # end to end: the backward's inputs in from pinned host memory, every gradient out
     host = {k: v.cpu().pin_memory() for k, v in (("x", t["x"]), ("delta", t["delta"]),
                                                   ("B", t["B"]), ("C", t["C"]), ("dy", dy),
@@ -615,7 +733,7 @@ def bwd_main(args):
             "config": {"workload": w.name, "chunk_len": chunk, "gate": w.gate,
                        "masked": w.mask is not None,
                        "l2": "flushed between steps (256 MiB memset outside the timed events)"},
-            "roofline": roofline,
+            "roofline": roofline_,
             "cpu_baseline": None if args.no_cpu_baseline else bwd_cpu(w, chunk, args.cpu_seconds),
             "e2e": {"value": c["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
@@ -831,73 +949,49 @@ def main():
     S.load()
 
     inp = W.make_inputs(w)
+    full_valid = inp["valid_len"]
+    if args.split_batch and world > 1:
+        # one workload split across ranks by batch row: rank r scans rows [lo, hi)
+        # (the rows are independent recurrences; no data-path exchange)
+        lo, hi = shard_rows(w.batch, rank, world)
+        inp = slice_rows(inp, lo, hi)
     prep = {}
     if args.fused_delta:
         raw, bias = W.make_raw_delta(w)
+        if args.split_batch and world > 1:
+            raw = np.ascontiguousarray(raw[lo:hi])
         inp["delta"] = raw
         prep = {"dt_bias": torch.from_numpy(bias).to(dev), "delta_softplus": True}
-    t = W.to_torch(inp, dev)
-    counts = algorithmic_counts(w, inp)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    wr = w.scaled(batch=int(inp["x"].shape[0]))  # this rank's rows
+    res = time_forward(args, S, wr, inp, prep, dev, stream, flush, args.steps, args.warmup,
+                       clocks_index=local, barrier=dist.barrier if world > 1 else None)
+    ms = max_over_ranks(res["ms"], dev)
+    res_launches, res_clocks, res_wall = res["launches"], res["clocks"], res["wall"]
+    res_per_step = res["per_step"]
+    res_kernel = args_kernel(args, S, wr)
+    counts = algorithmic_counts(w, {"valid_len": full_valid})
     if args.fused_delta:  # one exp and one log per valid (b, t, d)
         counts["exps"] += 2 * counts["valid_elements"]
         counts["bytes"] += w.dim * 4
-    kernel, grid = S.plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate,
-                          mask=w.mask is not None, chunk_len=w.chunk_len, kernel=args.kernel,
-                          warps_per_block=args.warps_per_block,
-                          states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane)
-    stream = torch.cuda.Stream(dev)
-    y = torch.empty_like(t["x"])
+    if args.split_batch and world > 1:
+        value = counts["elements"] / (ms * 1e-3)  # the whole workload, shared by the ranks
+    else:
+        value = job_rate(world, counts["elements"], ms)
+    t = res["t"]
     nch = (w.seqlen + w.chunk_len - 1) // w.chunk_len if w.chunk_len else 0
-    states = (torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32, device=dev)
-              if w.chunk_len else None)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def step():
-        S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
-                   chunk_len=w.chunk_len, out=y, out_states=states, kernel=args.kernel,
-                   warps_per_block=args.warps_per_block,
-                   states_per_lane=args.states_per_lane, channels_per_lane=args.channels_per_lane,
-                   stream=stream, **prep)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-            if not args.no_flush:
-                flush.zero_()
-    torch.cuda.synchronize(dev)
-
-    K = args.steps
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local)
-    wall0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            ev0[i].record(stream)
-            step()
-            ev1[i].record(stream)
-            if not args.no_flush:
-                flush.zero_()
-    torch.cuda.synchronize(dev)
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
-    if world > 1:
-        dist.barrier()
-    per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]  # ms, one launch each
-    ms = max_over_ranks(sum(per_step) / K, dev)
-    value = job_rate(world, counts["elements"], ms)
 
     # End to end through the C ABI with host buffers: H2D of the step's inputs from
     # pinned memory, the forward, D2H of y (and chunk states), every step.
     th = W.to_torch(inp, "cpu")
     pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in th.items()}
     y_h = torch.empty(tuple(t["x"].shape), dtype=t["x"].dtype, pin_memory=True)
-    s_h = (torch.empty((w.batch, nch, w.dim, w.dstate), dtype=torch.float32, pin_memory=True)
+    s_h = (torch.empty((wr.batch, nch, w.dim, w.dstate), dtype=torch.float32, pin_memory=True)
            if w.chunk_len else None)
-    ws = torch.empty(S.host_workspace_bytes(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
+    del res, t
+    torch.cuda.empty_cache()
+    ws = torch.empty(S.host_workspace_bytes(wr.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
                                             has_D=True, gate=w.gate, mask=w.mask is not None,
                                             chunk_len=w.chunk_len),
                      dtype=torch.uint8, device=dev)
@@ -922,6 +1016,8 @@ def main():
     h2d = sum(v.numel() * v.element_size() for k, v in pinned.items()
               if isinstance(v, torch.Tensor))
     d2h = y_h.numel() * es + (s_h.numel() * 4 if s_h is not None else 0)
+    del ws, pinned, th
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -931,37 +1027,49 @@ def main():
     peaks, peaks_src = load_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     sm_mhz_peak = float(peaks.get("sm_max_mhz", 2070.0))
-    r = roof(counts, peaks, sms, sm_mhz_peak)
-    t_meas = ms * 1e-3
-    if r["t_hbm"] >= max(r["t_mufu"], r["t_fp32"]):
-        achieved = counts["bytes"] / t_meas / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": measured_traffic(S.kernel_name(kernel), w.name)}
-    else:
-        pk = MUFU_PER_SM_CLK * sms * sm_mhz_peak * 1e6 / 1e9
-        achieved = counts["exps"] / t_meas / 1e9
-        roofline = {"bound": "alu", "achieved": achieved, "peak": pk, "unit": "Gex2/s",
-                    "frac": achieved / pk,
-                    "traffic": measured_traffic(S.kernel_name(kernel), w.name)}
-    roofline.update({
-        "peak_source": f"{peaks_src} (HBM copy GB/s); ALU = {MUFU_PER_SM_CLK} ex2 and "
-                       f"{FP32_PER_SM_CLK} fp32 lanes/clk/SM x {sms} SMs x {sm_mhz_peak:.0f} MHz",
-        "kernel": S.kernel_name(kernel), "grid": grid,
+    rates, rates_src = unit_rates()
+    peak_text = (f"{peaks_src} HBM copy GB/s; {rates_src} unit rates {_rates_text(rates)} "
+                 f"x {sms} SMs x {sm_mhz_peak:.0f} MHz")
+    rl = roofline(counts, ms * 1e-3, peaks, rates, sms, sm_mhz_peak)
+    rl.update({
+        "traffic": measured_traffic(S.kernel_name(res_kernel), w.name),
+        "peak_source": peak_text, "unit_rates": rates,
+        "kernel": S.kernel_name(res_kernel),
         "warps_per_block": args.warps_per_block, "states_per_lane": args.states_per_lane,
-        "channels_per_lane": args.channels_per_lane,
-        "roof_us": {"hbm": r["t_hbm"] * 1e6, "mufu": r["t_mufu"] * 1e6,
-                    "fp32": r["t_fp32"] * 1e6},
-        "frac_of_roof": r["t_roof"] / t_meas,
-        "algorithmic": {"bytes": counts["bytes"], "exps": counts["exps"],
-                        "fp32_ops": counts["fp32_ops"]}})
+        "channels_per_lane": args.channels_per_lane})
+    # The other full-size workloads of the same forward (device-timed only, the
+    # same timing rules), each with its own roofline.
+    per_config = {}
+    forced = args.kernel != "auto" or args.warps_per_block or args.states_per_lane \
+        or args.channels_per_lane
+    if not args.no_per_config and world == 1 and not args.fused_delta and not forced:
+        for key in sorted(W.WORKLOADS):
+            if key in (1, args.workload):
+                continue
+            wk = W.WORKLOADS[key]
+            ik = W.make_inputs(wk)
+            rk = time_forward(args, S, wk, ik, {}, dev, stream, flush,
+                              max(3, min(args.steps, 20)), 3, clocks_index=local)
+            ck = algorithmic_counts(wk, ik)
+            rlk = roofline(ck, rk["ms"] * 1e-3, peaks, rates, sms, sm_mhz_peak)
+            kk = args_kernel(args, S, wk)
+            per_config[wk.name] = {
+                "ms_per_step": rk["ms"], "value": ck["elements"] / (rk["ms"] * 1e-3),
+                "unit": UNIT, "valid_elements_per_s": ck["valid_elements"] / (rk["ms"] * 1e-3),
+                "kernel": S.kernel_name(kk), "clocks": rk["clocks"],
+                "roofline": {k: rlk[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                 "frac_of_roof", "roof_us")},
+                "gpu_launches": rk["launches"]}
+            del rk, ik
+            torch.cuda.empty_cache()
     cpu = None
     if not args.no_cpu_baseline:
         cpu = time_oracle(inp, args.cpu_seconds, os.cpu_count() or 1)
         cpu.pop("seconds", None)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if args.split_batch and world > 1 else "weak",
         "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32",
         "data": "synthetic",
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
@@ -971,16 +1079,18 @@ def main():
                             else "given (already positive)",
                    "l2": "flushed between steps (256 MiB memset outside the timed events)"
                          if not args.no_flush else "not flushed",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": roofline,
+                   "parallelism": (f"batch rows split over {world} ranks" if args.split_batch
+                                   else f"replicas x{world}") if world > 1 else "single GPU"},
+        "roofline": rl,
         "cpu_baseline": cpu,
-        "e2e": {"value": job_rate(world, counts["elements"], ms_e2e), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-        "gpu_launches": K,
-        "clocks": clk,
-        "timed_wall_s": wall,
-        "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
-                        "max": max(per_step)},
+        "e2e": {"value": job_rate(1 if args.split_batch else world, counts["elements"], ms_e2e),
+                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e},
+        "gpu_launches": res_launches,
+        "clocks": res_clocks,
+        "timed_wall_s": res_wall,
+        "per_step_ms": res_per_step,
+        "per_config": per_config,
     }
     if counts["valid_elements"] != counts["elements"]:
         line["valid_elements_per_s"] = job_rate(world, counts["valid_elements"], ms)

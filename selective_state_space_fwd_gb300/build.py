@@ -21,6 +21,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libssmscan.so")
+# measurement harness: unit-rate probes the benchmark's roofline uses
+PROBE_SRC = os.path.join(PKG, "probe", "unit_rates.cu")
+PROBE_LIB = os.path.join(PKG, "libssmprobe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -54,7 +57,25 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+def build_probe(force: bool = False) -> str:
+    """libssmprobe.so: the MUFU ex2 and fp32 FMA throughput probes."""
+    if (not force and os.path.exists(PROBE_LIB)
+            and os.path.getmtime(PROBE_LIB) >= max(os.path.getmtime(PROBE_SRC),
+                                                   os.path.getmtime(os.path.abspath(__file__)))):
+        return PROBE_LIB
+    nvcc = _nvcc()
+    tmp = PROBE_LIB + ".tmp"
+    cmd = [nvcc, *ARCH, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared",
+           "-o", tmp, PROBE_SRC, "-Xlinker", f"-rpath,{_cuda_lib_dir(nvcc)}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on unit_rates.cu:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    build_probe(force)
     if not force and up_to_date():
         return LIB
     nvcc = _nvcc()

@@ -1,0 +1,123 @@
+// unit_rates.cu -- throughput probes of the two arithmetic units the selective
+// scan's roofline counts (libssmprobe.so; measurement harness, not part of
+// the scan library).
+//
+//   ex2   : ex2.approx.ftz.f32 on the MUFU unit (one per decay exp(delta A))
+//   ffma  : fma.rn.f32 on the fp32 pipe
+//   ffma2 : fma.rn.f32x2 on the fp32 pipe (two lanes of work per instruction)
+//
+// One CTA of 1024 threads per SM (a large dynamic shared-memory request keeps
+// a second CTA off the SM).  Every thread runs 8 independent dependency chains
+// so that the unit, not latency, bounds the loop; each CTA times itself with
+// clock64, so the result is in operations per SM clock, independent of the
+// clock frequency.  The chains stay bounded: v <- 2^-v maps [1/2, 1] into
+// itself, and v <- v * 0.999 + 0.001 converges to 1.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kChains = 8;
+
+__device__ __forceinline__ float ex2_neg(float v) {
+  float r;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(-v));
+  return r;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) rate_kernel(int iters, float seed,
+                                                           long long* cycles, float* sink) {
+  float v[kChains];
+  unsigned long long w[kChains];
+#pragma unroll
+  for (int i = 0; i < kChains; ++i) {
+    v[i] = 0.5f + 0.01f * ((threadIdx.x + i) & 31) * seed;
+    const float lo = v[i], hi = v[i] * 0.5f;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w[i]) : "f"(lo), "f"(hi));
+  }
+  const unsigned long long a2 = 0x3F7FBE773F7FBE77ull;  // {0.999f, 0.999f}
+  const unsigned long long b2 = 0x3A83126F3A83126Full;  // {0.001f, 0.001f}
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kChains; ++i) {
+      if (KIND == 0) v[i] = ex2_neg(v[i]);
+      if (KIND == 1) v[i] = fmaf(v[i], 0.999f, 0.001f);
+      if (KIND == 2)
+        asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(w[i]) : "l"(a2), "l"(b2));
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kChains; ++i) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(w[i]));
+    s += v[i] + lo + hi;
+  }
+  if (s == 12345.678f) sink[threadIdx.x] = s;  // keeps the chains alive
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+template <int KIND>
+int run(int sms, int iters, long long* d_cycles, float* d_sink, double* out) {
+  const int smem = 120 * 1024;  // more than half an SM's shared memory: one CTA per SM
+  if (cudaFuncSetAttribute(rate_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return 1;
+  rate_kernel<KIND><<<sms, kThreads, smem>>>(iters, 1.0f, d_cycles, d_sink);  // warm-up
+  rate_kernel<KIND><<<sms, kThreads, smem>>>(iters, 1.0f, d_cycles, d_sink);
+  if (cudaDeviceSynchronize() != cudaSuccess) return 2;
+  long long* h = new long long[sms];
+  if (cudaMemcpy(h, d_cycles, sizeof(long long) * sms, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    delete[] h;
+    return 3;
+  }
+  // median over the SMs of lane-operations per clock
+  for (int i = 1; i < sms; ++i)
+    for (int j = i; j > 0 && h[j - 1] > h[j]; --j) {
+      const long long t = h[j];
+      h[j] = h[j - 1];
+      h[j - 1] = t;
+    }
+  const double cyc = static_cast<double>(h[sms / 2]);
+  delete[] h;
+  const double lanes_per_op = KIND == 2 ? 2.0 : 1.0;
+  *out = double(kThreads) * kChains * iters * lanes_per_op / cyc;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Measures, on the current device, MUFU ex2 results per SM clock and fp32 FMA
+// lane-operations per SM clock (scalar and f32x2 forms).  Returns 0 on
+// success; *sms receives the SM count.
+int ssmprobe_unit_rates(double* ex2_per_clk, double* ffma_per_clk, double* ffma2_per_clk,
+                        int* sms) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 10;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 11;
+  *sms = n;
+  long long* d_cycles = nullptr;
+  float* d_sink = nullptr;
+  if (cudaMalloc(&d_cycles, sizeof(long long) * n) != cudaSuccess) return 12;
+  if (cudaMalloc(&d_sink, sizeof(float) * kThreads) != cudaSuccess) {
+    cudaFree(d_cycles);
+    return 12;
+  }
+  int rc = run<0>(n, 4096, d_cycles, d_sink, ex2_per_clk);
+  if (rc == 0) rc = run<1>(n, 8192, d_cycles, d_sink, ffma_per_clk);
+  if (rc == 0) rc = run<2>(n, 4096, d_cycles, d_sink, ffma2_per_clk);
+  cudaFree(d_cycles);
+  cudaFree(d_sink);
+  return rc;
+}
+
+}  // extern "C"

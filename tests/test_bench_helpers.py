@@ -70,3 +70,42 @@ def test_counts_backward():
         + 8 * 16 * 1024 * 16 * 4 + 8 * 4
     writes = 2 * e * 4 + 2 * 8 * 4096 * 16 * 4 + 1024 * 16 * 4 + 1024 * 4
     assert c["bytes"] == reads + writes
+
+
+def test_roofline_takes_the_binding_term():
+    """frac is computed against the largest of the three roof terms, and equals
+    roof time / measured time."""
+    rates = {"ex2_per_clk_sm": 32.0, "fp32_per_clk_sm": 128.0}
+    sms, mhz = 152, 2070.0
+    unit = 152 * 2070e6
+    peaks = {"hbm_gbs": 1000.0}
+    # fp32 binds: 2 s of fp32, 1 s of MUFU, 0.5 s of HBM; measured 4 s
+    c = {"bytes": 500e9, "exps": 32 * unit, "fp32_ops": 2 * 128 * unit}
+    r = bench.roofline(c, 4.0, peaks, rates, sms, mhz)
+    assert r["bound"] == "alu" and r["alu_unit"] == "fp32 FMA pipe"
+    assert r["frac"] == pytest.approx(0.5) and r["frac_of_roof"] == pytest.approx(0.5)
+    # HBM binds
+    c = {"bytes": 3000e9, "exps": 32 * unit, "fp32_ops": 128 * unit}
+    r = bench.roofline(c, 6.0, peaks, rates, sms, mhz)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["frac"] == pytest.approx(0.5)
+    # MUFU binds
+    c = {"bytes": 1e9, "exps": 3 * 32 * unit, "fp32_ops": 128 * unit}
+    r = bench.roofline(c, 3.0, peaks, rates, sms, mhz)
+    assert r["alu_unit"] == "MUFU ex2" and r["frac"] == pytest.approx(1.0)
+
+
+def test_unit_rates_without_a_gpu_fall_back_to_nominal():
+    rates, src = bench.unit_rates()
+    if src == "nominal":
+        assert rates["ex2_per_clk_sm"] == 32.0 and rates["fp32_per_clk_sm"] == 128.0
+    else:
+        assert rates["ex2_per_clk_sm"] > 0 and rates["fp32_per_clk_sm"] > 0
+
+
+def test_slice_rows_is_pure_indexing():
+    w = W.WORKLOADS[4].scaled(batch=4, seqlen=64, dim=16)
+    inp = W.make_inputs(w)
+    s = bench.slice_rows(inp, 1, 3)
+    assert np.array_equal(s["x"], inp["x"][1:3]) and np.array_equal(s["B"], inp["B"][1:3])
+    assert np.array_equal(s["valid_len"], inp["valid_len"][1:3])
+    assert s["A"] is inp["A"] and s["D"] is inp["D"]

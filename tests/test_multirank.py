@@ -60,3 +60,60 @@ def test_shard_rows_cover_batch(batch, world):
         assert 0 <= lo <= hi <= batch
         seen.extend(range(lo, hi))
     assert seen == list(range(batch))
+
+
+def _slab_worker(rank, world, port, q):
+    """One rank of a batch-split run on CPU: it scans its batch rows with the
+    oracle; rank 0 gathers the slabs with gloo."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from oracle import ref_scan
+    from selective_state_space_fwd_gb300 import workloads as W
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = W.WORKLOADS[4].scaled(batch=5, seqlen=300, dim=24)
+        inp = W.make_inputs(w)
+        lo, hi = bench.shard_rows(w.batch, rank, world)
+        mine = bench.slice_rows(inp, lo, hi)
+        y, s = ref_scan.scan_fwd(mine["x"], mine["delta"], mine["A"], mine["B"], mine["C"],
+                                 mine["D"], mine["z"], mine["valid_len"],
+                                 chunk_len=w.chunk_len, threads=1)
+        # gather variable-sized slabs: pad to the largest shard
+        per = -(-w.batch // world)
+        pad_y = np.zeros((per,) + y.shape[1:])
+        pad_s = np.zeros((per,) + s.shape[1:])
+        pad_y[:hi - lo], pad_s[:hi - lo] = y, s
+        ys = [torch.zeros(pad_y.shape, dtype=torch.float64) for _ in range(world)]
+        ss = [torch.zeros(pad_s.shape, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(ys, torch.from_numpy(pad_y))
+        dist.all_gather(ss, torch.from_numpy(pad_s))
+        if rank == 0:
+            parts = [bench.shard_rows(w.batch, r, world) for r in range(world)]
+            y_all = np.concatenate([ys[r].numpy()[:h - l] for r, (l, h) in enumerate(parts)])
+            s_all = np.concatenate([ss[r].numpy()[:h - l] for r, (l, h) in enumerate(parts)])
+            y1, s1 = ref_scan.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                       inp["D"], inp["z"], inp["valid_len"],
+                                       chunk_len=w.chunk_len, threads=1)
+            q.put((bool(np.array_equal(y_all, y1)), bool(np.array_equal(s_all, s1))))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_batch_split_slabs_reassemble_the_single_rank_result():
+    """Splitting one workload's batch rows across two ranks (bench.py
+    --split-batch) needs no exchange: the slabs each rank computes, put back in
+    row order, are the single-rank result bit for bit."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_slab_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    same_y, same_s = q.get(timeout=180)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert same_y and same_s
