@@ -84,9 +84,16 @@ typedef enum {
   SSM_KERNEL_WARPSCAN = 2, /* [P1] s3.1 hierarchy: thread-serial run of k steps,
                               5-round shuffle scan across the warp, serial carry
                               between windows; one warp per (b, d) */
-  SSM_KERNEL_STREAM = 3    /* register sweep over channels x states per thread, TMA-staged
+  SSM_KERNEL_STREAM = 3,   /* register sweep over channels x states per thread, TMA-staged
                               tiles, f32x2 math over channel pairs; needs
                               batch*dim*dstate to fill the GPU */
+  SSM_KERNEL_STREAM_TM = 4 /* the register sweep with the B and C rows broadcast to every
+                              thread through tensor memory by one exact tensor-core
+                              product per group of steps ([P1] s3.2: B and C are shared by
+                              all channels); one channel x 4 (dstate 16) or 8 (dstate 64)
+                              states per thread, f32x2 math over state pairs; dstate 16
+                              or 64, no fused step-size preparation, bf16 only with
+                              dstate 16; no launch-shape options */
 } ssm_kernel;
 
 typedef struct {

@@ -33,6 +33,7 @@ class Kernel(enum.IntEnum):
     SERIAL = 1
     WARPSCAN = 2
     STREAM = 3
+    STREAM_TM = 4
 
 
 class DType(enum.IntEnum):
@@ -204,7 +205,7 @@ def plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False, mask=False, chu
 
 
 def _kernel(k) -> Kernel:
-    return Kernel[k.upper()] if isinstance(k, str) else Kernel(k)
+    return Kernel[k.upper().replace("-", "_")] if isinstance(k, str) else Kernel(k)
 
 
 def _dtype_code(dtype) -> DType:

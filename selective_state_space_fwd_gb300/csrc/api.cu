@@ -63,11 +63,12 @@ ssm_status check_options(const ssm_options* o) {
   if (o->warps_per_block != 0 && o->warps_per_block != 1 && o->warps_per_block != 2 &&
       o->warps_per_block != 4)
     return SSM_ERR_UNSUPPORTED;
-  if (o->kernel < SSM_KERNEL_AUTO || o->kernel > SSM_KERNEL_STREAM) return SSM_ERR_UNSUPPORTED;
+  if (o->kernel < SSM_KERNEL_AUTO || o->kernel > SSM_KERNEL_STREAM_TM) return SSM_ERR_UNSUPPORTED;
   if (o->states_per_lane != 0 && o->states_per_lane != 2 && o->states_per_lane != 4 &&
       o->states_per_lane != 8 && o->states_per_lane != 16)
     return SSM_ERR_UNSUPPORTED;
-  if (o->channels_per_lane != 0 && o->channels_per_lane != 2 && o->channels_per_lane != 4)
+  if (o->channels_per_lane != 0 && o->channels_per_lane != 2 && o->channels_per_lane != 4 &&
+      !(o->channels_per_lane == 1 && o->kernel == SSM_KERNEL_STREAM_TM))
     return SSM_ERR_UNSUPPORTED;
   return SSM_OK;
 }
@@ -76,6 +77,7 @@ struct Plan {
   ssm_kernel kernel;
   int64_t grid;
   ssm::StreamShape shape;
+  ssm::StreamTmShape tm_shape;
 };
 
 // Tier choice.  `forced` is the caller's request (AUTO = let the library pick).
@@ -90,6 +92,7 @@ ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o,
     k = ssm::stream_eligible(p, bf16, shape) ? SSM_KERNEL_STREAM : SSM_KERNEL_SERIAL;
   out->kernel = k;
   out->shape = shape;
+  out->tm_shape = ssm::StreamTmShape{0, 0, 0, 0};
   switch (k) {
     case SSM_KERNEL_SERIAL:
       out->grid = ssm::serial_grid(p);
@@ -102,6 +105,16 @@ ssm_status make_plan(const ScanParams& p, ssm_dtype dtype, const ssm_options* o,
       if (!ssm::warpscan_eligible(p)) return SSM_ERR_UNSUPPORTED;
       out->grid = ssm::warpscan_grid(p);
       return SSM_OK;
+    case SSM_KERNEL_STREAM_TM: {
+      // the tier's launch shape follows from dstate and the lane layout
+      if (o && (o->warps_per_block || o->states_per_lane || o->channels_per_lane > 2))
+        return SSM_ERR_UNSUPPORTED;
+      const ssm::StreamTmShape tm = ssm::stream_tm_shape(p, bf16, o ? o->channels_per_lane : 0);
+      if (!ssm::stream_tm_eligible(p, bf16, tm)) return SSM_ERR_UNSUPPORTED;
+      out->tm_shape = tm;
+      out->grid = ssm::stream_tm_grid(p, tm);
+      return SSM_OK;
+    }
     default:
       return SSM_ERR_UNSUPPORTED;
   }
@@ -173,6 +186,7 @@ ssm_status launch(const ScanParams& p, ssm_dtype dtype, const ssm_options* opts,
     case SSM_KERNEL_SERIAL: err = ssm::launch_serial(p, bf16, stream); break;
     case SSM_KERNEL_STREAM: err = ssm::launch_stream(p, bf16, stream, plan.shape); break;
     case SSM_KERNEL_WARPSCAN: err = ssm::launch_warpscan(p, bf16, stream); break;
+    case SSM_KERNEL_STREAM_TM: err = ssm::launch_stream_tm(p, bf16, stream, plan.tm_shape); break;
     default: return SSM_ERR_UNSUPPORTED;
   }
   return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
@@ -418,6 +432,7 @@ const char* ssm_kernel_name(ssm_kernel kernel) {
     case SSM_KERNEL_SERIAL: return "serial";
     case SSM_KERNEL_WARPSCAN: return "warpscan";
     case SSM_KERNEL_STREAM: return "stream";
+    case SSM_KERNEL_STREAM_TM: return "stream-tm";
   }
   return "unknown";
 }

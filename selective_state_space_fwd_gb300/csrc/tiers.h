@@ -26,6 +26,18 @@ bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
 int64_t stream_grid(const ScanParams& p, StreamShape sh);
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);
 
+// STREAM-TM tier: the register sweep with B and C broadcast through tensor memory.
+struct StreamTmShape {
+  int g;       // states per lane
+  int r;       // channels per lane: 1 (f32x2 over state pairs) or 2 (over the channel pair)
+  int warps;   // compute warps per thread block
+  int stages;  // slots in the shared-memory ring
+};
+StreamTmShape stream_tm_shape(const ScanParams& p, bool bf16, int channels_per_lane);
+bool stream_tm_eligible(const ScanParams& p, bool bf16, StreamTmShape sh);
+int64_t stream_tm_grid(const ScanParams& p, StreamTmShape sh);
+cudaError_t launch_stream_tm(const ScanParams& p, bool bf16, cudaStream_t s, StreamTmShape sh);
+
 // WARPSCAN tier: one warp per (b, d), lanes along time, 5-round shuffle scan.
 bool warpscan_eligible(const ScanParams& p);
 int64_t warpscan_grid(const ScanParams& p);

@@ -17,16 +17,19 @@ pytestmark = pytest.mark.gpu
 
 # Tiers and STREAM launch shapes: "stream" takes the library's default shape,
 # "stream-r4" four channels per thread, "stream-g8" eight states per thread,
-# "stream-w4" four warps per CTA.
-TIERS = ["serial", "warpscan", "stream", "stream-r4", "stream-g8", "stream-w4", "auto"]
+# "stream-w4" four warps per CTA; "stream-tm" is the tier with B and C
+# broadcast through tensor memory (channel pairs per lane), "stream-tm-r1" the
+# same with one channel per lane.
+TIERS = ["serial", "warpscan", "stream", "stream-r4", "stream-g8", "stream-w4", "stream-tm",
+         "stream-tm-r1", "auto"]
 _SHAPES = {"stream-r4": dict(channels_per_lane=4), "stream-g8": dict(states_per_lane=8),
-           "stream-w4": dict(warps_per_block=4)}
+           "stream-w4": dict(warps_per_block=4), "stream-tm-r1": dict(channels_per_lane=1)}
 
 
 def _tier(kernel):
     """(tier, launch-shape keyword arguments) of a TIERS entry."""
     if kernel in _SHAPES:
-        return "stream", _SHAPES[kernel]
+        return ("stream-tm" if kernel.startswith("stream-tm") else "stream"), _SHAPES[kernel]
     return kernel, {}
 
 
