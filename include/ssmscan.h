@@ -274,6 +274,53 @@ ssm_status ssm_ssd_fwd(const void* x, const void* delta, const float* A, const v
                        const float* h0, void* out_y, float* out_final_state,
                        const ssm_ssd_shapes* shapes, ssm_dtype dtype, cudaStream_t stream);
 
+/*
+ * ssm_scan_fwd_split -- the forward with its sequence split across CTAs
+ * (the time split: [P1] s3.1's cross-block level, [P1] s4.2 the per-chunk
+ * aggregates, their scan and the fix-up; [P2] s2.3-2.4).
+ *
+ * Each batch row is cut into `segments` segments of whole 64-step tiles.
+ * Three launches on `stream`:
+ *   1. the aggregate pass: every segment but the last runs the recurrence
+ *      only (no C, no y) from a zero state (the first from h0) and leaves its
+ *      end state and its sum of delta over the valid steps;
+ *   2. the carry: per (b, d, n), the state entering segment s is
+ *      h_s = exp(A sum(delta of s-1)) h_{s-1} + end_{s-1}, the composition of
+ *      the segments' (prod a, b) aggregates under the scan's combine;
+ *   3. the output pass: every segment runs the full forward from its carried
+ *      state, so y, the chunk states and the final state are those of one
+ *      unsplit run up to the rounding of the carried states (the decay of a
+ *      segment is formed once from its sum of delta).
+ * The aggregate pass costs about half an output pass over all but the last
+ * segment; the split pays where batch * dim * dstate leaves most of the GPU
+ * idle (long sequences of few channels).
+ *
+ *   h0, out_final_state: as ssm_scan_fwd_carry (nullable).
+ *   time_segments: 0 = the library's choice (1 when the rows already fill the
+ *                  GPU), else the requested count, rounded to whole tiles.
+ *   workspace:     device memory of at least the bytes ssm_scan_split_plan
+ *                  reports, 256-byte aligned, owned by the caller and unused
+ *                  by other work until `stream` passes this call; NULL when
+ *                  the plan has one segment.
+ * The forward is the STREAM tier's (its dstate, alignment and size rules);
+ * shapes it does not take return SSM_ERR_UNSUPPORTED.  Other arguments and
+ * the outputs are those of ssm_scan_fwd_carry.
+ */
+ssm_status ssm_scan_fwd_split(const void* x, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const int32_t* valid_len, const float* h0, void* out_y,
+                              float* out_chunk_states, float* out_final_state,
+                              const ssm_shapes* shapes, ssm_dtype dtype, int64_t time_segments,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The segment count ssm_scan_fwd_split would use for these shapes and
+ * `time_segments` (0 = the library's choice, which depends on the current
+ * device's SM count) and the workspace bytes it needs (0 for one segment).
+ * Either output may be NULL. */
+ssm_status ssm_scan_split_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z,
+                               int64_t time_segments, int64_t* segments,
+                               size_t* workspace_bytes);
+
 /* The tier (and its grid) that ssm_scan_fwd_ex would launch for these
  * arguments, without launching anything.  `has_*` describe which optional
  * tensors the call passes.  Writes the tier to *kernel and the launch grid

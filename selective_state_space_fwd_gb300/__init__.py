@@ -7,12 +7,14 @@ seeded synthetic workloads used by the benchmark and tests.
 from ._binding import (Kernel, SsmError, Status, check_device_errors, chunk_count,
                        decode_step, declared_functions,
                        host_workspace_bytes, kernel_name, load, plan, scan_bwd, scan_fwd, scan_fwd_host,
-                       scan_fwd_host_static, selftest_wait_timeout, ssd_fwd, static_capacity,
+                       scan_fwd_host_static, scan_fwd_split, selftest_wait_timeout, split_plan,
+                       ssd_fwd, static_capacity,
                        status_string, version)
 
 __all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "decode_step",
            "declared_functions",
            "host_workspace_bytes", "kernel_name", "load", "plan", "scan_bwd", "scan_fwd",
-           "scan_fwd_host", "scan_fwd_host_static", "selftest_wait_timeout", "ssd_fwd",
+           "scan_fwd_host", "scan_fwd_host_static", "scan_fwd_split", "selftest_wait_timeout",
+           "split_plan", "ssd_fwd",
            "static_capacity",
            "status_string", "version"]

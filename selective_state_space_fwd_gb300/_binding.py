@@ -133,6 +133,11 @@ def load() -> ctypes.CDLL:
     lib.ssm_version.argtypes = []
     lib.ssm_check_device_errors.restype = I32
     lib.ssm_check_device_errors.argtypes = []
+    lib.ssm_scan_fwd_split.restype = I32
+    lib.ssm_scan_fwd_split.argtypes = [P] * 12 + [SP, I32, I64, P, SZ, P]
+    lib.ssm_scan_split_plan.restype = I32
+    lib.ssm_scan_split_plan.argtypes = [SP, I32, I32, I64, ctypes.POINTER(I64),
+                                        ctypes.POINTER(SZ)]
     lib.ssm_selftest_wait_timeout.restype = I32
     lib.ssm_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
     _lib = lib
@@ -314,6 +319,84 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
         raise SsmError(st, "ssm_scan_fwd_prep" if prep is not None else
                        "ssm_scan_fwd_carry" if final is not None or h0 is not None
                        else "ssm_scan_fwd")
+    if want_final or out_final is not None:
+        return y, states, final
+    return y, states
+
+
+def split_plan(batch, seqlen, dim, dstate, *, dtype="f32", gate=False,
+               time_segments: int = 0) -> tuple[int, int]:
+    """(segments, workspace bytes) of scan_fwd_split for these shapes
+    (time_segments 0 = the library's choice for the current device)."""
+    s = _shapes(batch, seqlen, dim, dstate, 0)
+    segs, nbytes = ctypes.c_int64(), ctypes.c_size_t()
+    st = load().ssm_scan_split_plan(ctypes.byref(s), int(_dtype_code(dtype)), int(gate),
+                                    int(time_segments), ctypes.byref(segs), ctypes.byref(nbytes))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_split_plan")
+    return int(segs.value), int(nbytes.value)
+
+
+def scan_fwd_split(x, delta, A, B, C, D=None, z=None, valid_len=None, *, time_segments: int = 0,
+                   chunk_len: int = 0, h0=None, want_final: bool = False, workspace=None,
+                   out=None, out_states=None, out_final=None, stream=None):
+    """The forward with each sequence split into segments run by separate CTAs
+    (aggregate pass, carry, output pass).  Arguments and results as scan_fwd
+    with h0 / want_final; ``workspace`` (a CUDA uint8 tensor) is allocated
+    here when None and the plan needs one."""
+    import torch
+    lib = load()
+    if x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev, dt = x.device, x.dtype
+    code = _dtype_code(dt)
+    batch, L, dim = x.shape
+    dstate = B.shape[-1]
+    for name, t, shape, tdt in (("x", x, (batch, L, dim), dt), ("delta", delta, (batch, L, dim), dt),
+                                ("B", B, (batch, L, dstate), dt), ("C", C, (batch, L, dstate), dt),
+                                ("A", A, (dim, dstate), torch.float32)):
+        _check(t, name, shape, tdt, dev)
+    if D is not None:
+        _check(D, "D", (dim,), torch.float32, dev)
+    if z is not None:
+        _check(z, "z", (batch, L, dim), dt, dev)
+    if valid_len is not None:
+        _check(valid_len, "valid_len", (batch,), torch.int32, dev)
+    if h0 is not None:
+        _check(h0, "h0", (batch, dim, dstate), torch.float32, dev)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", (batch, L, dim), dt, dev)
+    states = None
+    if chunk_len > 0:
+        nch = (L + chunk_len - 1) // chunk_len
+        states = (torch.empty((batch, nch, dim, dstate), dtype=torch.float32, device=dev)
+                  if out_states is None else out_states)
+        _check(states, "out_states", (batch, nch, dim, dstate), torch.float32, dev)
+    final = None
+    if want_final or out_final is not None:
+        final = (torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+                 if out_final is None else out_final)
+        _check(final, "out_final", (batch, dim, dstate), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _, need = split_plan(batch, L, dim, dstate, dtype=dt, gate=z is not None,
+                             time_segments=time_segments)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None and (workspace.device != dev or workspace.dtype != torch.uint8
+                                      or not workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous uint8 tensor on x's device")
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        s = _shapes(batch, L, dim, dstate, chunk_len)
+        st = lib.ssm_scan_fwd_split(_ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                    _ptr(z), _ptr(valid_len), _ptr(h0), _ptr(y), _ptr(states),
+                                    _ptr(final), ctypes.byref(s), int(code), int(time_segments),
+                                    _ptr(workspace),
+                                    workspace.numel() if workspace is not None else 0,
+                                    ctypes.c_void_p(handle))
+    if st != 0:
+        raise SsmError(st, "ssm_scan_fwd_split")
     if want_final or out_final is not None:
         return y, states, final
     return y, states

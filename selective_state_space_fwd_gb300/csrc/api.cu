@@ -139,6 +139,11 @@ ScanParams make_params(const void* x, const void* delta, const float* A, const v
   p.delta_clamp = 0;
   p.delta_lo = 0.f;
   p.delta_hi = 0.f;
+  p.seg_len = 0;
+  p.n_seg = 1;
+  p.seg_h0 = nullptr;
+  p.seg_hend = nullptr;
+  p.seg_dtsum = nullptr;
   return p;
 }
 
@@ -540,6 +545,108 @@ ssm_status ssm_scan_fwd_prep(const void* x, const void* delta, const ssm_delta_p
                              h0, out_final_state);
   if ((st = apply_prep(prep, &p)) != SSM_OK) return st;
   return launch(p, dtype, opts, stream);
+}
+
+}  // extern "C"
+
+// ---- the time split of the forward ---------------------------------------------
+namespace {
+
+struct SplitPlan {
+  int64_t segments, seg_len;
+  size_t bytes, off_hend, off_dtsum, off_h0;
+  ssm::StreamShape shape;
+};
+
+// Segments (0 = the library's choice), their length (whole 64-step tiles) and
+// the workspace layout: per (batch row, segment) the end state from a zero
+// start, the sum of delta, and the state carried into the segment.
+ssm_status split_plan(const ScanParams& p, ssm_dtype dtype, int64_t requested, SplitPlan* out) {
+  const bool bf16 = dtype == SSM_BF16;
+  if (requested < 0) return SSM_ERR_SHAPE;
+  const ssm::StreamShape sh1 = ssm::stream_shape(p, bf16, 0, 0, 0);
+  if (!ssm::stream_eligible(p, bf16, sh1)) return SSM_ERR_UNSUPPORTED;
+  int64_t segs = requested == 0 ? ssm::stream_auto_segments(p, sh1) : requested;
+  const int64_t tiles = (p.seqlen + 63) / 64;
+  if (segs > tiles) segs = tiles;
+  const int64_t seg_len = ((p.seqlen + segs - 1) / segs + 63) / 64 * 64;
+  segs = (p.seqlen + seg_len - 1) / seg_len;
+  ScanParams q = p;  // the launch shape for batch * segments rows
+  q.batch = p.batch * segs;
+  const ssm::StreamShape sh = segs == 1 ? sh1 : ssm::stream_shape(q, bf16, 0, 0, 0);
+  if (sh.g == 0 || ssm::stream_grid(q, sh) > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  out->segments = segs;
+  out->seg_len = segs == 1 ? 0 : seg_len;
+  out->shape = sh;
+  out->bytes = out->off_hend = out->off_dtsum = out->off_h0 = 0;
+  if (segs > 1) {
+    const size_t rows = size_t(p.batch) * segs;
+    const size_t st = rows * size_t(p.dim) * p.dstate * 4;
+    out->off_hend = 0;
+    out->off_dtsum = round_up(st, 256);
+    out->off_h0 = out->off_dtsum + round_up(rows * size_t(p.dim) * 4, 256);
+    out->bytes = out->off_h0 + st;
+  }
+  return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_split_plan(const ssm_shapes* shapes, ssm_dtype dtype, int has_z,
+                               int64_t time_segments, int64_t* segments,
+                               size_t* workspace_bytes) {
+  ssm_status st = check_shapes(shapes, dtype, false);
+  if (st != SSM_OK) return st;
+  alignas(256) static const char dummy[256] = {0};
+  ScanParams p = make_params(dummy, dummy, reinterpret_cast<const float*>(dummy), dummy, dummy,
+                             nullptr, has_z ? dummy : nullptr, nullptr, const_cast<char*>(dummy),
+                             nullptr, shapes);
+  SplitPlan plan;
+  if ((st = split_plan(p, dtype, time_segments, &plan)) != SSM_OK) return st;
+  if (segments) *segments = plan.segments;
+  if (workspace_bytes) *workspace_bytes = plan.bytes;
+  return SSM_OK;
+}
+
+ssm_status ssm_scan_fwd_split(const void* x, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const int32_t* valid_len, const float* h0, void* out_y,
+                              float* out_chunk_states, float* out_final_state,
+                              const ssm_shapes* shapes, ssm_dtype dtype, int64_t time_segments,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  ssm_status st = check_shapes(shapes, dtype, out_chunk_states != nullptr);
+  if (st != SSM_OK) return st;
+  if (!x || !delta || !A || !B || !C || !out_y) return SSM_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(x, es) || !aligned(delta, es) || !aligned(B, es) || !aligned(C, es) ||
+      !aligned(out_y, es) || (z && !aligned(z, es)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+      (valid_len && !aligned(valid_len, 4)) || (out_chunk_states && !aligned(out_chunk_states, 4)) ||
+      (h0 && !aligned(h0, 4)) || (out_final_state && !aligned(out_final_state, 4)))
+    return SSM_ERR_ALIGN;
+  ScanParams p = make_params(x, delta, A, B, C, D, z, valid_len, out_y, out_chunk_states, shapes,
+                             h0, out_final_state);
+  SplitPlan plan;
+  if ((st = split_plan(p, dtype, time_segments, &plan)) != SSM_OK) return st;
+  int dev = 0;
+  if ((st = current_device_for(stream, &dev)) != SSM_OK) return st;
+  const bool bf16 = dtype == SSM_BF16;
+  if (plan.segments == 1)  // no split: the STREAM tier as it is
+    return ssm::launch_stream(p, bf16, stream, plan.shape) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  if (workspace == nullptr) return SSM_ERR_NULL;
+  if (!aligned(workspace, 256)) return SSM_ERR_ALIGN;
+  if (workspace_bytes < plan.bytes) return SSM_ERR_SHAPE;
+  char* ws = static_cast<char*>(workspace);
+  p.seg_len = plan.seg_len;
+  p.n_seg = static_cast<int>(plan.segments);
+  p.seg_hend = reinterpret_cast<float*>(ws + plan.off_hend);
+  p.seg_dtsum = reinterpret_cast<float*>(ws + plan.off_dtsum);
+  p.seg_h0 = reinterpret_cast<float*>(ws + plan.off_h0);
+  cudaError_t e = ssm::launch_stream_agg(p, bf16, stream, plan.shape);  // aggregates
+  if (e == cudaSuccess) e = ssm::launch_seg_carry(p, stream);           // carries
+  if (e == cudaSuccess) e = ssm::launch_stream(p, bf16, stream, plan.shape);  // the outputs
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A, const void* B,

@@ -40,6 +40,14 @@ struct ScanParams {
   int delta_softplus;         // 0 / 1
   int delta_clamp;            // 0 / 1: clip to [delta_lo, delta_hi]
   float delta_lo, delta_hi;
+  // Time split (STREAM): each batch row is cut into n_seg segments of seg_len
+  // steps (a multiple of 64; 0 = one segment), each run by its own CTAs.
+  // Rows of the segment arrays below are (batch row, segment) pairs.
+  int64_t seg_len;
+  int n_seg;
+  const float* seg_h0;        // [B * n_seg, D, N] state entering segments >= 1, nullable
+  float* seg_hend;            // aggregate pass: [B * n_seg, D, N] end state from a zero start
+  float* seg_dtsum;           // aggregate pass: [B * n_seg, D] sum of delta over the segment
 };
 
 __host__ __device__ inline bool has_delta_prep(const ScanParams& p) {

@@ -99,6 +99,8 @@ int stage_bytes_of(int n, int g, int r, bool bf16, bool gate, int warps) {
   return 0;
 }
 
+}  // namespace
+
 int sm_count() {
   static int count[64] = {};
   int dev = 0;
@@ -111,6 +113,8 @@ int sm_count() {
   }
   return count[dev];
 }
+
+namespace {
 
 int channels_per_warp(int n, int g, int r) { return (32 / (n / g)) * r; }
 
@@ -242,6 +246,62 @@ int64_t stream_grid(const ScanParams& p, StreamShape sh) {
   if (sh.g == 0) return 0;
   const int64_t cpc = int64_t(stream::channels_per_warp(p.dstate, sh.g, sh.r)) * sh.wpc;
   return (p.dim + cpc - 1) / cpc * p.batch;
+}
+
+namespace {
+
+// The carry between segments of the time split, one thread per (b, d, n): the
+// state entering segment s is the composition of the earlier segments'
+// aggregates ([P1] s2.1: (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2)), segment
+// s-1 contributing its decay product 2^(A log2(e) sum(delta)) and its end
+// state from a zero start: h_s = P_{s-1} h_{s-1} + hend_{s-1}.
+__global__ void seg_carry_kernel(const ScanParams p) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int N = p.dstate;
+  if (i >= p.batch * p.dim * N) return;
+  const int64_t n = i % N, d = (i / N) % p.dim, b = i / (int64_t(N) * p.dim);
+  const float a = __ldg(p.A + d * N + n) * kLog2e;
+  float h = p.seg_hend[((b * p.n_seg) * p.dim + d) * N + n];  // end of segment 0 (from h0)
+  for (int sg = 1; sg < p.n_seg; ++sg) {
+    const int64_t row = b * p.n_seg + sg;
+    const_cast<float*>(p.seg_h0)[(row * p.dim + d) * N + n] = h;
+    if (sg + 1 < p.n_seg) {
+      const float decay = ex2(a * p.seg_dtsum[row * p.dim + d]);
+      h = fmaf(decay, h, p.seg_hend[(row * p.dim + d) * N + n]);
+    }
+  }
+}
+
+}  // namespace
+
+int64_t stream_auto_segments(const ScanParams& p, StreamShape sh) {
+  // Split only when the rows leave most schedulers without a warp: then aim
+  // at two warps per scheduler, with segments of at least 256 steps (the
+  // aggregate pass costs about half a pass over all but the last segment).
+  const int64_t warps = stream_grid(p, sh) * sh.wpc;
+  const int64_t schedulers = 4 * int64_t(stream::sm_count());
+  if (warps * 2 >= schedulers) return 1;
+  int64_t segs = (2 * schedulers + warps - 1) / warps;
+  const int64_t most = p.seqlen / 256;
+  if (segs > most) segs = most;
+  return segs < 1 ? 1 : segs;
+}
+
+cudaError_t launch_stream_agg(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh) {
+  using namespace stream;
+#define SSM_GO_AGG(n_, g_, r_)                                \
+  if (p.dstate == n_ && sh.g == g_ && sh.r == r_)             \
+    return launch_ngr_agg<n_, g_, r_>(p, bf16, s, sh.wpc, sh.stages);
+  SSM_STREAM_INSTANCES(SSM_GO_AGG)
+#undef SSM_GO_AGG
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_seg_carry(const ScanParams& p, cudaStream_t s) {
+  const int64_t total = p.batch * p.dim * p.dstate;
+  const int threads = 256;
+  seg_carry_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh) {

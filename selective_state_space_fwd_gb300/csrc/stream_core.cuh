@@ -278,10 +278,14 @@ constexpr int pad_prow(int NG, int CW, int R, int PS) {
 }
 
 // Compile-time shape of one STREAM instance.
-template <int N_, int G_, int R_, typename IO_, bool GATE_, bool DTP_ = false>
+template <int N_, int G_, int R_, typename IO_, bool GATE_, bool DTP_ = false, bool AGG_ = false>
 struct Cfg {
   static constexpr int N = N_, G = G_, R = R_;
   static constexpr bool GATE = GATE_;
+  // AGG: the aggregate pass of the time split -- the state recurrence only
+  // (no C, no y), from a zero state for segments >= 1; writes each segment's
+  // end state and its sum of delta.
+  static constexpr bool AGG = AGG_;
   // DTP: the fused step-size preparation (bias, softplus, clipping) runs once
   // per tile over the warp's delta slab; for fp32 in place, for bf16 into an
   // fp32 slab of the warp (the prepared step is not rounded to bf16).
@@ -322,6 +326,7 @@ struct Cfg {
   static_assert(T % M == 0 && M % (2 * U) == 0 && M % NG == 0, "tile steps");
   static_assert(PROW % 4 == 0 && PS % 4 == 0 && PBYTES <= 12 * 1024, "partial buffer");
   static_assert(SLAB % 128 == 0 && ROWT % 128 == 0, "slot alignment");
+  static_assert(!(AGG && (DTP || GATE)), "the aggregate pass takes delta as given and has no gate");
 };
 
 // One batch of U steps' inputs for this lane, as loaded from the tile.
@@ -341,7 +346,7 @@ __device__ __forceinline__ void load_batch(Raw<K>& r, const typename K::DT* ds,
     Tile<typename K::DT>::template pairs<K::PR>(ds + (s + u) * K::CW, r.dt[u]);
     TL::template pairs<K::PR>(xs + (s + u) * K::CW, r.x[u]);
     TL::template row<K::G>(bs + (s + u) * K::N, r.b[u], coff);
-    TL::template row<K::G>(cs + (s + u) * K::N, r.c[u], coff);
+    if constexpr (!K::AGG) TL::template row<K::G>(cs + (s + u) * K::N, r.c[u], coff);
   }
 }
 
@@ -352,6 +357,7 @@ template <class K>
 struct Prep {
   u64 ab[K::U][K::PR][K::G], bi[K::U][K::PR][K::G];
   float c[K::U][K::G];
+  u64 dt[K::AGG ? K::U : 1][K::PR];  // the aggregate pass sums delta
 };
 
 template <class K>
@@ -361,6 +367,7 @@ __device__ __forceinline__ void prepare(Prep<K>& o, const Raw<K>& r, const u64 (
 #pragma unroll
     for (int q = 0; q < K::PR; ++q) {
       const u64 dt = r.dt[u][q];
+      if constexpr (K::AGG) o.dt[u][q] = dt;
       const u64 ux = mul2(dt, r.x[u][q]);  // delta x
 #pragma unroll
       for (int n = 0; n < K::G; ++n) {
@@ -369,8 +376,10 @@ __device__ __forceinline__ void prepare(Prep<K>& o, const Raw<K>& r, const u64 (
         o.bi[u][q][n] = mul2(ux, pk2(r.b[u][n], r.b[u][n]));
       }
     }
+    if constexpr (!K::AGG) {
 #pragma unroll
-    for (int n = 0; n < K::G; ++n) o.c[u][n] = r.c[u][n];
+      for (int n = 0; n < K::G; ++n) o.c[u][n] = r.c[u][n];
+    }
   }
 }
 
@@ -405,21 +414,27 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpc = W * CW;
   const int64_t n_cb = (p.dim + cpc - 1) / cpc;
-  const int64_t b = blockIdx.x / n_cb;
+  const int64_t row = blockIdx.x / n_cb;  // (batch row, segment of the time split)
+  const int64_t b = row / p.n_seg;
+  const int seg = static_cast<int>(row % p.n_seg);
+  if (K::AGG && seg == p.n_seg - 1) return;  // the last segment's aggregate is not needed
   const int d0 = static_cast<int>((blockIdx.x % n_cb) * cpc);
   const int cg = lane / NG, sg = lane % NG;
   const int dw = d0 + warp * CW;       // the warp's first channel
   const int64_t dl = dw + cg * R;      // the lane's first channel
   const bool d_ok = dl < p.dim;        // all R channels valid (dim is a multiple of R)
   const int64_t L = p.seqlen;
-  const int64_t lv = valid_steps(p, b);
+  // this CTA's steps: [seg0, seg0 + Ls) of the row, lv of them valid
+  const int64_t seg0 = p.seg_len > 0 ? seg * p.seg_len : 0;
+  const int64_t Ls = p.seg_len > 0 ? min(p.seg_len, L - seg0) : L;
+  const int64_t lv = min(max(valid_steps(p, b) - seg0, int64_t(0)), Ls);
   const int n_tiles = static_cast<int>((lv + T - 1) / T);  // tiles with a valid step
   const bool producer = threadIdx.x == 0;
 
   auto issue = [&](int tile, int slot) {
     char* st = smem + slot * SB;
-    const int t0 = tile * T;
-    mbar_expect_tx(&full[slot], SB);
+    const int t0 = static_cast<int>(seg0) + tile * T;
+    mbar_expect_tx(&full[slot], K::AGG ? SB - K::ROWT : SB);
     for (int w = 0; w < W; ++w) {
       tma_load_3d(st + (0 * W + w) * K::SLAB, &tm_x, d0 + w * CW, t0, static_cast<int>(b),
                   &full[slot]);
@@ -431,7 +446,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     char* rows = st + K::NACT * W * K::SLAB;
     tma_load_3d(rows, &tm_b, 0, t0, static_cast<int>(b), &full[slot]);
-    tma_load_3d(rows + K::ROWT, &tm_c, 0, t0, static_cast<int>(b), &full[slot]);
+    if constexpr (!K::AGG) tma_load_3d(rows + K::ROWT, &tm_c, 0, t0, static_cast<int>(b), &full[slot]);
   };
 
   if (producer) {
@@ -456,7 +471,10 @@ __global__ void __launch_bounds__(128, 1)
     return MCH > 1 ? sg * G + ((n / CHK + rot) % MCH) * CHK + n % CHK : sg * G + n;
   };
   // Per-lane constants: log2(e)-scaled A for (channel pair, state), the
-  // initial state.
+  // initial state: the caller's h0 for the first segment; for a later one the
+  // state carried into it (the aggregate pass starts those from zero).
+  const float* h0row = seg == 0 ? (p.h0 ? p.h0 + b * p.dim * N : nullptr)
+                                : (!K::AGG && p.seg_h0 ? p.seg_h0 + row * p.dim * N : nullptr);
   u64 a2[PR][G], h2[PR][G];
 #pragma unroll
   for (int q = 0; q < PR; ++q) {
@@ -470,14 +488,17 @@ __global__ void __launch_bounds__(128, 1)
       }
       a2[q][n] = pk2(lo, hi);
       float h_lo = 0.f, h_hi = 0.f;  // [P1] s4.1: h_0 = 0 unless given
-      if (d_ok && p.h0) {
-        h_lo = __ldg(p.h0 + (b * p.dim + d_lo) * N + gsn(n));
-        h_hi = __ldg(p.h0 + (b * p.dim + d_hi) * N + gsn(n));
+      if (d_ok && h0row) {
+        h_lo = __ldg(h0row + d_lo * N + gsn(n));
+        h_hi = __ldg(h0row + d_hi * N + gsn(n));
       }
       h2[q][n] = pk2(h_lo, h_hi);
     }
   }
 
+  u64 dsum[PR];  // the aggregate pass: sum of delta of the lane's channels
+#pragma unroll
+  for (int q = 0; q < PR; ++q) dsum[q] = 0;
   // Bias of the channels this lane prepares step sizes for (element e of the
   // warp's slab belongs to channel e % CW; lane l visits e = l + 32 k).
   constexpr int NBV = CW > 32 ? CW / 32 : 1;
@@ -497,11 +518,11 @@ __global__ void __launch_bounds__(128, 1)
   for (int q = 0; q < PR; ++q)
     dsk[q] = (de_ok && p.D) ? pk2(__ldg(p.D + de + 2 * q), __ldg(p.D + de + 2 * q + 1)) : 0;
   IO* __restrict__ yout = static_cast<IO*>(p.y);
-  const bool want_states = p.states != nullptr;
+  const bool want_states = !K::AGG && p.states != nullptr;
   // Chunk c ends at step min((c+1) chunk_len, L) - 1 ([P1] s3.4).
   auto chunk_end = [&](int64_t c) { return min((c + 1) * p.chunk_len, L) - 1; };
-  int64_t next_c = 0;
-  int64_t next_ce = want_states ? chunk_end(0) : INT64_MAX;
+  int64_t next_c = want_states ? seg0 / p.chunk_len : 0;  // first chunk ending in the segment
+  int64_t next_ce = want_states ? chunk_end(next_c) : INT64_MAX;
   // the lane's G states of each of its R channels, as rows of `dst`
   auto put_state = [&](float* dst) {
 #pragma unroll
@@ -546,8 +567,9 @@ __global__ void __launch_bounds__(128, 1)
     const typename K::DT* ds;  // this lane's delta column, as the recurrence reads it
     const IO* bs = reinterpret_cast<const IO*>(st + K::NACT * W * K::SLAB) + sg * G;
     const IO* cs = bs + T * N;
-    const int64_t t0 = static_cast<int64_t>(i) * T;
-    const int steps = static_cast<int>(lv - t0 < T ? lv - t0 : T);  // valid steps in tile
+    const int64_t tl = static_cast<int64_t>(i) * T;                 // tile start in the segment
+    const int64_t t0 = seg0 + tl;                                    // tile start in the row
+    const int steps = static_cast<int>(lv - tl < T ? lv - tl : T);  // valid steps in tile
     IO* ybase = yout + (b * L + t0) * p.dim + de;                    // y[b, t0, de]
     if constexpr (K::DTP) {
       // The step size of every (step, channel) of the warp, prepared once:
@@ -673,6 +695,16 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             const int j = k * U + u;  // step within the block
+            if constexpr (K::AGG) {  // the state only, and the sum of delta
+#pragma unroll
+              for (int q = 0; q < PR; ++q) {
+                dsum[q] = add2(dsum[q], cur.dt[u][q]);
+#pragma unroll
+                for (int n = 0; n < G; ++n)
+                  h2[q][n] = fma2(cur.ab[u][q][n], h2[q][n], cur.bi[u][q][n]);  // h = Abar h + b
+              }
+              continue;
+            }
             // C h accumulates in NA independent chains (short dependency
             // chains: one warp per scheduler has little else to overlap)
             constexpr int NA = G >= 8 ? 4 : (G >= 4 ? 2 : 1);
@@ -723,7 +755,7 @@ __global__ void __launch_bounds__(128, 1)
         ++next_c;
         next_ce = next_c < p.n_chunks ? chunk_end(next_c) : INT64_MAX;
       }
-      epilogue(s0);
+      if constexpr (!K::AGG) epilogue(s0);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -733,18 +765,37 @@ __global__ void __launch_bounds__(128, 1)
     return;
   }
 
+  if constexpr (K::AGG) {
+    // the segment's aggregate: its end state from a zero start (or the
+    // caller's h0 for the first segment) and its sum of delta over the valid
+    // steps (padded steps have delta 0)
+    if (d_ok) {
+      put_state(p.seg_hend + row * p.dim * N);
+      if (sg == 0) {
+#pragma unroll
+        for (int q = 0; q < PR; ++q) {
+          const float2 v = upk2(dsum[q]);
+          p.seg_dtsum[row * p.dim + dl + 2 * q] = v.x;
+          p.seg_dtsum[row * p.dim + dl + 2 * q + 1] = v.y;
+        }
+      }
+    }
+    return;
+  }
   // Steps past valid_len: exact zeros, frozen state for the remaining chunk ends.
-  if (lv < L) {
-    const int64_t total = (L - lv) * CW;
+  if (lv < Ls) {
+    const int64_t total = (Ls - lv) * CW;
     for (int64_t e = lane; e < total; e += 32) {
-      const int64_t t = lv + e / CW;
+      const int64_t t = seg0 + lv + e / CW;
       const int c = static_cast<int>(e % CW);
       if (dw + c < p.dim) TL::put_zero(yout, (b * L + t) * p.dim + dw + c);
     }
   }
-  if (want_states)
-    for (; next_c < p.n_chunks; ++next_c) store_state(chunk_end(next_c));  // frozen state
-  if (p.h_final && d_ok) put_state(p.h_final + b * p.dim * N);  // state after the last step
+  if (want_states)  // frozen state for the chunks that end in this segment
+    for (; next_c < p.n_chunks && chunk_end(next_c) < seg0 + Ls; ++next_c)
+      store_state(chunk_end(next_c));
+  if (p.h_final && d_ok && seg == p.n_seg - 1)
+    put_state(p.h_final + b * p.dim * N);  // state after the last step
 }
 
 // Host side, defined in kernel_stream.cu.
@@ -790,7 +841,7 @@ cudaError_t launch_k(const ScanParams& p, cudaStream_t s, int warps, int stages)
   }
   if (smem > max_dynamic_smem()) return cudaErrorInvalidValue;
   const int64_t n_cb = (p.dim + warps * K::CW - 1) / (warps * K::CW);
-  const int64_t grid = n_cb * p.batch;
+  const int64_t grid = n_cb * p.batch * p.n_seg;
   stream_kernel<K><<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(mx, mdt, mz, mb, mc, p,
                                                                         la);
   return cudaGetLastError();
@@ -799,6 +850,10 @@ cudaError_t launch_k(const ScanParams& p, cudaStream_t s, int warps, int stages)
 // Every launcher of one (N, G, R) instance: fp32 / bf16, with / without gate.
 template <int N, int G, int R>
 cudaError_t launch_ngr(const ScanParams& p, bool bf16, cudaStream_t s, int warps, int stages);
+
+// The aggregate pass of the time split (default shapes only).
+template <int N, int G, int R>
+cudaError_t launch_ngr_agg(const ScanParams& p, bool bf16, cudaStream_t s, int warps, int stages);
 
 // Per-stage bytes of an instance, for the host's ring sizing.
 template <int N, int G, int R>
@@ -841,6 +896,21 @@ cudaError_t launch_ngr_impl(const ScanParams& p, bool bf16, cudaStream_t s, int 
 }
 
 template <int N, int G, int R>
+cudaError_t launch_ngr_agg_impl(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
+  if constexpr (dtp_shape(N, G, R)) {
+    if (bf16) {
+      if constexpr (bf16_ok<N, G, R>())
+        return launch_k<Cfg<N, G, R, __nv_bfloat16, false, false, true>>(p, s, w, st);
+      else
+        return cudaErrorInvalidValue;
+    }
+    return launch_k<Cfg<N, G, R, float, false, false, true>>(p, s, w, st);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+}
+
+template <int N, int G, int R>
 int stage_bytes_impl(bool bf16, bool gate, int w) {
   if (bf16) {
     if constexpr (bf16_ok<N, G, R>())
@@ -860,6 +930,11 @@ int stage_bytes_impl(bool bf16, bool gate, int w) {
     return launch_ngr_impl<N_, G_, R_>(p, bf16, s, w, st);                                   \
   }                                                                                          \
   template <>                                                                                \
+  cudaError_t launch_ngr_agg<N_, G_, R_>(const ScanParams& p, bool bf16, cudaStream_t s,    \
+                                         int w, int st) {                                    \
+    return launch_ngr_agg_impl<N_, G_, R_>(p, bf16, s, w, st);                               \
+  }                                                                                          \
+  template <>                                                                                \
   int stage_bytes_ngr<N_, G_, R_>(bool bf16, bool gate, int w) {                             \
     return stage_bytes_impl<N_, G_, R_>(bf16, gate, w);                                      \
   }
@@ -875,6 +950,8 @@ int stage_bytes_impl(bool bf16, bool gate, int w) {
 #define SSM_STREAM_DECLARE(N_, G_, R_)                                                      \
   template <>                                                                               \
   cudaError_t launch_ngr<N_, G_, R_>(const ScanParams&, bool, cudaStream_t, int, int);     \
+  template <>                                                                               \
+  cudaError_t launch_ngr_agg<N_, G_, R_>(const ScanParams&, bool, cudaStream_t, int, int); \
   template <>                                                                               \
   int stage_bytes_ngr<N_, G_, R_>(bool, bool, int);
 

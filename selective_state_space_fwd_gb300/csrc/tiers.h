@@ -25,6 +25,12 @@ StreamShape stream_shape(const ScanParams& p, bool bf16, int warps_per_block, in
 bool stream_eligible(const ScanParams& p, bool bf16, StreamShape sh);
 int64_t stream_grid(const ScanParams& p, StreamShape sh);
 cudaError_t launch_stream(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);
+// Time split of STREAM: the aggregate pass (segments' end states from a zero
+// start and their sums of delta) and the carry between segments.
+cudaError_t launch_stream_agg(const ScanParams& p, bool bf16, cudaStream_t s, StreamShape sh);
+cudaError_t launch_seg_carry(const ScanParams& p, cudaStream_t s);
+// The number of segments the library picks for a row layout (1 = no split).
+int64_t stream_auto_segments(const ScanParams& p, StreamShape sh);
 
 // STREAM-TM tier: the register sweep with B and C broadcast through tensor memory.
 struct StreamTmShape {

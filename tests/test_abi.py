@@ -12,7 +12,7 @@ EXPECTED = {"ssm_scan_fwd", "ssm_scan_fwd_ex", "ssm_scan_fwd_carry", "ssm_scan_f
             "ssm_scan_fwd_host_static", "ssm_scan_host_static_capacity", "ssm_scan_fwd_host",
             "ssm_scan_host_workspace_bytes", "ssm_chunk_count", "ssm_status_string",
             "ssm_kernel_name", "ssm_version", "ssm_check_device_errors", "ssm_ssd_fwd",
-            "ssm_selftest_wait_timeout"}
+            "ssm_selftest_wait_timeout", "ssm_scan_fwd_split", "ssm_scan_split_plan"}
 
 
 def test_every_declared_symbol_is_exported(ssmlib):
@@ -300,3 +300,25 @@ def test_selftest_poll_bound(ssmlib):
     """The bounded-wait self-test refuses a poll count above its bound before
     launching anything."""
     assert Bd.load().ssm_selftest_wait_timeout((1 << 20) + 1, None) == Bd.Status.ERR_SHAPE
+
+
+def test_split_argument_errors_return_status(ssmlib):
+    """The time-split entry validates before launching anything."""
+    lib = Bd.load()
+    P = ctypes.c_void_p
+    s = Bd.Shapes(2, 640, 32, 16, 0)
+
+    def call(x=FAKE, y=FAKE, segs=2, ws=None, nbytes=0, shapes=s, h0=None):
+        return lib.ssm_scan_fwd_split(P(x), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, None, None,
+                                      P(h0), P(y), None, None, ctypes.byref(shapes), 0, segs, P(ws),
+                                      nbytes, None)
+    assert call(x=None) == Bd.Status.ERR_NULL
+    assert call(y=None) == Bd.Status.ERR_NULL
+    assert call(segs=-1) == Bd.Status.ERR_SHAPE
+    assert call(h0=FAKE + 2) == Bd.Status.ERR_ALIGN
+    assert call(shapes=Bd.Shapes(2, 0, 32, 16, 0)) == Bd.Status.ERR_SHAPE
+    segs, nbytes = Bd.split_plan(2, 640, 32, 16, time_segments=2)
+    assert segs == 2 and nbytes > 0
+    assert Bd.split_plan(2, 640, 32, 16, time_segments=1) == (1, 0)
+    with pytest.raises(Bd.SsmError):
+        Bd.split_plan(2, 640, 32, 16, time_segments=-3)
