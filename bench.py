@@ -246,11 +246,14 @@ def parse():
     ap.add_argument("--fused-delta", action="store_true",
                     help="softplus workloads: pass the raw step inputs and dt_bias and let the "
                          "kernel apply softplus(raw + dt_bias)")
-    ap.add_argument("--op", default="scan", choices=["scan", "decode", "bwd", "ssd"],
+    ap.add_argument("--op", default="scan", choices=["scan", "decode", "bwd", "ssd", "split"],
                     help="scan: the forward (default); decode: one recurrence step on a "
                          "carried state (--workload picks a decode workload); bwd: the "
                          "backward, replaying from chunk states (--bwd-chunk); ssd: the "
-                         "SSD form (one decay per head) on the tensor cores")
+                         "SSD form (one decay per head) on the tensor cores; split: a long "
+                         "sequence of few channels split across CTAs (--split-workload)")
+    ap.add_argument("--split-workload", type=int, default=1,
+                    help="with --op split: 1 = b1 L65536 d256 N16, 2 = b2 L32768 d512 N64")
     ap.add_argument("--bwd-chunk", type=int, default=256)
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the chosen workload, not the other full-size forwards")
@@ -918,6 +921,118 @@ def ssd_main(args):
     print(json.dumps(line), flush=True)
 
 
+SPLIT_METRIC = ("selective-scan fwd, sequence split across CTAs: B*L*D elems/s and achieved % "
+                "of roofline, 1xGB300")
+
+
+def split_main(args):
+    """The time split on a long sequence of few channels: scan_fwd with the
+    library's choice (the split) against one segment, device buffers."""
+    from selective_state_space_fwd_gb300 import workloads as W
+    w = W.SPLIT_WORKLOADS[args.split_workload]
+    if args.impl == "reference":
+        reference_arm(args, w)
+        return
+    import torch
+    import selective_state_space_fwd_gb300 as S
+    from selective_state_space_fwd_gb300 import build as B
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.build()
+    S.load()
+    inp = W.make_inputs(w)
+    t = W.to_torch(inp, dev)
+    segs, nbytes = S.split_plan(w.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype, gate=w.gate)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(t["x"])
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(nseg, K):
+        def step():
+            S.scan_fwd_split(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                             t["valid_len"], time_segments=nseg, out=y, workspace=ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                step()
+                flush.zero_()
+        torch.cuda.synchronize(dev)
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        clocks = ClockSampler(local)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                ev0[i].record(stream)
+                step()
+                ev1[i].record(stream)
+                flush.zero_()
+        torch.cuda.synchronize(dev)
+        clk = clocks.stop()
+        S.check_device_errors()
+        per = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+        return sum(per) / K, clk, per
+
+    ms, clk, per = timed(segs, args.steps)
+    ms1, _, _ = timed(1, max(3, min(args.steps, 10)))
+    counts = algorithmic_counts(w, inp)
+    peaks, peaks_src = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    rates, rates_src = unit_rates()
+    rl = roofline(counts, ms * 1e-3, peaks, rates, sms, mhz)
+    rl.update({"kernel": "stream (aggregate pass, carry, output pass)", "traffic": None,
+               "peak_source": f"{peaks_src} HBM copy GB/s; {rates_src} unit rates "
+                              f"{_rates_text(rates)} x {sms} SMs x {mhz:.0f} MHz"})
+    # end to end: inputs from pinned host memory, the split forward, y back
+    th = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) else None)
+          for k, v in t.items() if k in ("x", "delta", "A", "B", "C", "D")}
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in th.items() if v is not None}
+    y_h = torch.empty(tuple(y.shape), dtype=y.dtype, pin_memory=True)
+
+    def step_host():
+        with torch.cuda.stream(stream):
+            for k, v in th.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            S.scan_fwd_split(dbuf["x"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"], dbuf["D"],
+                             time_segments=segs, out=y, workspace=ws, stream=stream)
+            y_h.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        step_host()
+    torch.cuda.synchronize(dev)
+    KE = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        step_host()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / KE
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = time_oracle(inp, args.cpu_seconds, os.cpu_count() or 1)
+        cpu.pop("seconds", None)
+    line = {
+        "metric": SPLIT_METRIC, "value": counts["elements"] / (ms * 1e-3), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
+                   "dstate": w.dstate, "segments": segs,
+                   "l2": "flushed between steps (256 MiB memset outside the timed events)"},
+        "roofline": rl, "cpu_baseline": cpu,
+        "unsplit": {"ms_per_step": ms1, "value": counts["elements"] / (ms1 * 1e-3)},
+        "e2e": {"value": counts["elements"] / (ms_e2e * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in th.values()
+                                          if v is not None),
+                "d2h_bytes_per_step": y_h.numel() * y_h.element_size(), "ms_per_step": ms_e2e},
+        "gpu_launches": 3 * args.steps, "clocks": clk,
+        "per_step_ms": {"min": min(per), "median": statistics.median(per), "max": max(per)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.op == "decode":
@@ -928,6 +1043,9 @@ def main():
         return
     if args.op == "ssd":
         ssd_main(args)
+        return
+    if args.op == "split":
+        split_main(args)
         return
     from selective_state_space_fwd_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]

@@ -244,7 +244,7 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
              out=None, out_states=None, kernel: Kernel | str = Kernel.AUTO,
              warps_per_block: int = 0, states_per_lane: int = 0, channels_per_lane: int = 0,
              stream=None, h0=None, want_final: bool = False, out_final=None, dt_bias=None,
-             delta_softplus: bool = False, delta_clamp=None):
+             delta_softplus: bool = False, delta_clamp=None, time_segments: int | None = None):
     """The fused selective-scan forward on CUDA tensors.
 
     x, delta, z: [batch, L, dim]; B, C: [batch, L, dstate] (fp32 or bf16, all the
@@ -256,12 +256,32 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, valid_len=None, *, chunk_len: in
     final being the fp32 state after the last step.  ``dt_bias`` (fp32 [dim]),
     ``delta_softplus`` and ``delta_clamp`` = (lo, hi) ask for the fused
     step-size preparation of delta.
+    With the library's choice of tier (AUTO, no launch-shape options, no
+    step-size preparation) and ``time_segments`` None, a sequence whose batch
+    rows leave most of the GPU idle runs through the time split
+    (scan_fwd_split, workspace from PyTorch); ``time_segments`` = 1 keeps one
+    segment, k > 1 asks for k.
     Runs on ``stream`` (default: the current PyTorch stream of x's device).
     """
     import torch
     lib = load()
     if x.device.type != "cuda":
         raise ValueError("x must be a CUDA tensor")
+    plain = (_kernel(kernel) == Kernel.AUTO and not (warps_per_block or states_per_lane
+             or channels_per_lane) and dt_bias is None and not delta_softplus
+             and delta_clamp is None)
+    if plain and time_segments != 1 and x.dim() == 3 and B.dim() == 3:
+        segs = time_segments or 0
+        try:
+            with torch.cuda.device(x.device):
+                n, _ = split_plan(x.shape[0], x.shape[1], x.shape[2], B.shape[-1], dtype=x.dtype,
+                                  gate=z is not None, time_segments=segs)
+        except SsmError:
+            n = 1  # the split does not take this shape: the tiers below do
+        if n > 1:
+            return scan_fwd_split(x, delta, A, B, C, D, z, valid_len, time_segments=segs,
+                                  chunk_len=chunk_len, h0=h0, want_final=want_final, out=out,
+                                  out_states=out_states, out_final=out_final, stream=stream)
     dev, dt = x.device, x.dtype
     code = _dtype_code(dt)
     batch, L, dim = x.shape

@@ -79,6 +79,15 @@ WORKLOADS: dict[int, Workload] = {
                 "ones", False, None, 0, 4),
 }
 
+# Long sequences of few channels, for the time split of the forward (the rows
+# alone leave most of the GPU idle): distributions of workloads 2 and 5.
+SPLIT_WORKLOADS = {
+    1: Workload(301, "long-few-channels-fp32-b1-l65536-d256-n16", 1, 65536, 256, 16, "f32",
+                "softplus", "s4d_exp", "normal", False, None, 0, 31),
+    2: Workload(302, "long-few-channels-fp32-b2-l32768-d512-n64", 2, 32768, 512, 64, "f32",
+                "loguniform", "s4d", "ones", False, None, 0, 32),
+}
+
 # Decode steps (one step of the recurrence on a carried state): the inputs of
 # one time step for every (batch row, channel), drawn like the scan workloads'
 # (seqlen 1), plus a state [batch, dim, dstate] ~ N(0, 1) in fp32.  The state

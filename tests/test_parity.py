@@ -47,11 +47,11 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(inp: dict, kernel="auto"):
+def run_gpu(inp: dict, kernel="auto", **kw):
     t = W.to_torch(inp, "cuda")
     k, shape = _tier(kernel)
     y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
-                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, **shape)
+                      t["valid_len"], chunk_len=inp["chunk_len"], kernel=k, **shape, **kw)
     torch.cuda.synchronize()
     return to_f64(y), (to_f64(s) if s is not None else None)
 
@@ -265,7 +265,7 @@ def test_host_entry_point_matches_device(oracle):
                                pinned["C"], pinned["D"], pinned["z"], pinned["valid_len"],
                                chunk_len=inp["chunk_len"])
     torch.cuda.synchronize()
-    y_d, s_d = run_gpu(inp)
+    y_d, s_d = run_gpu(inp, time_segments=1)  # the host entry runs the unsplit tier per piece
     assert np.array_equal(to_f64(y_h), y_d)
     assert np.array_equal(to_f64(s_h), s_d)
 
@@ -286,7 +286,7 @@ def test_host_entry_pipelined_pieces(oracle, case):
                                pinned["C"], pinned["D"], pinned["z"], pinned["valid_len"],
                                chunk_len=inp["chunk_len"])
     torch.cuda.synchronize()
-    y_d, s_d = run_gpu(inp)
+    y_d, s_d = run_gpu(inp, time_segments=1)  # the host entry runs the unsplit tier per piece
     assert np.array_equal(to_f64(y_h), y_d)
     if s_d is not None:
         assert np.array_equal(to_f64(s_h), s_d)

@@ -99,3 +99,21 @@ def test_split_argument_errors():
     with pytest.raises(S.SsmError) as ei:
         S.scan_fwd_split(t1["x"], t1["delta"], t1["A"], t1["B"], t1["C"], time_segments=2)
     assert ei.value.status == S.Status.ERR_UNSUPPORTED
+
+
+def test_scan_fwd_routes_few_channel_rows_through_the_split(oracle):
+    """scan_fwd with the library's choice of tier takes the time split when the
+    rows leave the GPU mostly idle, and the result is the oracle's."""
+    w, inp, _ = _case(batch=1, L=8192, dim=64, N=16, chunk=512, mask=[7000])
+    segs, _ = S.split_plan(w.batch, w.seqlen, w.dim, w.dstate)
+    assert segs > 1
+    t = W.to_torch(inp, "cuda")
+    y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], None, t["valid_len"],
+                      chunk_len=w.chunk_len)
+    y1, s1 = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], None, t["valid_len"],
+                        chunk_len=w.chunk_len, time_segments=1)
+    torch.cuda.synchronize()
+    y_ref, s_ref = oracle.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   None, inp["valid_len"], chunk_len=w.chunk_len)
+    for yy, ss in ((y, s), (y1, s1)):
+        assert _rel(_f64(yy), y_ref) <= 1e-5 and _rel(_f64(ss), s_ref) <= 1e-5
