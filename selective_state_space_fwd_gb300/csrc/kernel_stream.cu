@@ -261,13 +261,27 @@ __global__ void seg_carry_kernel(const ScanParams p) {
   if (i >= p.batch * p.dim * N) return;
   const int64_t n = i % N, d = (i / N) % p.dim, b = i / (int64_t(N) * p.dim);
   const float a = __ldg(p.A + d * N + n) * kLog2e;
+  float* seg_h0 = const_cast<float*>(p.seg_h0);
   float h = p.seg_hend[((b * p.n_seg) * p.dim + d) * N + n];  // end of segment 0 (from h0)
-  for (int sg = 1; sg < p.n_seg; ++sg) {
-    const int64_t row = b * p.n_seg + sg;
-    const_cast<float*>(p.seg_h0)[(row * p.dim + d) * N + n] = h;
-    if (sg + 1 < p.n_seg) {
-      const float decay = ex2(a * p.seg_dtsum[row * p.dim + d]);
-      h = fmaf(decay, h, p.seg_hend[(row * p.dim + d) * N + n]);
+  // The aggregates do not depend on the carried state: those of 16 segments
+  // are loaded together, then composed in order.
+  constexpr int CH = 16;
+  for (int s0 = 1; s0 < p.n_seg; s0 += CH) {
+    float dts[CH], he[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int64_t row = b * p.n_seg + s0 + j;
+      const bool need = s0 + j + 1 < p.n_seg;  // the last segment's aggregate is not used
+      dts[j] = need ? p.seg_dtsum[row * p.dim + d] : 0.f;
+      he[j] = need ? p.seg_hend[(row * p.dim + d) * N + n] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int sg = s0 + j;
+      if (sg < p.n_seg) {
+        seg_h0[((b * p.n_seg + sg) * p.dim + d) * N + n] = h;
+        h = fmaf(ex2(a * dts[j]), h, he[j]);
+      }
     }
   }
 }
