@@ -729,7 +729,7 @@ def bwd_main(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1) / KE
-    line = {"metric": BWD_METRIC, "value": c["elements"] / t_meas, "unit": UNIT, "n_gpus": 1,
+    line = {"metric": BWD_METRIC, "value": c["elements"] / (ms * 1e-3), "unit": UNIT, "n_gpus": 1,
             "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if w.dtype == "f32" else "bf16-io/f32", "data": "synthetic",

@@ -393,6 +393,7 @@ size_t bwd_smem_bytes(int64_t chunk_len, int dstate) {
 }
 
 cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s) {
+  if (bwd_tiled_eligible(p, bf16)) return launch_bwd_tiled(p, bf16, s);
   if (bf16) return p.fwd.z ? launch_tg<__nv_bfloat16, true>(p, s) : launch_tg<__nv_bfloat16, false>(p, s);
   return p.fwd.z ? launch_tg<float, true>(p, s) : launch_tg<float, false>(p, s);
 }

@@ -65,6 +65,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+bool tma_encode_available() { return encode_fn() != nullptr; }
+
 // 3-D map over a [batch, seqlen, inner] tensor with a box of {box_inner, box_t, 1}.
 bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_t L, int64_t batch,
               int box_inner, int box_t) {

@@ -803,6 +803,7 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_
               int box_inner, int box_t);
 unsigned int* error_word();
 int max_dynamic_smem();
+bool tma_encode_available();  // the driver's tensor-map encoder was found
 
 template <class K>
 int stage_bytes(int warps) {

@@ -56,6 +56,10 @@ cudaError_t launch_decode(const DecodeParams& p, bool bf16, cudaStream_t s);
 // chunk boundary states.
 cudaError_t launch_bwd(const BwdParams& p, bool bf16, cudaStream_t s);
 size_t bwd_smem_bytes(int64_t chunk_len, int dstate);
+// Its TMA-tiled form (16, 32 or 64 states, chunks a multiple of 16 steps,
+// 16-byte aligned buffers); launch_bwd takes it whenever it is eligible.
+bool bwd_tiled_eligible(const BwdParams& p, bool bf16);
+cudaError_t launch_bwd_tiled(const BwdParams& p, bool bf16, cudaStream_t s);
 
 // One thread runs a bounded wait on an mbarrier nothing arrives on, gives up
 // after `polls` polls and sets the sticky error word (test of the error path).

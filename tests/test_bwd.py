@@ -6,6 +6,12 @@ adds the summed gradients (dA over batch and steps, dB and dC over channels,
 dD) with fp32 atomics in no fixed order, so 1e-4 for every fp32 result, and
 1e-2 for gradients stored in bf16 (dx, ddelta, dz with bf16 I/O: rounding of
 the stored value, as for the forward's y).
+
+Two kernels serve the backward: the TMA-tiled one for 16, 32 or 64 states,
+chunks a multiple of 16 steps and 16-byte aligned buffers (every case below
+that meets those), and the generic one for the rest (chunks of 1, 7, 100;
+N of 1, 2, 8), which the ``misaligned`` variant also forces on tiled shapes
+by placing x 4 (or 2) bytes past a 16-byte boundary.
 """
 import numpy as np
 import pytest
@@ -14,7 +20,7 @@ import torch
 import selective_state_space_fwd_gb300 as S
 from selective_state_space_fwd_gb300 import workloads as W
 
-from test_parity import _edge, rel_err, to_f64
+from test_parity import _edge, _poison_padding, rel_err, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -41,13 +47,35 @@ CASES = {
     # chunks of exactly one replay piece: the chunk states are the checkpoints
     "fp32-gate-mask-chunk16": dict(e=dict(batch=2, L=100, dim=24, N=16, gate=True,
                                           mask=[100, 37]), chunk=16, h0=True),
+    # tiled: several channel blocks with a ragged last one, ragged L, valid
+    # lengths inside a piece, on a piece boundary and zero
+    "fp32-n16-mask-h0-chunk64": dict(e=dict(batch=4, L=333, dim=72, N=16,
+                                            mask=[333, 0, 170, 64]), chunk=64, h0=True),
+    "fp32-n32-gate-mask-chunk48": dict(e=dict(batch=2, L=200, dim=20, N=32, gate=True,
+                                              mask=[200, 77]), chunk=48, h0=False),
+    "bf16-n64-gate-mask-h0-chunk128": dict(e=dict(batch=2, L=300, dim=24, N=64, dtype="bf16",
+                                                  gate=True, mask=[300, 129]), chunk=128,
+                                           h0=True),
+    "bf16-n32-chunk32": dict(e=dict(batch=2, L=90, dim=48, N=32, dtype="bf16"), chunk=32,
+                             h0=False),
+    # 32 checkpoints per chunk (one CTA per SM)
+    "fp32-n16-gate-chunk512": dict(e=dict(batch=2, L=1100, dim=32, N=16, gate=True), chunk=512,
+                                   h0=True),
 }
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_backward_matches_oracle(oracle, name):
-    case = CASES[name]
+def _misaligned(t):
+    """The same values one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def _run_case(oracle, case, misalign=False, poison=False):
     inp = _edge(**case["e"])
+    if poison:
+        inp = _poison_padding(inp)
     Bt, L, Dm = inp["x"].shape
     N = inp["B"].shape[-1]
     rng = np.random.default_rng(61)
@@ -63,7 +91,8 @@ def test_backward_matches_oracle(oracle, name):
     _, states = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
                            t["valid_len"], chunk_len=case["chunk"], h0=h0t)
     dyt = W.to_torch({"dy": dy_io}, "cuda")["dy"]
-    g = S.scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
+    xt = _misaligned(t["x"]) if misalign else t["x"]
+    g = S.scan_bwd(xt, t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
                    chunk_states=states, chunk_len=case["chunk"], dy=dyt, h0=h0t,
                    want_dh0=True)
     torch.cuda.synchronize()
@@ -81,9 +110,38 @@ def test_backward_matches_oracle(oracle, name):
                                    dy=dy_ref.astype(np.float64),
                                    h0=np.zeros((Bt, Dm, N), np.float32))["dh0"]
         tol = TOL_BF16 if (bf16 and key in ("dx", "ddelta", "dz")) else TOL_F32
-        e = rel_err(to_f64(g[key]), want)
+        got = to_f64(g[key])
+        assert np.all(np.isfinite(got)), f"{key}: non-finite values"
+        e = rel_err(got, want)
         assert e <= tol, f"{key}: rel err {e:.3e} > {tol}"
     if inp["valid_len"] is not None:
         for b, v in enumerate(inp["valid_len"]):
             v = min(max(int(v), 0), L)
             assert torch.all(g["dx"][b, v:] == 0) and torch.all(g["ddelta"][b, v:] == 0)
+            if g["dz"] is not None:
+                assert torch.all(g["dz"][b, v:] == 0)
+            assert torch.all(g["dB"][b, v:] == 0) and torch.all(g["dC"][b, v:] == 0)
+    return g
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_backward_matches_oracle(oracle, name):
+    _run_case(oracle, CASES[name])
+
+
+TILED = ["fp32-n16-mask-h0-chunk64", "bf16-n64-gate-mask-h0-chunk128",
+         "fp32-n32-gate-mask-chunk48"]
+
+
+@pytest.mark.parametrize("name", TILED)
+def test_backward_generic_kernel_on_tiled_shapes(oracle, name):
+    """The generic kernel on shapes the tiled one would take (x misaligned)."""
+    _run_case(oracle, CASES[name], misalign=True)
+
+
+@pytest.mark.parametrize("name", TILED)
+@pytest.mark.parametrize("misalign", [False, True])
+def test_backward_ignores_padding(oracle, name, misalign):
+    """NaN and infinities at every step past valid_len of x, delta, z, B and C
+    reach no gradient (padded steps are the identity, [P1] s2.3)."""
+    _run_case(oracle, CASES[name], misalign=misalign, poison=True)
