@@ -225,22 +225,15 @@ __global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
   int pending = Lv > 0 ? 2 : 0;
   int inflight = 0;
   bool bad = false;
-  float dt_next = row < Lv ? __bfloat162float(dg[(b * L + row) * H + h]) : 0.f;
-  for (int64_t t0 = 0; t0 < L; t0 += Q) {
-    const int64_t t = t0 + row;
-    const bool in = t < Lv;
-    const int64_t grow = b * L + t;
-    if (t0 >= Lv) {
-      if (t < L) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(yg + grow * Dm + h * P + (c0 + c) * 8) = make_uint4(0, 0, 0, 0);
-      }
-      continue;
-    }
-    const bool more = t0 + Q < Lv;
-    const float dt = dt_next;
-    dt_next = t + Q < Lv ? __bfloat162float(dg[(grow + Q) * H + h]) : 0.f;
+  // The running sum of delta A over a block (log2 units) and the factors
+  // derived from it, for row `row`: cs, e = cs - log2(delta), the column
+  // factor toward the block's last step of the row's 32-step part, u =
+  // delta 2^(cs_end - cs), and the block total.  A block's values are
+  // computed while the previous block's second product runs.
+  struct Scan {
+    float cs, e, colf, u, tot;
+  };
+  auto scan_block = [&](float dt) {
     float cs = dt * al;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -257,9 +250,54 @@ __global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
       tot += v;
     }
     cs += pre;
-    const float e = cs - lg2(dt);
-    const float colf = dt * ex2(__shfl_sync(0xFFFFFFFFu, cs, 31) - cs);
-    const float u = dt * ex2(tot - cs);
+    Scan r;
+    r.cs = cs;
+    r.e = cs - lg2(dt);
+    r.colf = dt * ex2(__shfl_sync(0xFFFFFFFFu, cs, 31) - cs);
+    r.u = dt * ex2(tot - cs);
+    r.tot = tot;
+    return r;
+  };
+  float dt_next = row < Lv ? __bfloat162float(dg[(b * L + row) * H + h]) : 0.f;
+  Scan nxt = scan_block(dt_next);
+  dt_next = row + Q < Lv ? __bfloat162float(dg[(b * L + row + Q) * H + h]) : 0.f;
+  for (int64_t t0 = 0; t0 < L; t0 += Q) {
+    const int64_t t = t0 + row;
+    const bool in = t < Lv;
+    const int64_t grow = b * L + t;
+    if (t0 >= Lv) {
+      if (t < L) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(yg + grow * Dm + h * P + (c0 + c) * 8) = make_uint4(0, 0, 0, 0);
+      }
+      continue;
+    }
+    const bool more = t0 + Q < Lv;
+    const Scan cur = nxt;
+    const float cs = cur.cs;
+
+    {  // this thread's halves of the state rows: bf16 operand of Yo; kept scaled by
+       // 2^cs_end (needs only the previous block's products, not this block's copies)
+      const float etot = ex2(cur.tot);
+#pragma unroll
+      for (int jh = 0; jh < NH; ++jh) {
+        uint32_t r0[32];
+        umma::tmem_ld32_async(tl + kColS + 64 * jh + hf * 32, r0);
+        umma::tmem_wait_ld(r0);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
+          sts128(sm, kTileS + (c0 + c) * kStripS + (row + 128 * jh) * 16, pack8(f));
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
+        umma::tmem_st32(tl + kColS + 64 * jh + hf * 32, r0);
+      }
+      umma::tmem_wait_st();
+    }
 
     if (umma::mbar_wait(tbar, tphase, kSsdWaitLimit)) {
       tphase ^= 1;
@@ -285,28 +323,8 @@ __global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
       float f[8];
       unpack8(xr[c], f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] *= u;
+      for (int j = 0; j < 8; ++j) f[j] *= cur.u;
       sts128(sm, kTileXw + (c0 + c) * kStrip + rowo, pack8(f));
-    }
-    {  // this thread's halves of the state rows: bf16 operand of Yo; kept scaled by 2^cs_end
-      const float etot = ex2(tot);
-#pragma unroll
-      for (int jh = 0; jh < NH; ++jh) {
-        uint32_t r0[32];
-        umma::tmem_ld32_async(tl + kColS + 64 * jh + hf * 32, r0);
-        umma::tmem_wait_ld(r0);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float f[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r0[c * 8 + j]);
-          sts128(sm, kTileS + (c0 + c) * kStripS + (row + 128 * jh) * 16, pack8(f));
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r0[j] = __float_as_uint(__uint_as_float(r0[j]) * etot);
-        umma::tmem_st32(tl + kColS + 64 * jh + hf * 32, r0);
-      }
-      umma::tmem_wait_st();
     }
     umma::fence_smem_to_async();
     umma::fence_before_sync();
@@ -357,8 +375,8 @@ __global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
       if (tid == 0) copy_c(t0 + Q);
     }
     if (hf == 0) {
-      sE[row] = e;
-      sF[row] = colf;
+      sE[row] = cur.e;
+      sF[row] = cur.colf;
     }
     __syncthreads();
 
@@ -432,6 +450,10 @@ __global__ void __launch_bounds__(2 * kThreads, SsdCfg<NS>::kMinBlocks)
     if (tid == 32) umma::mbar_arrive(bar);
     __syncwarp();
     inflight = 1;
+    if (more) {  // the next block's running sums, while the product runs
+      nxt = scan_block(dt_next);
+      dt_next = t + 2 * Q < Lv ? __bfloat162float(dg[(grow + 2 * Q) * H + h]) : 0.f;
+    }
     if (umma::mbar_wait(bar, phase, kSsdWaitLimit)) {
       phase ^= 1;
       --inflight;
