@@ -375,17 +375,35 @@ __global__ void __launch_bounds__(kThreads, 2)
           hs[k + 1][q] = fma2(a2[k][q], hs[k][q], mul2(ux2, B2[q]));
         }
       }
-      // the adjoint back over the piece
+      // the adjoint back over the piece.  A step's inputs are loaded one step
+      // ahead (before the previous step's warp barrier, which the compiler
+      // does not move loads across), so their shared-memory latency overlaps
+      // that step's arithmetic.
+      struct In {
+        float dt, x, dy, z;
+        u64 B2[2], C2[2];
+      };
+      auto load_in = [&](int k) {
+        In v;
+        v.dt = f32_of(ds[k * CPB]);
+        v.x = f32_of(xs[k * CPB]);
+        v.dy = f32_of(ys[k * CPB]);
+        v.z = K::GATE ? f32_of(zs[k * CPB]) : 0.f;
+        row4(bs + k * N, v.B2[0], v.B2[1]);
+        row4(cs + k * N, v.C2[0], v.C2[1]);
+        return v;
+      };
+      In nxt = load_in(kK - 1);
 #pragma unroll
       for (int k = kK - 1; k >= 0; --k) {
-        const float dt = f32_of(ds[k * CPB]), x = f32_of(xs[k * CPB]);
-        const float dy = f32_of(ys[k * CPB]);
-        u64 B2[2], C2[2];
-        row4(bs + k * N, B2[0], B2[1]);
-        row4(cs + k * N, C2[0], C2[1]);
+        const In cur = nxt;
+        if (k > 0) nxt = load_in(k - 1);
+        const float dt = cur.dt, x = cur.x, dy = cur.dy;
+        const u64(&B2)[2] = cur.B2;
+        const u64(&C2)[2] = cur.C2;
         float dyp = dy, z = 0.f, sg = 0.f;
         if constexpr (K::GATE) {
-          z = f32_of(zs[k * CPB]);
+          z = cur.z;
           sg = __fdividef(1.f, 1.f + ex2(-z * kLog2e));
           dyp = dy * z * sg;  // dy silu(z)
         }
