@@ -454,10 +454,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncwarp();
 #pragma unroll
         for (int o = 0; o < K::OPL; ++o) {
-          float s = 0.f;
+          float v[CWB];  // summed as a tree: short dependency chains
 #pragma unroll
-          for (int c2 = 0; c2 < CWB; ++c2) s += xbuf[c2 * K::XS + lane + 32 * o];
-          red[(k * kW + warp) * 2 * N + lane + 32 * o] = s;
+          for (int c2 = 0; c2 < CWB; ++c2) v[c2] = xbuf[c2 * K::XS + lane + 32 * o];
+#pragma unroll
+          for (int w = CWB / 2; w >= 1; w /= 2)
+#pragma unroll
+            for (int i = 0; i < w; ++i) v[i] += v[i + w];
+          red[(k * kW + warp) * 2 * N + lane + 32 * o] = v[0];
         }
         __syncwarp();
       }
