@@ -61,6 +61,8 @@ CASES = {
     # 32 checkpoints per chunk (one CTA per SM)
     "fp32-n16-gate-chunk512": dict(e=dict(batch=2, L=1100, dim=32, N=16, gate=True), chunk=512,
                                    h0=True),
+    "fp32-n64-mask-chunk512": dict(e=dict(batch=2, L=1030, dim=16, N=64, mask=[1030, 517]),
+                                   chunk=512, h0=True),
 }
 
 
