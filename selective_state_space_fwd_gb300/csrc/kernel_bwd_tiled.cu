@@ -13,7 +13,8 @@
 // * A first pass over the chunk keeps the state before every 16-step piece in
 //   shared memory.  Each piece is then replayed once more with its 16 decays
 //   and 17 states held in registers, and the adjoint runs back over it from
-//   those registers: the reverse step takes no exponential.
+//   those registers: the reverse step recomputes no decay (with the gate it
+//   still takes the sigmoid of z).
 // * dx, d delta and dz of a piece are written to shared-memory tiles and
 //   leave by TMA store.
 // * dB and dC (sums over channels) are reduced in two levels before any
