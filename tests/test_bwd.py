@@ -147,3 +147,34 @@ def test_backward_ignores_padding(oracle, name, misalign):
     """NaN and infinities at every step past valid_len of x, delta, z, B and C
     reach no gradient (padded steps are the identity, [P1] s2.3)."""
     _run_case(oracle, CASES[name], misalign=misalign, poison=True)
+
+
+@pytest.mark.parametrize("key", [2, 3, 4])
+def test_backward_full_size_whole_tensor(oracle, key):
+    """Every gradient of the full-size workloads (the bench's chunk of 256 steps)
+    against the oracle's backward, whole tensors."""
+    w = W.WORKLOADS[key]
+    chunk = 256
+    inp = W.make_inputs(w)
+    Bt, L, Dm = inp["x"].shape
+    rng = np.random.default_rng(62)
+    dy = rng.standard_normal((Bt, L, Dm)).astype(np.float32)
+    bf16 = inp["dtype"] == "bf16"
+    dy_io = W.f32_to_bf16_bits(dy) if bf16 else dy
+    dy_ref = W.bf16_bits_to_f32(dy_io) if bf16 else dy
+    t = W.to_torch(inp, "cuda")
+    _, states = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                           t["valid_len"], chunk_len=chunk)
+    dyt = W.to_torch({"dy": dy_io}, "cuda")["dy"]
+    g = S.scan_bwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["valid_len"],
+                   chunk_states=states, chunk_len=chunk, dy=dyt)
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    got = {k: to_f64(v) for k, v in g.items() if v is not None}
+    del g, t, states, dyt
+    ref = oracle.scan_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["z"], inp["valid_len"], dy=dy_ref.astype(np.float64))
+    for key_g, v in got.items():
+        tol = TOL_BF16 if (bf16 and key_g in ("dx", "ddelta", "dz")) else TOL_F32
+        e = rel_err(v, ref[key_g])
+        assert e <= tol, f"workload {key}: {key_g} rel err {e:.3e} > {tol}"

@@ -117,3 +117,24 @@ def test_scan_fwd_routes_few_channel_rows_through_the_split(oracle):
                                    None, inp["valid_len"], chunk_len=w.chunk_len)
     for yy, ss in ((y, s), (y1, s1)):
         assert _rel(_f64(yy), y_ref) <= 1e-5 and _rel(_f64(ss), s_ref) <= 1e-5
+
+
+@pytest.mark.parametrize("key", sorted(W.SPLIT_WORKLOADS))
+def test_split_full_size_whole_tensor(oracle, key):
+    """The split workloads at full size through scan_fwd (which takes the time
+    split for them), whole y and final state against the oracle."""
+    w = W.SPLIT_WORKLOADS[key]
+    inp = W.make_inputs(w)
+    segs, _ = S.split_plan(w.batch, w.seqlen, w.dim, w.dstate)
+    assert segs > 1
+    t = W.to_torch(inp, "cuda")
+    y, _, fin = S.scan_fwd_split(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                                 t["valid_len"], time_segments=0, want_final=True)
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    yg, fg = _f64(y), _f64(fin)
+    del y, fin, t
+    y_ref, _, f_ref = oracle.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                      inp["D"], inp["z"], inp["valid_len"], want_final=True)
+    assert _rel(yg, y_ref) <= TOL_Y[w.dtype]
+    assert _rel(fg, f_ref) <= TOL_STATES
