@@ -85,3 +85,21 @@ def test_prefill_then_decode_follows_the_scan(oracle, name):
     assert e <= TOL_Y[inp["dtype"]], f"y rel err {e:.3e}"
     es = rel_err(to_f64(state), f_ref)
     assert es <= TOL_STATES, f"final state rel err {es:.3e}"
+
+
+@pytest.mark.parametrize("key", sorted(W.DECODE_WORKLOADS))
+def test_decode_full_size_whole_tensor(oracle, key):
+    """One decode step of the benchmark's decode workloads (batch 1024, dim
+    2048, 16 states) from the workload's state, whole y and state against the
+    oracle's scan of one step."""
+    w = W.DECODE_WORKLOADS[key]
+    inp = W.make_inputs(w)
+    h0 = W.make_state(w)
+    y_ref, _, f_ref = oracle.scan_fwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                      inp["D"], inp["z"], None, h0=h0, want_final=True)
+    state = torch.from_numpy(h0.copy()).cuda()
+    y = _gpu_step(_step_inputs(inp, 0), inp["A"], inp["D"], state)
+    torch.cuda.synchronize()
+    e = rel_err(to_f64(y), y_ref[:, 0])
+    assert e <= TOL_Y[inp["dtype"]], f"y rel err {e:.3e}"
+    assert rel_err(to_f64(state), f_ref) <= TOL_STATES

@@ -119,3 +119,30 @@ def test_decode_with_prepared_delta_follows_the_scan(oracle):
     e = rel_err(np.concatenate(ys, axis=1), y_ref)
     assert e <= TOL_Y["f32"], f"y rel err {e:.3e}"
     assert rel_err(to_f64(state), f_ref) <= TOL_STATES
+
+
+@pytest.mark.parametrize("key", [2, 3])
+def test_fused_delta_full_size_whole_tensor(oracle, key):
+    """The benchmark's fused-preparation configuration at full size (raw delta
+    and dt_bias from the workload's recipe), whole y and chunk states against
+    the oracle."""
+    w = W.WORKLOADS[key]
+    inp = W.make_inputs(w)
+    raw, bias = W.make_raw_delta(w)
+    inp["delta"] = raw
+    t = W.to_torch(inp, "cuda")
+    y, s = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                      t["valid_len"], chunk_len=w.chunk_len,
+                      dt_bias=torch.from_numpy(bias).cuda(), delta_softplus=True)
+    torch.cuda.synchronize()
+    S.check_device_errors()
+    yg = to_f64(y)
+    sg = to_f64(s) if s is not None else None
+    del y, s, t
+    y_ref, s_ref = oracle.scan_fwd(inp["x"], raw, inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["z"], inp["valid_len"], chunk_len=w.chunk_len,
+                                   dt_bias=bias, delta_softplus=True)
+    e = rel_err(yg, y_ref)
+    assert e <= TOL_Y[w.dtype], f"workload {key}: y rel err {e:.3e}"
+    if s_ref is not None:
+        assert rel_err(sg, s_ref) <= TOL_STATES
