@@ -103,3 +103,32 @@ def test_decode_full_size_whole_tensor(oracle, key):
     e = rel_err(to_f64(y), y_ref[:, 0])
     assert e <= TOL_Y[inp["dtype"]], f"y rel err {e:.3e}"
     assert rel_err(to_f64(state), f_ref) <= TOL_STATES
+
+
+def _offset(t):
+    """The same values one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("name", ["fp32-n16", "bf16-n64-gate"])
+def test_decode_with_unaligned_rows(oracle, name):
+    """B and C rows that do not start on a 16-byte boundary (the entry point
+    requires only their element alignment) take element loads."""
+    inp = _edge(**CASES[name])
+    Bt, L, Dm = inp["x"].shape
+    N = inp["B"].shape[-1]
+    h0 = np.random.default_rng(6).standard_normal((Bt, Dm, N)).astype(np.float32)
+    one = {k: (v[:, :1] if isinstance(v, np.ndarray) and v.ndim == 3 else v) for k, v in inp.items()}
+    y_ref, _, f_ref = oracle.scan_fwd(one["x"], one["delta"], inp["A"], one["B"], one["C"],
+                                      inp["D"], one["z"], None, h0=h0, want_final=True)
+    step = _step_inputs(inp, 0)
+    cv = lambda a: None if a is None else W.to_torch({"v": a}, "cuda")["v"]
+    state = torch.from_numpy(h0.copy()).cuda()
+    y = S.decode_step(cv(step["x"]), cv(step["delta"]), cv(inp["A"]), _offset(cv(step["B"])),
+                      _offset(cv(step["C"])), cv(inp["D"]), cv(step["z"]), state=state)
+    torch.cuda.synchronize()
+    assert rel_err(to_f64(y), y_ref[:, 0]) <= TOL_Y[inp["dtype"]]
+    assert rel_err(to_f64(state), f_ref) <= TOL_STATES
