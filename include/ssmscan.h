@@ -226,6 +226,11 @@ ssm_status ssm_decode_step_prep(const void* x, const void* delta, const ssm_delt
  *                  the state before the first step.
  * Steps past valid_len get zero gradients.  The summed outputs are added with
  * atomics: their last bits depend on the order.  Asynchronous on `stream`.
+ * Kernel: with dstate 16, 32 or 64, chunk_len a multiple of 16, dim times the
+ * element size a multiple of 16 bytes and every tensor 16-byte aligned, a
+ * TMA-tiled kernel (the decays of each 16-step piece kept in registers, dB and
+ * dC reduced in shared memory before the atomics); otherwise a generic kernel
+ * with the same results within the same tolerance.
  */
 ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A, const void* B,
                         const void* C, const float* D, const void* z,
