@@ -243,6 +243,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="--op decode: also time consecutive steps captured in a CUDA graph "
+                         "against the same steps launched one by one (no L2 flush: the steps "
+                         "of one generation loop)")
     ap.add_argument("--fused-delta", action="store_true",
                     help="softplus workloads: pass the raw step inputs and dt_bias and let the "
                          "kernel apply softplus(raw + dt_bias)")
@@ -475,6 +479,37 @@ def decode_main(args):
     per_step = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     ms = sum(per_step) / K
     c = decode_counts(w)
+    graph = None
+    if args.graph:
+        # consecutive steps of one generation loop, back to back: launched one
+        # by one through the binding, and captured once into a CUDA graph
+        G, R = 64, 8
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for _ in range(G * R):
+                step()
+            g1.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_ms = g0.elapsed_time(g1) / (G * R)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(cg, stream=stream):
+                for _ in range(G):
+                    step()
+            for _ in range(3):
+                cg.replay()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for _ in range(R):
+                cg.replay()
+            g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph = {"steps_per_graph": G, "replays": R, "ms_per_step": g0.elapsed_time(g1) / (G * R),
+                 "eager_ms_per_step": eager_ms,
+                 "l2": "not flushed (consecutive steps of one generation loop)"}
     # end to end: the step's inputs from pinned host memory, y back, every step
     th = {k: (v.reshape(w.batch, -1).cpu().pin_memory() if v is not None else None)
           for k, v in flat.items()}
@@ -526,6 +561,8 @@ def decode_main(args):
         "per_step_ms": {"min": min(per_step), "median": statistics.median(per_step),
                         "max": max(per_step)},
     }
+    if graph is not None:
+        line["graph"] = graph
     print(json.dumps(line), flush=True)
 
 

@@ -40,6 +40,12 @@
  *     any launch and are returned as a status; nothing is launched then.  A
  *     launch failure is returned as SSM_ERR_CUDA (cudaGetLastError() tells
  *     which).  No entry point aborts, throws or traps.
+ *   - `stream` must belong to the calling thread's current device (checked,
+ *     SSM_ERR_CUDA otherwise), except while it is being captured into a CUDA
+ *     graph: the device entry points (forward, split, backward, decode, SSD)
+ *     then only record their work, and the captured graph replays it.  Make one
+ *     call of each shape outside the capture first (it performs the library's
+ *     one-time lookups).
  *   - Inputs and outputs must not overlap.
  */
 #ifndef SSMSCAN_H_

@@ -172,6 +172,11 @@ ssm_status current_device_for(cudaStream_t stream, int* dev) {
   if (cudaGetDevice(dev) != cudaSuccess) return SSM_ERR_CUDA;
   if (stream == nullptr || stream == cudaStreamLegacy || stream == cudaStreamPerThread)
     return SSM_OK;
+  // A stream being captured into a CUDA graph is not queried for its device
+  // (the query would invalidate the capture); the calls then only record work.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SSM_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return SSM_OK;
   int sdev = -1;
   if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return SSM_ERR_CUDA;
   return sdev == *dev ? SSM_OK : SSM_ERR_CUDA;

@@ -97,6 +97,10 @@ DECODE_WORKLOADS = {
                 "s4d_exp", "normal", False, None, 0, 11),
     2: Workload(102, "decode-bf16-gated-b1024-d2048-n16", 1024, 1, 2048, 16, "bf16",
                 "softplus", "s4d_exp", "normal", True, None, 0, 12),
+    # one sequence's step of a generation loop: a 128 KB state, bound by launch
+    # latency rather than HBM
+    3: Workload(103, "decode-fp32-b1-d2048-n16", 1, 1, 2048, 16, "f32", "softplus",
+                "s4d_exp", "normal", False, None, 0, 13),
 }
 
 
