@@ -44,6 +44,9 @@ CASES = {
     "fp32-n2-gate": dict(batch=2, L=20, dim=8, N=2, gate=True),
     "bf16-n64-gate": dict(batch=2, L=24, dim=24, N=64, dtype="bf16", gate=True),
     "bf16-n8": dict(batch=4, L=16, dim=64, N=8, dtype="bf16"),
+    # bf16 with 16 states stores the outputs of channel pairs together; an odd
+    # batch * dim leaves the last output alone
+    "bf16-n16-gate-odd": dict(batch=3, L=10, dim=33, N=16, dtype="bf16", gate=True),
 }
 
 
