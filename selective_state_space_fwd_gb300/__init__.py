@@ -10,11 +10,12 @@ from ._binding import (Kernel, SsmError, Status, check_device_errors, chunk_coun
                        scan_fwd_host_static, scan_fwd_split, selftest_wait_timeout, split_plan,
                        ssd_fwd, static_capacity,
                        status_string, version)
+from .autograd import selective_scan
 
 __all__ = ["Kernel", "SsmError", "Status", "check_device_errors", "chunk_count", "decode_step",
            "declared_functions",
            "host_workspace_bytes", "kernel_name", "load", "plan", "scan_bwd", "scan_fwd",
            "scan_fwd_host", "scan_fwd_host_static", "scan_fwd_split", "selftest_wait_timeout",
-           "split_plan", "ssd_fwd",
+           "selective_scan", "split_plan", "ssd_fwd",
            "static_capacity",
            "status_string", "version"]
