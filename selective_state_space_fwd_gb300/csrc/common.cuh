@@ -168,4 +168,29 @@ __device__ __forceinline__ int64_t valid_steps(const ScanParams& p, int64_t b) {
   return v < 0 ? 0 : (v > p.seqlen ? p.seqlen : v);
 }
 
+// Rows of a batch with valid lengths are handed to the CTAs longest first: a
+// CTA's work is proportional to its row's valid steps, and CTAs start in
+// index order, so the long rows start first and the short ones fill the end
+// (longest processing time first).  The order is computed for batches of up
+// to 32 rows (one row per lane); larger batches keep the index order.
+__device__ __forceinline__ bool rows_ranked(const ScanParams& p) {
+  return p.valid_len != nullptr && p.batch <= 32;
+}
+// The row of rank r in the order of decreasing valid steps (ties by index),
+// computed by the calling warp (all 32 lanes, converged): lane l ranks row l
+// against every row's length, passed around by shuffles.
+__device__ __forceinline__ int64_t row_of_rank(const ScanParams& p, int64_t r) {
+  const int lane = threadIdx.x & 31;
+  const int nb = static_cast<int>(p.batch);
+  const int64_t len = lane < nb ? valid_steps(p, lane) : -1;
+  int rank = 0;
+#pragma unroll 1
+  for (int j = 0; j < nb; ++j) {
+    const int64_t lj = __shfl_sync(0xffffffffu, len, j);
+    rank += lj > len || (lj == len && j < lane);
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, lane < nb && rank == r);
+  return m != 0u ? __ffs(m) - 1 : r;
+}
+
 }  // namespace ssm

@@ -278,7 +278,8 @@ constexpr int pad_prow(int NG, int CW, int R, int PS) {
 }
 
 // Compile-time shape of one STREAM instance.
-template <int N_, int G_, int R_, typename IO_, bool GATE_, bool DTP_ = false, bool AGG_ = false>
+template <int N_, int G_, int R_, typename IO_, bool GATE_, bool DTP_ = false, bool AGG_ = false,
+          bool RANK_ = false>
 struct Cfg {
   static constexpr int N = N_, G = G_, R = R_;
   static constexpr bool GATE = GATE_;
@@ -290,6 +291,9 @@ struct Cfg {
   // per tile over the warp's delta slab; for fp32 in place, for bf16 into an
   // fp32 slab of the warp (the prepared step is not rounded to bf16).
   static constexpr bool DTP = DTP_;
+  // RANK: the batch rows have valid lengths and are handed to the CTAs
+  // longest first (rows_ranked, row_of_rank in common.cuh)
+  static constexpr bool RANK = RANK_;
   using IO = IO_;
   static constexpr int PR = R / 2;           // channel pairs per lane
   static constexpr int NG = N / G;           // lanes per channel group
@@ -327,6 +331,7 @@ struct Cfg {
   static_assert(PROW % 4 == 0 && PS % 4 == 0 && PBYTES <= 12 * 1024, "partial buffer");
   static_assert(SLAB % 128 == 0 && ROWT % 128 == 0, "slot alignment");
   static_assert(!(AGG && (DTP || GATE)), "the aggregate pass takes delta as given and has no gate");
+  static_assert(!(AGG && RANK), "the aggregate pass runs segments, not ranked rows");
 };
 
 // One batch of U steps' inputs for this lane, as loaded from the tile.
@@ -414,7 +419,11 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpc = W * CW;
   const int64_t n_cb = (p.dim + cpc - 1) / cpc;
-  const int64_t row = blockIdx.x / n_cb;  // (batch row, segment of the time split)
+  // (batch row, segment of the time split); ranked instances take the rows
+  // longest first
+  const int64_t row = K::RANK && p.n_seg == 1 && rows_ranked(p)
+                          ? row_of_rank(p, blockIdx.x / n_cb)
+                          : blockIdx.x / n_cb;
   const int64_t b = row / p.n_seg;
   const int seg = static_cast<int>(row % p.n_seg);
   if (K::AGG && seg == p.n_seg - 1) return;  // the last segment's aggregate is not needed
@@ -867,17 +876,17 @@ constexpr bool bf16_ok() {
   return N * 2 >= 16 && (32 / (N / G)) * R * 2 % 16 == 0;
 }
 
-template <int N, int G, int R, bool DTP>
+template <int N, int G, int R, bool DTP, bool RANK>
 cudaError_t launch_ngr_dtp(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
   if (bf16) {
     if constexpr (bf16_ok<N, G, R>())
-      return p.z ? launch_k<Cfg<N, G, R, __nv_bfloat16, true, DTP>>(p, s, w, st)
-                 : launch_k<Cfg<N, G, R, __nv_bfloat16, false, DTP>>(p, s, w, st);
+      return p.z ? launch_k<Cfg<N, G, R, __nv_bfloat16, true, DTP, false, RANK>>(p, s, w, st)
+                 : launch_k<Cfg<N, G, R, __nv_bfloat16, false, DTP, false, RANK>>(p, s, w, st);
     else
       return cudaErrorInvalidValue;
   }
-  return p.z ? launch_k<Cfg<N, G, R, float, true, DTP>>(p, s, w, st)
-             : launch_k<Cfg<N, G, R, float, false, DTP>>(p, s, w, st);
+  return p.z ? launch_k<Cfg<N, G, R, float, true, DTP, false, RANK>>(p, s, w, st)
+             : launch_k<Cfg<N, G, R, float, false, DTP, false, RANK>>(p, s, w, st);
 }
 
 // Shapes compiled with the fused step-size preparation: the default ones.
@@ -887,13 +896,18 @@ constexpr bool dtp_shape(int n, int g, int r) {
 
 template <int N, int G, int R>
 cudaError_t launch_ngr_impl(const ScanParams& p, bool bf16, cudaStream_t s, int w, int st) {
+  // ranked instances exist for the default shapes (the host side of rows_ranked)
+  const bool rank = p.valid_len != nullptr && p.batch <= 32 && p.n_seg == 1;
   if (has_delta_prep(p)) {
     if constexpr (dtp_shape(N, G, R))
-      return launch_ngr_dtp<N, G, R, true>(p, bf16, s, w, st);
+      return rank ? launch_ngr_dtp<N, G, R, true, true>(p, bf16, s, w, st)
+                  : launch_ngr_dtp<N, G, R, true, false>(p, bf16, s, w, st);
     else
       return cudaErrorInvalidValue;
   }
-  return launch_ngr_dtp<N, G, R, false>(p, bf16, s, w, st);
+  if constexpr (dtp_shape(N, G, R))
+    if (rank) return launch_ngr_dtp<N, G, R, false, true>(p, bf16, s, w, st);
+  return launch_ngr_dtp<N, G, R, false, false>(p, bf16, s, w, st);
 }
 
 template <int N, int G, int R>

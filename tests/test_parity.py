@@ -329,3 +329,24 @@ def test_full_size_whole_tensor(oracle, key):
     if s is not None:
         es = rel_err(to_f64(s), s_ref)
         assert es <= TOL_STATES, f"workload {key}: state rel err {es:.3e}"
+
+
+def test_length_ranked_rows_change_nothing_but_the_order():
+    """Batches of at most 32 rows with valid lengths run their rows longest
+    first; larger ones in index order.  The assignment of rows to CTAs is the
+    only difference: the first 32 rows of a 33-row batch equal, bit for bit,
+    the same 32 rows run as a batch of their own."""
+    w = W.WORKLOADS[4].scaled(batch=33, seqlen=600, dim=48)
+    inp = W.make_inputs(w)
+    inp["valid_len"] = np.random.default_rng(9).integers(0, 700, size=33).astype(np.int32)
+    t = W.to_torch(inp, "cuda")
+    y33, s33 = S.scan_fwd(t["x"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"],
+                          t["valid_len"], chunk_len=w.chunk_len, time_segments=1)
+    sl = lambda v: v[:32].contiguous() if v is not None else None
+    y32, s32 = S.scan_fwd(sl(t["x"]), sl(t["delta"]), t["A"], sl(t["B"]), sl(t["C"]), t["D"],
+                          sl(t["z"]), sl(t["valid_len"]), chunk_len=w.chunk_len,
+                          time_segments=1)
+    torch.cuda.synchronize()
+    assert torch.equal(y33[:32], y32)
+    if s33 is not None:
+        assert torch.equal(s33[:32], s32)
