@@ -50,11 +50,13 @@ constexpr int kW = 4;         // warps per CTA
 constexpr int kThreads = 32 * kW;
 constexpr int kSmemPerSm = 228 * 1024;
 
-template <int N_, typename T_, bool GATE_>
+template <int N_, typename T_, bool GATE_, bool RANK_ = false>
 struct Cfg {
   static constexpr int N = N_;
   using T = T_;
   static constexpr bool GATE = GATE_;
+  // RANK: rows with valid lengths taken longest first (rows_ranked, row_of_rank)
+  static constexpr bool RANK = RANK_;
   static constexpr int G = 4;              // states per thread
   static constexpr int NL = N / G;         // threads per channel
   static constexpr int CWB = 32 / NL;      // channels per warp
@@ -188,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* empty = full + S;
 
   const int64_t nblk = (D_ + CPB - 1) / CPB;
-  const int b = static_cast<int>(blockIdx.x / nblk);
+  const int b = static_cast<int>(K::RANK && rows_ranked(p.fwd) ? row_of_rank(p.fwd, blockIdx.x / nblk)
+                                                                : blockIdx.x / nblk);
   const int d0 = static_cast<int>((blockIdx.x % nblk) * CPB);
   const int ch = lane / NL, sl = lane % NL, n0 = sl * 4;
   const int cc = warp * CWB + ch;  // the thread's channel within the CTA's block
@@ -574,10 +577,12 @@ cudaError_t launch_k(const BwdParams& p, cudaStream_t s) {
 
 template <typename T, bool GATE>
 cudaError_t launch_tg(const BwdParams& p, cudaStream_t s) {
+  // rows with valid lengths run longest first (the host side of rows_ranked)
+  const bool rank = p.fwd.valid_len != nullptr && p.fwd.batch <= 32;
   switch (p.fwd.dstate) {
-    case 16: return launch_k<Cfg<16, T, GATE>>(p, s);
-    case 32: return launch_k<Cfg<32, T, GATE>>(p, s);
-    case 64: return launch_k<Cfg<64, T, GATE>>(p, s);
+    case 16: return rank ? launch_k<Cfg<16, T, GATE, true>>(p, s) : launch_k<Cfg<16, T, GATE>>(p, s);
+    case 32: return rank ? launch_k<Cfg<32, T, GATE, true>>(p, s) : launch_k<Cfg<32, T, GATE>>(p, s);
+    case 64: return rank ? launch_k<Cfg<64, T, GATE, true>>(p, s) : launch_k<Cfg<64, T, GATE>>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }
