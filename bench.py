@@ -1212,8 +1212,9 @@ def main():
                 "ms_per_step": rk["ms"], "value": ck["elements"] / (rk["ms"] * 1e-3),
                 "unit": UNIT, "valid_elements_per_s": ck["valid_elements"] / (rk["ms"] * 1e-3),
                 "kernel": S.kernel_name(kk), "clocks": rk["clocks"],
-                "roofline": {k: rlk[k] for k in ("bound", "achieved", "peak", "unit", "frac",
-                                                 "frac_of_roof", "roof_us")},
+                "roofline": dict({k: rlk[k] for k in ("bound", "achieved", "peak", "unit",
+                                                      "frac", "frac_of_roof", "roof_us")},
+                                 traffic=measured_traffic(S.kernel_name(kk), wk.name)),
                 "gpu_launches": rk["launches"]}
             del rk, ik
             torch.cuda.empty_cache()
