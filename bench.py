@@ -240,6 +240,8 @@ def parse():
     ap.add_argument("--channels-per-lane", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-inflight", type=int, default=2,
+                    help="forward end-to-end calls in flight (own stream, workspace, outputs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-flush", action="store_true")
@@ -1141,37 +1143,54 @@ def main():
     # pinned memory, the forward, D2H of y (and chunk states), every step.
     th = W.to_torch(inp, "cpu")
     pinned = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in th.items()}
-    y_h = torch.empty(tuple(t["x"].shape), dtype=t["x"].dtype, pin_memory=True)
-    s_h = (torch.empty((wr.batch, nch, w.dim, w.dstate), dtype=torch.float32, pin_memory=True)
-           if w.chunk_len else None)
+    # NF calls in flight, as a serving loop issues them: call k runs on stream
+    # k % NF with its own workspace and output buffers, so that its copies in
+    # overlap the previous call's last kernel and copies out (the library's
+    # copy streams keep the calls' copies in order).
+    NF = max(1, args.e2e_inflight)
+    y_hs = [torch.empty(tuple(t["x"].shape), dtype=t["x"].dtype, pin_memory=True)
+            for _ in range(NF)]
+    s_hs = [torch.empty((wr.batch, nch, w.dim, w.dstate), dtype=torch.float32, pin_memory=True)
+            if w.chunk_len else None for _ in range(NF)]
+    y_h, s_h = y_hs[0], s_hs[0]
     del res, t
     torch.cuda.empty_cache()
-    ws = torch.empty(S.host_workspace_bytes(wr.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
-                                            has_D=True, gate=w.gate, mask=w.mask is not None,
-                                            chunk_len=w.chunk_len),
-                     dtype=torch.uint8, device=dev)
+    ws_bytes = S.host_workspace_bytes(wr.batch, w.seqlen, w.dim, w.dstate, dtype=w.dtype,
+                                      has_D=True, gate=w.gate, mask=w.mask is not None,
+                                      chunk_len=w.chunk_len)
+    wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(NF)]
+    streams = [stream] + [torch.cuda.Stream(dev) for _ in range(NF - 1)]
 
-    def step_host():
+    def step_host(k):
+        j = k % NF
         S.scan_fwd_host(pinned["x"], pinned["delta"], pinned["A"], pinned["B"], pinned["C"],
                         pinned["D"], pinned["z"], pinned["valid_len"], chunk_len=w.chunk_len,
-                        out=y_h, out_states=s_h, workspace=ws, stream=stream)
+                        out=y_hs[j], out_states=s_hs[j], workspace=wss[j], stream=streams[j])
 
-    for _ in range(3):
-        step_host()
+    for k in range(3 * NF):
+        step_host(k)
     torch.cuda.synchronize(dev)
     KE = max(1, args.e2e_steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(KE):
-        step_host()
+    for sj in streams[1:]:
+        sj.wait_event(e0)
+    for k in range(KE):
+        step_host(k)
+    for sj in streams[1:]:
+        stream.wait_stream(sj)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / KE, dev)
+    # every in-flight slot returned the same y as the device-timed forward
+    for yk in y_hs[1:min(NF, KE)]:
+        if not torch.equal(yk, y_h):
+            raise RuntimeError("end-to-end calls in flight returned different outputs")
     es = 2 if w.dtype == "bf16" else 4
     h2d = sum(v.numel() * v.element_size() for k, v in pinned.items()
               if isinstance(v, torch.Tensor))
     d2h = y_h.numel() * es + (s_h.numel() * 4 if s_h is not None else 0)
-    del ws, pinned, th
+    del wss, pinned, th, y_hs, s_hs
     torch.cuda.empty_cache()
 
     if rank != 0:
@@ -1241,7 +1260,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": job_rate(1 if args.split_batch else world, counts["elements"], ms_e2e),
                 "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": ms_e2e},
+                "ms_per_step": ms_e2e, "calls_in_flight": NF},
         "gpu_launches": res_launches,
         "clocks": res_clocks,
         "timed_wall_s": res_wall,

@@ -294,6 +294,35 @@ def test_host_entry_pipelined_pieces(oracle, case):
     check(inp, to_f64(y_h), None if s_h is None else to_f64(s_h), y_ref, s_ref)
 
 
+def test_host_entry_calls_in_flight():
+    """Several end-to-end calls enqueued without waiting, alternating two
+    streams and two workspaces (the calls share the library's copy streams):
+    each returns, bit for bit, what the device entry point gives for its own
+    inputs.  Consecutive calls get different inputs, so outputs that crossed
+    over between calls, or a workspace overwritten while in use, would show."""
+    case = dict(batch=2, L=8192, dim=64, N=16, gate=True, mask=[5000, 8192], chunk=256)
+    inps = [_edge(**case, seed=s) for s in (11, 12, 13, 14)]
+    pinned = []
+    for inp in inps:
+        t = W.to_torch(inp, "cpu")
+        pinned.append({k: (v.pin_memory() if isinstance(v, torch.Tensor) else v)
+                       for k, v in t.items()})
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    need = S.host_workspace_bytes(2, 8192, 64, 16, dtype="f32", has_D=True, gate=True, mask=True,
+                                  chunk_len=256)
+    wss = [torch.empty(need, dtype=torch.uint8, device="cuda") for _ in streams]
+    outs = []
+    for k, p in enumerate(pinned):
+        outs.append(S.scan_fwd_host(p["x"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                                    p["valid_len"], chunk_len=256, workspace=wss[k % 2],
+                                    stream=streams[k % 2]))
+    torch.cuda.synchronize()
+    for inp, (y_h, s_h) in zip(inps, outs):
+        y_d, s_d = run_gpu(inp, time_segments=1)
+        assert np.array_equal(to_f64(y_h), y_d)
+        assert np.array_equal(to_f64(s_h), s_d)
+
+
 def test_stream_argument_is_respected():
     inp = W.make_inputs(SMALL["w2-fp32"])
     t = W.to_torch(inp, "cuda")
