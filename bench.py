@@ -30,7 +30,7 @@ UNIT = "elements/s"
 # Nominal per-SM unit rates of GB300 (sm_103a): MUFU ex2 32 lanes/clk/SM, fp32
 # FMA 128 lanes/clk/SM.  Used only when the probe kernels cannot run; the
 # roofline normally takes the rates measured on the GPU by unit_rates().
-NOMINAL_RATES = {"ex2_per_clk_sm": 32.0, "fp32_per_clk_sm": 128.0}
+NOMINAL_RATES = {"ex2_per_clk_sm": 32.0, "fp32_per_clk_sm": 128.0, "lds_bytes_per_clk_sm": 128.0}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}
 
 
@@ -42,10 +42,10 @@ def load_peaks() -> tuple[dict, str]:
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def measured_traffic(kernel: str, workload: str) -> int | None:
-    """DRAM bytes (read + write) per launch from an ncu capture recorded in
-    profiles/traffic.json, if that capture was taken on the kernel sources as
-    they are now (sha256 of each listed file); None otherwise."""
+def measured_capture(kernel: str, workload: str) -> dict | None:
+    """The ncu capture of one launch recorded in profiles/traffic.json for this
+    kernel and workload, if it was taken on the kernel sources as they are now
+    (sha256 of each listed file); None otherwise."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -62,8 +62,33 @@ def measured_traffic(kernel: str, workload: str) -> int | None:
                 ok = False
                 break
         if ok:
-            return int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
+            return e
     return None
+
+
+def measured_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes (read + write) per launch from the ncu capture of this kernel
+    and workload (measured_capture); None without a current capture."""
+    e = measured_capture(kernel, workload)
+    return None if e is None else int(e["dram_read_bytes"]) + int(e["dram_write_bytes"])
+
+
+def smem_port(kernel: str, workload: str, t_meas: float, rates: dict, sms: int,
+              sm_mhz: float) -> dict | None:
+    """The shared-memory port floor of a launch: ncu's shared-memory wavefronts
+    (128 bytes each) of the current capture, delivered at the measured 16-byte
+    load rate, with the CTAs spread evenly over the SMs (the busiest SM holds
+    ceil(grid / SMs) of them).  `frac` = floor / measured time.  None without a
+    current capture that counted the wavefronts."""
+    e = measured_capture(kernel, workload)
+    if e is None or "smem_wavefronts" not in e or "grid" not in e:
+        return None
+    wf, grid = float(e["smem_wavefronts"]), int(e["grid"])
+    per_sm = -(-grid // sms) * wf / grid
+    rate = float(rates.get("lds_bytes_per_clk_sm", NOMINAL_RATES["lds_bytes_per_clk_sm"]))
+    floor_s = per_sm * 128.0 / rate / (sm_mhz * 1e6)
+    return {"wavefronts": int(wf), "grid": grid, "lds_bytes_per_clk_sm": rate,
+            "floor_us": floor_s * 1e6, "frac": floor_s / t_meas}
 
 
 def algorithmic_counts(w, inp) -> dict:
@@ -106,10 +131,15 @@ def unit_rates() -> tuple[dict, str]:
                                      ctypes.byref(n))
         if rc != 0 or not (e.value > 0 and f.value > 0 and f2.value > 0):
             raise RuntimeError(f"probe status {rc}")
+        ld, ldb = ctypes.c_double(), ctypes.c_double()
+        rc = lib.ssmprobe_lds_rates(ctypes.byref(ld), ctypes.byref(ldb))
+        if rc != 0 or not (ld.value > 0 and ldb.value > 0):
+            raise RuntimeError(f"lds probe status {rc}")
     except Exception as ex:  # no GPU, no compiler: the nominal figures, said so
         return dict(NOMINAL_RATES, error=str(ex)[:80]), "nominal"
     return {"ex2_per_clk_sm": e.value, "fp32_per_clk_sm": max(f.value, f2.value),
-            "ffma_per_clk_sm": f.value, "ffma2_lanes_per_clk_sm": f2.value}, "measured"
+            "ffma_per_clk_sm": f.value, "ffma2_lanes_per_clk_sm": f2.value,
+            "lds_bytes_per_clk_sm": ld.value, "lds_bcast_bytes_per_clk_sm": ldb.value}, "measured"
 
 
 def roof(counts, peaks, sms, sm_mhz, rates=NOMINAL_RATES) -> dict:
@@ -734,6 +764,7 @@ def bwd_main(args):
     rates, rates_src = unit_rates()
     roofline_ = roofline(c, ms * 1e-3, peaks, rates, sms, mhz)
     roofline_.update({"traffic": measured_traffic("bwd", w.name), "kernel": "bwd",
+                      "smem_port": smem_port("bwd", w.name, ms * 1e-3, rates, sms, mhz),
                       "peak_source": f"{peaks_src} HBM copy GB/s; {rates_src} unit rates "
                                      f"{_rates_text(rates)} x {sms} SMs x {mhz:.0f} MHz"})
     # end to end: the backward's inputs in from pinned host memory, every gradient out
@@ -1207,6 +1238,8 @@ def main():
     rl = roofline(counts, ms * 1e-3, peaks, rates, sms, sm_mhz_peak)
     rl.update({
         "traffic": measured_traffic(S.kernel_name(res_kernel), w.name),
+        "smem_port": smem_port(S.kernel_name(res_kernel), w.name, ms * 1e-3, rates, sms,
+                               sm_mhz_peak),
         "peak_source": peak_text, "unit_rates": rates,
         "kernel": S.kernel_name(res_kernel),
         "warps_per_block": args.warps_per_block, "states_per_lane": args.states_per_lane,
@@ -1233,7 +1266,9 @@ def main():
                 "kernel": S.kernel_name(kk), "clocks": rk["clocks"],
                 "roofline": dict({k: rlk[k] for k in ("bound", "achieved", "peak", "unit",
                                                       "frac", "frac_of_roof", "roof_us")},
-                                 traffic=measured_traffic(S.kernel_name(kk), wk.name)),
+                                 traffic=measured_traffic(S.kernel_name(kk), wk.name),
+                                 smem_port=smem_port(S.kernel_name(kk), wk.name,
+                                                     rk["ms"] * 1e-3, rates, sms, sm_mhz_peak)),
                 "gpu_launches": rk["launches"]}
             del rk, ik
             torch.cuda.empty_cache()

@@ -58,7 +58,7 @@ def up_to_date() -> bool:
 
 
 def build_probe(force: bool = False) -> str:
-    """libssmprobe.so: the MUFU ex2 and fp32 FMA throughput probes."""
+    """libssmprobe.so: the MUFU ex2, fp32 FMA and shared-memory load rate probes."""
     if (not force and os.path.exists(PROBE_LIB)
             and os.path.getmtime(PROBE_LIB) >= max(os.path.getmtime(PROBE_SRC),
                                                    os.path.getmtime(os.path.abspath(__file__)))):

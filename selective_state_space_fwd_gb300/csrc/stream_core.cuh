@@ -251,14 +251,32 @@ constexpr bool phase_ok(int l0, int n, int R, F offset) {
     }
   return true;
 }
-// Stride (floats) between the state groups of a partial row: compute lane
-// (cg = lane / NG, sg = lane % NG) writes R floats at sg * PS + cg * R.
+// Lane layout of the recurrence: lane l holds state group lane_sg of channel
+// group lane_cg.  With two channels per lane the two lanes of each pair share
+// a state group, so that a warp's loads of its B and C slices (16 or 8 bytes
+// per lane) cost half the shared-memory wavefronts of the layout whose
+// neighbouring lanes read different slices (measured on GB300: 2 against 4 for
+// 16-byte loads), while the delta and x loads of the channel groups keep their
+// single-pass cost.  With four channels per lane that layout would need a
+// partial buffer over its size limit to stay free of bank conflicts, so those
+// shapes keep state groups in consecutive lanes.
+__host__ __device__ constexpr int lane_sg(int l, int NG, int R) {
+  return R == 2 ? (l >> 1) % NG : l % NG;
+}
+__host__ __device__ constexpr int lane_cg(int l, int NG, int R) {
+  return R == 2 ? (l / (2 * NG)) * 2 + (l & 1) : l / NG;
+}
+
+// Stride (floats) between the state groups of a partial row: compute lane l
+// writes R floats at lane_sg * PS + lane_cg * R.
 constexpr int pad_ps(int NG, int CW, int R) {
   for (int pad = 0; pad < 32; pad += 4) {
     const int ps = CW + pad;
     bool ok = true;
     for (int l0 = 0; l0 < 32; l0 += 32 / R)
-      ok = ok && phase_ok(l0, 32 / R, R, [&](int l) { return (l % NG) * ps + (l / NG) * R; });
+      ok = ok && phase_ok(l0, 32 / R, R, [&](int l) {
+             return lane_sg(l, NG, R) * ps + lane_cg(l, NG, R) * R;
+           });
     if (ok) return ps;
   }
   return CW;
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(128, 1)
   const int seg = static_cast<int>(row % p.n_seg);
   if (K::AGG && seg == p.n_seg - 1) return;  // the last segment's aggregate is not needed
   const int d0 = static_cast<int>((blockIdx.x % n_cb) * cpc);
-  const int cg = lane / NG, sg = lane % NG;
+  const int cg = lane_cg(lane, NG, R), sg = lane_sg(lane, NG, R);
   const int dw = d0 + warp * CW;       // the warp's first channel
   const int64_t dl = dw + cg * R;      // the lane's first channel
   const bool d_ok = dl < p.dim;        // all R channels valid (dim is a multiple of R)

@@ -5,6 +5,11 @@
 //   ex2   : ex2.approx.ftz.f32 on the MUFU unit (one per decay exp(delta A))
 //   ffma  : fma.rn.f32 on the fp32 pipe
 //   ffma2 : fma.rn.f32x2 on the fp32 pipe (two lanes of work per instruction)
+//   lds   : 16-byte shared-memory loads into registers, every lane its own
+//           address (conflict-free), and the same with one address per warp
+//           (a broadcast); the rate is bytes written to registers per clock,
+//           the delivery that bounds kernels whose threads read their
+//           operands from shared tiles
 //
 // One CTA of 1024 threads per SM (a large dynamic shared-memory request keeps
 // a second CTA off the SM).  Every thread runs 8 independent dependency chains
@@ -63,6 +68,74 @@ __global__ void __launch_bounds__(kThreads, 1) rate_kernel(int iters, float seed
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// 16-byte shared-memory loads: kChains independent loads per iteration, each
+// folded into an integer checksum.  The loads are ld.volatile (a plain load
+// from an unchanged address could be hoisted out of the loop by the assembler,
+// inline asm or not).  BCAST 0: lane l reads 16 bytes at 16 l of its chain's 512-byte
+// row (each quarter warp covers the 32 banks once); BCAST 1: every lane of a
+// warp reads the same 16 bytes.  Addresses stay inside 32 KB of the CTA's
+// dynamic shared memory.
+template <int BCAST>
+__global__ void __launch_bounds__(kThreads, 1) lds_kernel(int iters, long long* cycles,
+                                                          unsigned* sink) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 32 * 1024 / 4; i += kThreads) reinterpret_cast<unsigned*>(sm)[i] = i;
+  __syncthreads();
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+  uint32_t off[kChains];
+#pragma unroll
+  for (int i = 0; i < kChains; ++i)  // row (warp + 4 i) mod 64 of 512 bytes
+    off[i] = base + ((warp + 4 * i) & 63) * 512 + (BCAST ? 0 : lane * 16);
+  unsigned acc0 = 0, acc1 = 0;
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < kChains; ++i) {
+      unsigned a, b, c, d;
+      asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(off[i]));
+      acc0 ^= a ^ b;
+      acc1 ^= c ^ d;
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  if ((acc0 ^ acc1) == 0x9e3779b9u) sink[tid] = acc0;  // keeps the loads' results live
+  if (tid == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+// median over the SMs of the per-CTA cycle counts (sorts h in place)
+double median_cycles(long long* h, int n) {
+  for (int i = 1; i < n; ++i)
+    for (int j = i; j > 0 && h[j - 1] > h[j]; --j) {
+      const long long t = h[j];
+      h[j] = h[j - 1];
+      h[j - 1] = t;
+    }
+  return static_cast<double>(h[n / 2]);
+}
+
+template <int BCAST>
+int run_lds(int sms, int iters, long long* d_cycles, unsigned* d_sink, double* out) {
+  const int smem = 120 * 1024;  // one CTA per SM, as for the arithmetic probes
+  if (cudaFuncSetAttribute(lds_kernel<BCAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return 1;
+  lds_kernel<BCAST><<<sms, kThreads, smem>>>(iters, d_cycles, d_sink);  // warm-up
+  lds_kernel<BCAST><<<sms, kThreads, smem>>>(iters, d_cycles, d_sink);
+  if (cudaDeviceSynchronize() != cudaSuccess) return 2;
+  long long* h = new long long[sms];
+  if (cudaMemcpy(h, d_cycles, sizeof(long long) * sms, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    delete[] h;
+    return 3;
+  }
+  const double cyc = median_cycles(h, sms);
+  delete[] h;
+  *out = double(kThreads) * kChains * iters * 16.0 / cyc;  // register bytes per clock
+  return 0;
+}
+
 template <int KIND>
 int run(int sms, int iters, long long* d_cycles, float* d_sink, double* out) {
   const int smem = 120 * 1024;  // more than half an SM's shared memory: one CTA per SM
@@ -78,13 +151,7 @@ int run(int sms, int iters, long long* d_cycles, float* d_sink, double* out) {
     return 3;
   }
   // median over the SMs of lane-operations per clock
-  for (int i = 1; i < sms; ++i)
-    for (int j = i; j > 0 && h[j - 1] > h[j]; --j) {
-      const long long t = h[j];
-      h[j] = h[j - 1];
-      h[j - 1] = t;
-    }
-  const double cyc = static_cast<double>(h[sms / 2]);
+  const double cyc = median_cycles(h, sms);
   delete[] h;
   const double lanes_per_op = KIND == 2 ? 2.0 : 1.0;
   *out = double(kThreads) * kChains * iters * lanes_per_op / cyc;
@@ -115,6 +182,28 @@ int ssmprobe_unit_rates(double* ex2_per_clk, double* ffma_per_clk, double* ffma2
   int rc = run<0>(n, 4096, d_cycles, d_sink, ex2_per_clk);
   if (rc == 0) rc = run<1>(n, 8192, d_cycles, d_sink, ffma_per_clk);
   if (rc == 0) rc = run<2>(n, 4096, d_cycles, d_sink, ffma2_per_clk);
+  cudaFree(d_cycles);
+  cudaFree(d_sink);
+  return rc;
+}
+
+// Measures, on the current device, the bytes per SM clock that 16-byte
+// shared-memory loads write into registers: every lane its own address
+// (conflict-free) and one address per warp (broadcast).  Returns 0 on success.
+int ssmprobe_lds_rates(double* bytes_per_clk, double* bcast_bytes_per_clk) {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 10;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 11;
+  long long* d_cycles = nullptr;
+  unsigned* d_sink = nullptr;
+  if (cudaMalloc(&d_cycles, sizeof(long long) * n) != cudaSuccess) return 12;
+  if (cudaMalloc(&d_sink, sizeof(unsigned) * kThreads) != cudaSuccess) {
+    cudaFree(d_cycles);
+    return 12;
+  }
+  int rc = run_lds<0>(n, 2048, d_cycles, d_sink, bytes_per_clk);
+  if (rc == 0) rc = run_lds<1>(n, 2048, d_cycles, d_sink, bcast_bytes_per_clk);
   cudaFree(d_cycles);
   cudaFree(d_sink);
   return rc;
