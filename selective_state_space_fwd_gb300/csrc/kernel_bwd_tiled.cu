@@ -193,7 +193,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = static_cast<int>(K::RANK && rows_ranked(p.fwd) ? row_of_rank(p.fwd, blockIdx.x / nblk)
                                                                 : blockIdx.x / nblk);
   const int d0 = static_cast<int>((blockIdx.x % nblk) * CPB);
-  const int ch = lane / NL, sl = lane % NL, n0 = sl * 4;
+  // The two lanes of each pair share a state group, so that a warp's 16-byte
+  // loads of its B and C slices cost half the shared-memory wavefronts of a
+  // layout whose neighbouring lanes read different slices; a channel's NL
+  // lanes then differ in lane bits 1 .. log2(NL).
+  const int sl = (lane >> 1) % NL, ch = (lane / (2 * NL)) * 2 + (lane & 1), n0 = sl * 4;
   const int cc = warp * CWB + ch;  // the thread's channel within the CTA's block
   const bool ok = d0 + cc < D_;
   const int64_t dd = ok ? d0 + cc : 0;
@@ -429,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         float pA = hsum(pA2), S1 = hsum(S12), yp = hsum(yp2);
 #pragma unroll
-        for (int msk = 1; msk < NL; msk *= 2) {
+        for (int msk = 2; msk < 2 * NL; msk *= 2) {  // over the channel's lanes
           pA += __shfl_xor_sync(0xffffffffu, pA, msk);
           S1 += __shfl_xor_sync(0xffffffffu, S1, msk);
           if constexpr (K::GATE) yp += __shfl_xor_sync(0xffffffffu, yp, msk);
