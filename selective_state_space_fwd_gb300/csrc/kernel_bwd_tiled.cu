@@ -18,9 +18,12 @@
 // * dx, d delta and dz of a piece are written to shared-memory tiles and
 //   leave by TMA store.
 // * dB and dC (sums over channels) are reduced in two levels before any
-//   atomic: within the warp through a transposed shared-memory buffer, then
-//   across the CTA's warps once per piece, ending in one 16-byte vector
-//   atomic per four (t, n) per CTA.
+//   atomic: within the warp, then across the CTA's warps once per piece,
+//   ending in one 16-byte vector atomic per four (t, n) per CTA.  The warp
+//   sum is a shuffle reduce-scatter over the lane bits that select the
+//   channel; with the gate it goes through a transposed shared-memory buffer
+//   instead (measured on GB300: the shuffles took fp32 workloads 6-16 % off,
+//   but made the bf16 gated ones 2-3 % slower).
 //
 // Work split: 4 consecutive states per thread (two f32x2 pairs), N / 4
 // threads per channel, 128 / N channels per warp, four warps per CTA, all of
@@ -70,17 +73,20 @@ struct Cfg {
   static constexpr int TX2 = STAGE;          // pieces: everything
   static constexpr int NOUT = GATE ? 3 : 2;  // dx, d delta (, dz)
   static constexpr int OUTB = kK * CPB * ES;
-  static constexpr int XS = 2 * N + 16;      // row stride (floats) of the transpose buffer
-  static constexpr int XBUF = CWB * XS * 4;  // bytes per warp
   static constexpr int OPL = 2 * N / 32;     // dB/dC outputs per lane in the warp sum
+  static constexpr int LCW = CWB == 8 ? 3 : (CWB == 4 ? 2 : 1);  // log2 of the channels per warp
+  static constexpr bool XPOSE = GATE;        // warp sum through the transpose buffer
+  static constexpr int XS = 2 * N + 16;      // row stride (floats) of the transpose buffer
+  static constexpr int XBUF = XPOSE ? CWB * XS * 4 : 0;  // bytes per warp
   static constexpr int REDB = kK * kW * 2 * N * 4;
   static_assert(N % 16 == 0 && N <= 64, "16, 32 or 64 states");
   static_assert(ACT % 128 == 0 && ROW % 128 == 0 && XBUF % 128 == 0, "tile alignment");
+  static_assert((1 << LCW) == CWB && 8 >> LCW == OPL, "warp sum of dB, dC");
 };
 
 // Shared memory of a CTA: the ring, the checkpoints (one 16-byte slot per
-// thread and piece), the output tiles, the warps' transpose buffers, the
-// CTA's dB/dC partial sums, the mbarriers.
+// thread and piece), the output tiles, the warps' transpose buffers (gate
+// instances), the CTA's dB/dC partial sums, the mbarriers.
 template <class K>
 size_t smem_bytes(int stages, int nck) {
   return size_t(stages) * K::STAGE + size_t(nck) * kThreads * 16 + K::NOUT * K::OUTB +
@@ -450,28 +456,56 @@ __global__ void __launch_bounds__(kThreads, 2)
           put(o_ddt + k * CPB + cc, g_dt);
           if constexpr (K::GATE) put(o_dz + k * CPB + cc, g_dz);
         }
-        // dB, dC summed over the warp's channels: each lane stores its four
-        // of each, then lane o sums output o (and o + 32, ...) over them
-        {
+        // dB, dC summed over the warp's channels by a reduce-scatter: in each
+        // round over one channel bit of the lane (lane bit 0, then the bits
+        // from log2(2 NL) up) a lane keeps one half of its values, adds the
+        // partner's copy of that half and hands over the other half.  The
+        // lane ends with OPL outputs of its state group, from position o of
+        // (dB n0 .. n0+3, dC n0 .. n0+3).
+        if constexpr (K::XPOSE) {
+          // through the transpose buffer: each lane stores its four of each,
+          // then lane o sums output o (and o + 32, ...) over the channels
           const float2 b0 = upk2(db2[0]), b1 = upk2(db2[1]);
           const float2 c0 = upk2(dc2[0]), c1 = upk2(dc2[1]);
           *reinterpret_cast<float4*>(xbuf + ch * K::XS + n0) = make_float4(b0.x, b0.y, b1.x, b1.y);
           *reinterpret_cast<float4*>(xbuf + ch * K::XS + N + n0) =
               make_float4(c0.x, c0.y, c1.x, c1.y);
+          __syncwarp();
+#pragma unroll
+          for (int o = 0; o < K::OPL; ++o) {
+            float v[CWB];  // summed as a tree: short dependency chains
+#pragma unroll
+            for (int c2 = 0; c2 < CWB; ++c2) v[c2] = xbuf[c2 * K::XS + lane + 32 * o];
+#pragma unroll
+            for (int w = CWB / 2; w >= 1; w /= 2)
+#pragma unroll
+              for (int i = 0; i < w; ++i) v[i] += v[i + w];
+            red[(k * kW + warp) * 2 * N + lane + 32 * o] = v[0];
+          }
+          __syncwarp();
+        } else {
+          const float2 b0 = upk2(db2[0]), b1 = upk2(db2[1]);
+          const float2 c0 = upk2(dc2[0]), c1 = upk2(dc2[1]);
+          float v[8] = {b0.x, b0.y, b1.x, b1.y, c0.x, c0.y, c1.x, c1.y};
+          int o = 0;
+#pragma unroll
+          for (int r = 0; r < K::LCW; ++r) {
+            const int w = 8 >> r, m = r == 0 ? 1 : (2 * NL) << (r - 1);
+            const bool hi = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < w / 2; ++i) {
+              const float give = hi ? v[i] : v[i + w / 2];
+              const float keep = hi ? v[i + w / 2] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+            }
+            o += hi ? w / 2 : 0;
+          }
+#pragma unroll
+          for (int j = 0; j < K::OPL; ++j) {
+            const int q = o + j;  // 0..3: dB of state n0 + q; 4..7: dC of state n0 + q - 4
+            red[(k * kW + warp) * 2 * N + (q < 4 ? n0 + q : N + n0 + q - 4)] = v[j];
+          }
         }
-        __syncwarp();
-#pragma unroll
-        for (int o = 0; o < K::OPL; ++o) {
-          float v[CWB];  // summed as a tree: short dependency chains
-#pragma unroll
-          for (int c2 = 0; c2 < CWB; ++c2) v[c2] = xbuf[c2 * K::XS + lane + 32 * o];
-#pragma unroll
-          for (int w = CWB / 2; w >= 1; w /= 2)
-#pragma unroll
-            for (int i = 0; i < w; ++i) v[i] += v[i + w];
-          red[(k * kW + warp) * 2 * N + lane + 32 * o] = v[0];
-        }
-        __syncwarp();
       }
       fence_async_smem();  // the output tiles go out by TMA
       release();
