@@ -53,6 +53,40 @@ constexpr int kW = 4;         // warps per CTA
 constexpr int kThreads = 32 * kW;
 constexpr int kSmemPerSm = 228 * 1024;
 
+// Lane layout with NL lanes per channel: lane l holds state group bwd_sl of
+// channel bwd_ch of its warp.  The two lanes of each pair share a state group
+// (a warp's 16-byte loads of its B and C slices then cost half the
+// shared-memory wavefronts), so a channel's lanes differ in lane bits 1 ..
+// log2(NL) and the channels in lane bit 0 and the bits from log2(2 NL) up;
+// round r of the warp sum of dB, dC pairs lanes across channel bit
+// sum_mask(r).
+__host__ __device__ constexpr int bwd_sl(int l, int NL) { return (l >> 1) % NL; }
+__host__ __device__ constexpr int bwd_ch(int l, int NL) { return (l / (2 * NL)) * 2 + (l & 1); }
+__host__ __device__ constexpr int sum_mask(int r, int NL) { return r == 0 ? 1 : (2 * NL) << (r - 1); }
+// The layout gives each (channel, state group) to one lane, and the LCW
+// rounds pair lanes of one state group and different channels, reaching every
+// channel of the warp.
+constexpr bool sum_masks_ok(int NL, int LCW) {
+  const int CW = 32 / NL;
+  bool seen[32] = {};
+  for (int l = 0; l < 32; ++l) {
+    const int sl = bwd_sl(l, NL), ch = bwd_ch(l, NL);
+    if (sl >= NL || ch >= CW || seen[ch * NL + sl]) return false;
+    seen[ch * NL + sl] = true;
+    bool reach[32] = {};
+    for (int sub = 0; sub < (1 << LCW); ++sub) {
+      int p = l;
+      for (int r = 0; r < LCW; ++r)
+        if (sub >> r & 1) p ^= sum_mask(r, NL);
+      if (p < 0 || p >= 32 || bwd_sl(p, NL) != sl) return false;
+      reach[bwd_ch(p, NL)] = true;
+    }
+    for (int c = 0; c < CW; ++c)
+      if (!reach[c]) return false;
+  }
+  return true;
+}
+
 template <int N_, typename T_, bool GATE_, bool RANK_ = false>
 struct Cfg {
   static constexpr int N = N_;
@@ -82,6 +116,7 @@ struct Cfg {
   static_assert(N % 16 == 0 && N <= 64, "16, 32 or 64 states");
   static_assert(ACT % 128 == 0 && ROW % 128 == 0 && XBUF % 128 == 0, "tile alignment");
   static_assert((1 << LCW) == CWB && 8 >> LCW == OPL, "warp sum of dB, dC");
+  static_assert(sum_masks_ok(NL, LCW), "lane layout and the masks of the warp sum");
 };
 
 // Shared memory of a CTA: the ring, the checkpoints (one 16-byte slot per
@@ -199,11 +234,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = static_cast<int>(K::RANK && rows_ranked(p.fwd) ? row_of_rank(p.fwd, blockIdx.x / nblk)
                                                                 : blockIdx.x / nblk);
   const int d0 = static_cast<int>((blockIdx.x % nblk) * CPB);
-  // The two lanes of each pair share a state group, so that a warp's 16-byte
-  // loads of its B and C slices cost half the shared-memory wavefronts of a
-  // layout whose neighbouring lanes read different slices; a channel's NL
-  // lanes then differ in lane bits 1 .. log2(NL).
-  const int sl = (lane >> 1) % NL, ch = (lane / (2 * NL)) * 2 + (lane & 1), n0 = sl * 4;
+  const int sl = bwd_sl(lane, NL), ch = bwd_ch(lane, NL), n0 = sl * 4;  // lane layout above
   const int cc = warp * CWB + ch;  // the thread's channel within the CTA's block
   const bool ok = d0 + cc < D_;
   const int64_t dd = ok ? d0 + cc : 0;
@@ -490,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           int o = 0;
 #pragma unroll
           for (int r = 0; r < K::LCW; ++r) {
-            const int w = 8 >> r, m = r == 0 ? 1 : (2 * NL) << (r - 1);
+            const int w = 8 >> r, m = sum_mask(r, NL);
             const bool hi = (lane & m) != 0;
 #pragma unroll
             for (int i = 0; i < w / 2; ++i) {

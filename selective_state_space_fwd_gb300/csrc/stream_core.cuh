@@ -266,6 +266,17 @@ __host__ __device__ constexpr int lane_sg(int l, int NG, int R) {
 __host__ __device__ constexpr int lane_cg(int l, int NG, int R) {
   return R == 2 ? (l / (2 * NG)) * 2 + (l & 1) : l / NG;
 }
+// The layout gives each (channel group, state group) of a warp to exactly one lane.
+constexpr bool lane_layout_ok(int NG, int R) {
+  bool seen[32] = {};
+  for (int l = 0; l < 32; ++l) {
+    const int sg = lane_sg(l, NG, R), cg = lane_cg(l, NG, R);
+    if (sg < 0 || sg >= NG || cg < 0 || cg >= 32 / NG) return false;
+    if (seen[cg * NG + sg]) return false;
+    seen[cg * NG + sg] = true;
+  }
+  return true;
+}
 
 // Stride (floats) between the state groups of a partial row: compute lane l
 // writes R floats at lane_sg * PS + lane_cg * R.
@@ -343,6 +354,7 @@ struct Cfg {
   static constexpr int SLAB = T * CW * ES;     // one warp's [T x CW] tile of one tensor
   static constexpr int ROWT = T * N * ES;      // [T x N] tile of B or C
   static_assert(R == 2 || R == 4, "two or four channels per lane");
+  static_assert(lane_layout_ok(NG, R), "lane layout");
   static_assert(G >= 2 && N % G == 0 && NG <= 16 && (NG & (NG - 1)) == 0, "state groups");
   static_assert((CW * ES) % 16 == 0 && (N * ES) % 16 == 0, "TMA box rows are 16-byte multiples");
   static_assert(T % M == 0 && M % (2 * U) == 0 && M % NG == 0, "tile steps");
