@@ -292,12 +292,18 @@ __global__ void seg_carry_kernel(const ScanParams p) {
 
 int64_t stream_auto_segments(const ScanParams& p, StreamShape sh) {
   // Split only when the rows leave most schedulers without a warp: then aim
-  // at two warps per scheduler, with segments of at least 256 steps (the
+  // at two warps per scheduler for 4 states per lane, four for 8 (twice the
+  // dependent work per warp-step), with segments of at least 256 steps (the
   // aggregate pass costs about half a pass over all but the last segment).
+  // Measured on GB300: b1 x L65536 x D256 x N16 (4 states per lane) is
+  // fastest at two warps per scheduler (74 segments: 154 us; 147: 162 us);
+  // b2 x L32768 x D512 x N64 (8 per lane) took 1127 us at two, 1014 us at
+  // about four (20 segments) and 999 us at 32 segments.
   const int64_t warps = stream_grid(p, sh) * sh.wpc;
   const int64_t schedulers = 4 * int64_t(stream::sm_count());
   if (warps * 2 >= schedulers) return 1;
-  int64_t segs = (2 * schedulers + warps - 1) / warps;
+  const int64_t per_scheduler = sh.g >= 8 ? 4 : 2;
+  int64_t segs = (per_scheduler * schedulers + warps - 1) / warps;
   const int64_t most = p.seqlen / 256;
   if (segs > most) segs = most;
   return segs < 1 ? 1 : segs;
