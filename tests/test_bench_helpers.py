@@ -109,3 +109,37 @@ def test_slice_rows_is_pure_indexing():
     assert np.array_equal(s["x"], inp["x"][1:3]) and np.array_equal(s["B"], inp["B"][1:3])
     assert np.array_equal(s["valid_len"], inp["valid_len"][1:3])
     assert s["A"] is inp["A"] and s["D"] is inp["D"]
+
+
+def test_smem_port_floor_by_hand(monkeypatch):
+    """The shared-memory port floor: the capture's wavefronts of 128 bytes,
+    the busiest SM holding ceil(grid / SMs) of the CTAs, at the load rate."""
+    entry = {"smem_wavefronts": 152 * 4 * 1000, "grid": 152 * 4 - 1}
+    monkeypatch.setattr(bench, "measured_capture", lambda k, w: entry)
+    rates = {"lds_bytes_per_clk_sm": 128.0}
+    r = bench.smem_port("stream", "any", 1e-3, rates, 152, 1000.0)
+    per_cta = entry["smem_wavefronts"] / entry["grid"]
+    floor_s = 4 * per_cta / 1e9  # four CTAs on the busiest SM, one wavefront per clock at 1 GHz
+    assert r["floor_us"] == pytest.approx(floor_s * 1e6)
+    assert r["frac"] == pytest.approx(floor_s / 1e-3)
+    assert r["grid"] == entry["grid"] and r["wavefronts"] == entry["smem_wavefronts"]
+    # twice the load rate halves the floor
+    r2 = bench.smem_port("stream", "any", 1e-3, {"lds_bytes_per_clk_sm": 256.0}, 152, 1000.0)
+    assert r2["floor_us"] == pytest.approx(r["floor_us"] / 2)
+
+
+def test_smem_port_needs_a_capture_with_wavefronts(monkeypatch):
+    assert bench.smem_port("stream", "no-such-workload", 1e-3, {}, 152, 2070.0) is None
+    monkeypatch.setattr(bench, "measured_capture", lambda k, w: {"dram_read_bytes": 1})
+    assert bench.smem_port("stream", "any", 1e-3, {}, 152, 2070.0) is None
+
+
+def test_committed_captures_are_current():
+    """Every capture recorded in profiles/traffic.json was taken on the kernel
+    sources as they are (otherwise the bench would report no traffic)."""
+    import json
+    import os
+    entries = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    assert entries
+    for e in entries:
+        assert bench.measured_capture(e["kernel"], e["workload"]) is not None, e["workload"]
