@@ -105,6 +105,75 @@ __global__ void __launch_bounds__(kThreads, 1) lds_kernel(int iters, long long* 
   if (tid == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// Lane l's byte offset, inside a 512-byte row, of the address patterns whose
+// cost the scan kernels' lane layouts depend on (W = 16 or 8 bytes per lane):
+//   0  every lane its own 16 bytes
+//   1  one address for the warp (broadcast)
+//   2  B/C slice of 4 states, state groups in consecutive lanes (l mod 4)
+//   3  B/C slice of 4 states, the two lanes of a pair sharing a state group
+//   4  first chunk of an 8-state B/C slice, consecutive lanes, rotated chunks
+//   5  the same with pair-shared state groups
+//   6  8-byte delta/x pair of 4-lane channel groups (l / 4)
+//   7  8-byte delta/x pair of the pair-shared layout's channel groups
+__device__ __forceinline__ uint32_t pattern_offset(int P, int l) {
+  switch (P) {
+    case 0: return l * 16;
+    case 1: return 0;
+    case 2: return (l & 3) * 16;
+    case 3: return ((l >> 1) & 3) * 16;
+    case 4: { const int sg = l & 7; return (2 * sg + ((sg >> 2) & 1)) * 16; }
+    case 5: { const int sg = (l >> 1) & 7; return (2 * sg + ((sg >> 2) & 1)) * 16; }
+    case 6: return (l >> 2) * 8;
+    case 7: return (((l >> 3) << 1) | (l & 1)) * 8;
+    default: return 0;
+  }
+}
+constexpr int kPatterns = 8;
+
+// Cycles per warp-wide load of pattern P (the shared-memory wavefronts it
+// takes): kChains independent volatile loads per iteration, 16 bytes per lane
+// for patterns 0-5 and 8 bytes for 6-7, rows inside 32 KB of the CTA's
+// shared memory.
+__global__ void __launch_bounds__(kThreads, 1) pattern_kernel(int P, int iters, long long* cycles,
+                                                              unsigned* sink) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 32 * 1024 / 4; i += kThreads) reinterpret_cast<unsigned*>(sm)[i] = i;
+  __syncthreads();
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+  uint32_t off[kChains];
+#pragma unroll
+  for (int i = 0; i < kChains; ++i) off[i] = base + ((warp + 4 * i) & 63) * 512 + pattern_offset(P, lane);
+  unsigned acc0 = 0, acc1 = 0;
+  const long long t0 = clock64();
+  if (P < 6) {
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int i = 0; i < kChains; ++i) {
+        unsigned a, b, c, d;
+        asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(off[i]));
+        acc0 ^= a ^ b;
+        acc1 ^= c ^ d;
+      }
+    }
+  } else {
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int i = 0; i < kChains; ++i) {
+        unsigned a, b;
+        asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(off[i]));
+        acc0 ^= a;
+        acc1 ^= b;
+      }
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  if ((acc0 ^ acc1) == 0x9e3779b9u) sink[tid] = acc0;
+  if (tid == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
 // median over the SMs of the per-CTA cycle counts (sorts h in place)
 double median_cycles(long long* h, int n) {
   for (int i = 1; i < n; ++i)
@@ -182,6 +251,43 @@ int ssmprobe_unit_rates(double* ex2_per_clk, double* ffma_per_clk, double* ffma2
   int rc = run<0>(n, 4096, d_cycles, d_sink, ex2_per_clk);
   if (rc == 0) rc = run<1>(n, 8192, d_cycles, d_sink, ffma_per_clk);
   if (rc == 0) rc = run<2>(n, 4096, d_cycles, d_sink, ffma2_per_clk);
+  cudaFree(d_cycles);
+  cudaFree(d_sink);
+  return rc;
+}
+
+// Measures, on the current device, the cycles per warp-wide shared-memory
+// load of each address pattern of pattern_offset (out[kPatterns]).  Returns
+// 0 on success.
+int ssmprobe_lds_patterns(double* cycles_per_load, int n) {
+  if (n < kPatterns) return 13;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 10;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 11;
+  long long* d_cycles = nullptr;
+  unsigned* d_sink = nullptr;
+  if (cudaMalloc(&d_cycles, sizeof(long long) * sms) != cudaSuccess) return 12;
+  if (cudaMalloc(&d_sink, sizeof(unsigned) * kThreads) != cudaSuccess) {
+    cudaFree(d_cycles);
+    return 12;
+  }
+  const int smem = 120 * 1024, iters = 1024;
+  int rc = cudaFuncSetAttribute(pattern_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                   cudaSuccess ? 0 : 1;
+  long long* h = new long long[sms];
+  for (int P = 0; P < kPatterns && rc == 0; ++P) {
+    pattern_kernel<<<sms, kThreads, smem>>>(P, iters, d_cycles, d_sink);  // warm-up
+    pattern_kernel<<<sms, kThreads, smem>>>(P, iters, d_cycles, d_sink);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = 2; break; }
+    if (cudaMemcpy(h, d_cycles, sizeof(long long) * sms, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      rc = 3;
+      break;
+    }
+    const double warp_loads = double(kThreads / 32) * kChains * iters;
+    cycles_per_load[P] = median_cycles(h, sms) / warp_loads;
+  }
+  delete[] h;
   cudaFree(d_cycles);
   cudaFree(d_sink);
   return rc;
