@@ -1,5 +1,7 @@
 """Benchmark bookkeeping on CPU: algorithmic work counts and the roofline
 arithmetic, checked against hand-computed values for two workloads."""
+import os
+
 import numpy as np
 import pytest
 
@@ -143,3 +145,16 @@ def test_committed_captures_are_current():
     assert entries
     for e in entries:
         assert bench.measured_capture(e["kernel"], e["workload"]) is not None, e["workload"]
+
+
+def test_probe_library_exports_its_entry_points():
+    """libssmprobe.so (the roofline's unit-rate and shared-load probes) builds
+    and exports every entry the bench and the pattern script call."""
+    import ctypes
+    import shutil
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("no CUDA compiler")
+    from selective_state_space_fwd_gb300 import build as B
+    lib = ctypes.CDLL(B.build_probe())
+    for name in ("ssmprobe_unit_rates", "ssmprobe_lds_rates", "ssmprobe_lds_patterns"):
+        assert hasattr(lib, name), name
